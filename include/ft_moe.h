@@ -1,0 +1,268 @@
+/*
+ * ft_moe.h -- C ABI of the routed, quantized expert-FFN MoE layer for GB300
+ * (sm_103a).  One shared library, libft_moe.so, plain pointers and sizes.
+ *
+ * The layer, one call per step, all on one CUDA stream with no host sync:
+ *   ft_moe_route          router logits, softmax, top-k
+ *   ft_moe_resolve_slots  (layer, expert) -> cache slot or -1, q* split inside
+ *   ft_moe_fetch          copy the chosen misses from the pool into the cache
+ *   ft_moe_experts_fwd    quantized SwiGLU experts (decode: combine fused)
+ *   ft_moe_permute        token permutation by expert (prefill)
+ *   ft_moe_combine        top-k weighted sum of permuted expert rows (prefill)
+ *   ft_moe_split_q16      the q* rule alone, batched (the resolve kernel runs
+ *                         the same device function)
+ *
+ * Sources, by page title and section:
+ *   "FreeToken 딥다이브" (fiv.co.kr) -- design pattern 1 (whole-layer double
+ *     buffer for prefill), 2 (Q16 q* split inside the decode graph), 3 (-1
+ *     sentinel and masking: every (token, expert) pair computed once),
+ *     5 (slot LRU: int64 usage, global step, flat id layer*E+expert;
+ *     expert_recency picks which misses are fetched).
+ *   "FreeToken: 让消费级电脑跑起 284B MoE ..." (fengjutian.github.io) --
+ *     sec. 2 (router on the GPU), sec. 4 (one slot = one (layer, expert);
+ *     host pool is the source of truth), sec. 6 (q* = m*B_P/B_H; one kernel
+ *     does dedup, residency, q, victims and id rewrite; exact merge),
+ *     sec. 7 (banks with leading dimension layer*E+expert).
+ *   "NVMe에서 전문가(experts)를 스트리밍하여 8GB GPU에서 133GB MoE 모델
+ *     구동하기" (molayo1419.me) -- "Why this model" (three 2560x640 NVFP4
+ *     matrices per expert), engine step 1 (one block per expert:
+ *     gate|up|down|gate_scale|up_scale|down_scale), step 4 (single-token NVFP4
+ *     SwiGLU expert kernel), step 5 (whole-prompt per-layer expert batching).
+ *   "SSD 가중치층으로 35B MoE를 ..." (onedev.kr) -- "How it works":
+ *     down(silu(gate(x)) * up(x)) over int4 weights, dedup/stack/gather.
+ *
+ * Conventions (all entry points):
+ *   - Pointers named *_host are host memory; every other pointer is device
+ *     accessible memory (cudaMalloc, or pinned host memory mapped into the
+ *     device address space, e.g. the expert pool).  The caller owns all
+ *     memory; no entry point allocates or frees device memory.
+ *   - `stream` is a cudaStream_t passed as void*.  Calls only enqueue work;
+ *     none synchronises the host, so a fixed-shape sequence of calls can be
+ *     captured into a CUDA graph.
+ *   - Return value: FT_OK, or an error found on the host before anything is
+ *     enqueued (FT_ERR_INVALID: null pointer, bad size or range;
+ *     FT_ERR_UNSUPPORTED: format/shape the kernels do not implement), or
+ *     FT_ERR_CUDA when a launch fails.  ft_last_error() gives the message.
+ *   - Errors that only the device can see (an expert id outside [0, E), a
+ *     bounded wait that gave up) are recorded in the caller's int32
+ *     `dev_status` word (first error wins, 0 = fine); the caller reads it
+ *     after a synchronisation of its choosing.  dev_status may be NULL.
+ *   - bf16 tensors are passed as uint16_t bit patterns.
+ */
+#ifndef FT_MOE_H
+#define FT_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FT_API __attribute__((visibility("default")))
+#else
+#define FT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t ft_status;
+enum {
+  FT_OK = 0,
+  FT_ERR_INVALID = 1,
+  FT_ERR_UNSUPPORTED = 2,
+  FT_ERR_CUDA = 3,
+  FT_ERR_TIMEOUT = 4,   /* device: a bounded wait ran out */
+  FT_ERR_BAD_ID = 5     /* device: an expert id outside [0, E) */
+};
+
+/* Expert weight formats. */
+enum {
+  FT_INT4 = 0,   /* code q in 0..15 means (q - 8) * s; fp16 scale s per `group` K elements */
+  FT_NVFP4 = 1   /* E2M1 code * E4M3 scale per 16 K elements * fp32 per-tensor scale */
+};
+
+enum { FT_DECODE = 0, FT_PREFILL = 1 };
+enum { FT_OUT_F32 = 0, FT_OUT_BF16 = 1 };
+
+/*
+ * A bank: consecutive expert blocks (the pool indexed by flat id
+ * fid = layer*E + expert, or the cache indexed by slot).  One block holds
+ * gate [I,H] | up [I,H] | down [H,I] | gate_scale | up_scale | down_scale,
+ * matrices row-major with K contiguous, two 4-bit codes per byte (low
+ * nibble = even K).  Scales: int4 fp16 [rows, K/group]; NVFP4 E4M3 bytes
+ * [rows, K/16].  Every block starts at base + index*stride; base and stride
+ * must be multiples of 16 bytes; n_blocks is the number of blocks (kernels
+ * skip, and record FT_ERR_BAD_ID for, any index outside it).  tensor_scale
+ * (NVFP4 only) is a device
+ * array [n_fids, 3] fp32 (gate, up, down) indexed by flat id, the same array
+ * for pool and cache; NULL for int4.
+ */
+typedef struct {
+  int32_t fmt;
+  int32_t H;
+  int32_t I;
+  int32_t group;          /* int4: 32, 64 or 128; NVFP4: 16 */
+  const void* base;
+  uint64_t stride;
+  int64_t n_blocks;
+  const float* tensor_scale;
+} ft_bank;
+
+/*
+ * The global slot cache state (device arrays, caller-owned), shared by all
+ * layers.  slot_owner[S]: flat id held by the slot or -1.  map[L*E]: slot of
+ * a flat id or -1.  usage[S]: last step the slot was used, -1 when empty.
+ * recency[L*E]: last step the expert was routed.  step[1]: the global step,
+ * advanced once per resolve call.
+ */
+typedef struct {
+  int32_t L;
+  int32_t E;
+  int32_t S;
+  int32_t* slot_owner;
+  int32_t* map;
+  int64_t* usage;
+  int64_t* recency;
+  int64_t* step;
+} ft_cache_state;
+
+/* Library and error queries. */
+FT_API const char* ft_version(void);
+FT_API const char* ft_status_string(ft_status s);
+FT_API const char* ft_last_error(void);  /* message of the last failing call on this thread */
+
+/*
+ * Bytes of one expert block and the byte offsets of its six parts (off6 may
+ * be NULL).  Returns 0 for an unsupported (fmt, H, I, group).
+ */
+FT_API uint64_t ft_block_bytes(int32_t fmt, int32_t H, int32_t I, int32_t group, uint64_t* off6_host);
+
+/*
+ * Copy the int32 status word to the host (synchronous: waits for the device
+ * copy).  Use after the caller's own synchronisation point.
+ */
+FT_API ft_status ft_moe_get_status(const int32_t* dev_status, int32_t* out_host);
+
+/*
+ * ft_moe_route -- router on the GPU (FreeToken paper post, sec. 2).
+ *   logits[t,e] = sum_h x[t,h] * w_router[e,h], fp32 accumulation;
+ *   p = softmax over all E; topk_ids[t, 0..k-1] = experts by p descending,
+ *   ties to the lower id; topk_w = p at those ids (divided by their sum when
+ *   renorm != 0).
+ * x [T,H] bf16 row-major; w_router [E,H] fp32 row-major; topk_ids [T,k]
+ * int32; topk_w [T,k] fp32.  ws: device scratch of ft_moe_route_workspace(T,E)
+ * bytes (the logits).  Limits: 1 <= k <= min(E, 32), E <= 4096, H % 8 == 0.
+ * T == 0 is a no-op.
+ */
+FT_API size_t ft_moe_route_workspace(int32_t T, int32_t E);
+FT_API ft_status ft_moe_route(const uint16_t* x, int32_t T, int32_t H, const float* w_router,
+                       int32_t E, int32_t k, int32_t renorm, int32_t* topk_ids, float* topk_w,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * ft_moe_split_q16 -- the bandwidth-matched q* rule in Q16 fixed point
+ * (FreeToken deep-dive, design pattern 2; paper post, sec. 6).  For each m =
+ * num_missing[i] and phi = frac_q16 = round(65536 * B_P / B_H):
+ *   phi > 0: lo = (m*phi) >> 16; fetch lo or lo+1, whichever has the smaller
+ *            max(f*(65536-phi), (m-f)*phi), ties to lo; capped at m.
+ *   phi = 0: no cap, num_fetch = m.
+ * num_missing, num_fetch: device int32 [n].  phi outside [0, 65536] or a
+ * negative n is FT_ERR_INVALID.  Negative m gives 0.
+ */
+FT_API ft_status ft_moe_split_q16(const int32_t* num_missing, int32_t n, int32_t frac_q16,
+                           int32_t* num_fetch, void* stream);
+
+/*
+ * ft_moe_resolve_slots -- one device kernel resolves a layer's top-k ids
+ * against the global slot cache (FreeToken deep-dive, patterns 3 and 5;
+ * paper post, sec. 6):
+ *   U = distinct experts of ids (ascending); hits: map[layer*E+e] >= 0;
+ *   m misses; num_fetch = min(q*(m, frac_q16), S - #hits); the fetched
+ *   misses are the first num_fetch by (recency desc, id asc); the victims
+ *   are the non-hit slots by (usage asc, slot asc), the i-th fetched expert
+ *   taking the i-th victim; usage := step for hit and fetched slots;
+ *   recency := step for all of U; step += 1; then
+ *   slot_ids[t,j] = slot of ids[t,j] after the update, or -1 (host path).
+ * topk_ids, slot_ids: [T,k] int32.  num_fetch: [1] int32.  fetch_fid,
+ * fetch_slot: [max_list] int32, entries i < num_fetch hold (flat id, slot),
+ * the rest -1; max_list >= min(T*k, S) is required.  An id outside [0, E)
+ * records FT_ERR_BAD_ID in dev_status, leaves the state untouched and
+ * writes slot_ids = -1, num_fetch = 0.  Limits: E <= 4096, T*k <= 4096.
+ */
+FT_API ft_status ft_moe_resolve_slots(const ft_cache_state* state_host, int32_t layer,
+                               const int32_t* topk_ids, int32_t T, int32_t k,
+                               int32_t frac_q16, int32_t* slot_ids, int32_t* num_fetch,
+                               int32_t* fetch_fid, int32_t* fetch_slot, int32_t max_list,
+                               int32_t* dev_status, void* stream);
+
+/*
+ * ft_moe_fetch -- copy each fetched expert block pool[fetch_fid[i]] ->
+ * cache[fetch_slot[i]] for i < *num_fetch (read on the device, so the copy
+ * count may come straight from resolve).  Pool and cache must have the same
+ * format and shape; pool may be pinned host memory (the source of truth,
+ * FreeToken paper post, sec. 4; deep-dive pattern 3 copy_missing).  A flat
+ * id or slot outside its bank's n_blocks is skipped and records
+ * FT_ERR_BAD_ID.
+ */
+FT_API ft_status ft_moe_fetch(const ft_bank* pool_host, const ft_bank* cache_host,
+                       const int32_t* num_fetch, const int32_t* fetch_fid,
+                       const int32_t* fetch_slot, int32_t max_list, int32_t* dev_status,
+                       void* stream);
+
+/*
+ * ft_moe_experts_fwd -- quantized SwiGLU experts y = down(silu(gate.x) * up.x)
+ * (SSD-tier Edge0 summary, "How it works"; NVMe post, step 4).
+ * FT_DECODE: x [T,H] bf16; slot_ids, raw_ids, topk_w [T,k]; for each pair
+ *   the expert block is cache[slot] when slot >= 0, else pool[layer*E + raw]
+ *   when pool is non-NULL (the host-path pair, read in place), else the pair
+ *   is skipped (masked: deep-dive pattern 3).  out [T,H] (FT_OUT_F32 or
+ *   FT_OUT_BF16) = sum over computed pairs of topk_w * y, combine fused.
+ *   Each distinct expert's bytes are read once for all its tokens.  h is
+ *   kept in fp32.  Limits: T*k <= 256, T <= 16.  offsets unused (NULL).
+ * FT_PREFILL: x is the permuted batch Xp [T*k, H] bf16 from ft_moe_permute,
+ *   offsets [E+1] its expert segments; slot_ids is a per-expert table [E]
+ *   (block of expert e: cache[slot_ids[e]] when >= 0, else
+ *   pool[layer*E + e]); raw_ids and topk_w unused (NULL); out = Yp
+ *   [T*k, H] bf16 (FT_OUT_BF16), the unweighted expert rows, h rounded to
+ *   bf16.  NVFP4 only.
+ * ws: device scratch of ft_moe_experts_workspace(...) bytes.
+ */
+FT_API size_t ft_moe_experts_workspace(int32_t mode, int32_t T, int32_t k, int32_t H, int32_t I,
+                                int32_t E);
+FT_API ft_status ft_moe_experts_fwd(const ft_bank* cache_host, const ft_bank* pool_host, int32_t layer,
+                             int32_t E, const uint16_t* x, int32_t T, const int32_t* slot_ids,
+                             const int32_t* raw_ids, const float* topk_w, int32_t k,
+                             int32_t mode, const int32_t* offsets, void* out, int32_t out_dtype,
+                             void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * ft_moe_permute -- stable sort of the T*k (token, rank) pairs by expert
+ * (expert asc, then token, then rank) and gather of the permuted batch
+ * (NVMe post, step 5: the whole prompt through a layer's experts at once;
+ * Edge0 "How it works": dedup, stack, gather).
+ * topk_ids [T,k]; perm [T*k] (pair index t*k+j at each position); inv [T,k]
+ * (position of each pair); offsets [E+1]; x [T,H] bf16 -> xp [T*k,H] bf16
+ * (xp may be NULL to skip the gather).  ws: ft_moe_permute_workspace(T,k,E)
+ * bytes.  An id outside [0, E) records FT_ERR_BAD_ID.  Limits: E <= 4096.
+ */
+FT_API size_t ft_moe_permute_workspace(int32_t T, int32_t k, int32_t E);
+FT_API ft_status ft_moe_permute(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E,
+                         const uint16_t* x, int32_t H, int32_t* perm, int32_t* inv,
+                         int32_t* offsets, uint16_t* xp, void* ws, size_t ws_bytes,
+                         int32_t* dev_status, void* stream);
+
+/*
+ * ft_moe_combine -- out[t] = sum_j topk_w[t,j] * yp[inv[t,j]] in j order,
+ * fp32 accumulation, plus host_partial[t] when non-NULL (the host path's
+ * partial sum: FreeToken paper post, sec. 6, exact merge), rounded to bf16.
+ * yp [T*k,H] bf16; inv, topk_w [T,k]; host_partial [T,H] fp32; out [T,H] bf16.
+ */
+FT_API ft_status ft_moe_combine(const uint16_t* yp, const int32_t* inv, const float* topk_w,
+                         int32_t T, int32_t k, int32_t H, const float* host_partial,
+                         uint16_t* out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FT_MOE_H */

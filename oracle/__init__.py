@@ -81,6 +81,12 @@ def lib():
                                       c.c_int, c.c_double, c.c_void_p]
             L.orc_split_q16.restype = c.c_int32
             L.orc_split_q16.argtypes = [c.c_int32, c.c_int32]
+            L.orc_split_q16_grid.restype = None
+            L.orc_split_q16_grid.argtypes = [c.c_int32, c.c_int32, c.c_int32, c.c_void_p]
+            L.orc_resolve_many.restype = c.c_int
+            L.orc_resolve_many.argtypes = ([c.c_int] * 3 + [c.c_void_p] * 5 + [c.c_int, c.c_void_p,
+                                           c.c_int, c.c_int, c.c_int32, c.c_int] + [c.c_void_p] * 4
+                                           + [c.c_int])
             L.orc_route.restype = None
             L.orc_route.argtypes = [c.c_void_p, c.c_int, c.c_int, c.c_void_p, c.c_int,
                                     c.c_int, c.c_int, c.c_void_p, c.c_void_p, c.c_void_p]
@@ -168,6 +174,13 @@ def split_q16_many(ms, phi: int) -> np.ndarray:
                     np.int32).reshape(np.shape(ms))
 
 
+def split_q16_grid(m_max: int, phi_lo: int, phi_hi: int) -> np.ndarray:
+    """[phi_hi - phi_lo + 1, m_max + 1] table of the rule."""
+    out = np.empty((phi_hi - phi_lo + 1, m_max + 1), np.int32)
+    lib().orc_split_q16_grid(m_max, phi_lo, phi_hi, _ptr(out))
+    return out
+
+
 # -------------------------------------------------------------------- route
 def route(x_bf16: np.ndarray, W: np.ndarray, k: int, renorm: bool = False,
           want_logits: bool = False):
@@ -225,6 +238,23 @@ def resolve(st: CacheState, layer: int, ids: np.ndarray, phi: int, max_list: int
     if rc != 0:
         raise ValueError("orc_resolve rejected its arguments")
     return slot_ids, int(nf[0]), ff, fs
+
+
+def resolve_many(st: CacheState, layer: int, ids: np.ndarray, phi: int, max_list: int):
+    """ids [steps, T, k]; returns slot_ids [steps, T, k], num_fetch [steps],
+    fetch_fid / fetch_slot [steps, max_list]."""
+    ids = _c(ids, np.int32)
+    steps, T, k = ids.shape
+    sl = np.empty_like(ids)
+    nf = np.empty(steps, np.int32)
+    ff = np.empty((steps, max_list), np.int32)
+    fs = np.empty((steps, max_list), np.int32)
+    rc = lib().orc_resolve_many(st.L, st.E, st.S, _ptr(st.slot_owner), _ptr(st.map), _ptr(st.usage),
+                                _ptr(st.recency), _ptr(st.step), layer, _ptr(ids), T, k, int(phi),
+                                steps, _ptr(sl), _ptr(nf), _ptr(ff), _ptr(fs), max_list)
+    if rc != 0:
+        raise ValueError("orc_resolve_many rejected its arguments")
+    return sl, nf, ff, fs
 
 
 # ------------------------------------------------------------------ permute

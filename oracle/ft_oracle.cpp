@@ -240,6 +240,14 @@ int32_t orc_split_q16(int32_t m, int32_t phi) {
   return static_cast<int32_t>(std::min(M, max_fetch));
 }
 
+// The rule over a grid: out[(phi - phi_lo) * (m_max + 1) + m] for every
+// m in [0, m_max] and phi in [phi_lo, phi_hi].
+void orc_split_q16_grid(int32_t m_max, int32_t phi_lo, int32_t phi_hi, int32_t* out) {
+  for (int32_t phi = phi_lo; phi <= phi_hi; ++phi)
+    for (int32_t m = 0; m <= m_max; ++m)
+      out[static_cast<int64_t>(phi - phi_lo) * (m_max + 1) + m] = orc_split_q16(m, phi);
+}
+
 // ---------------------------------------------------------------- route ----
 // logits = x . W^T in fp64 from bf16 x [T,H] and fp32 W [E,H]; p = softmax
 // over all E experts; top-k by p descending, ties to the lower expert id;
@@ -375,6 +383,24 @@ int orc_resolve(int L, int E, int S, int32_t* slot_owner, int32_t* map,
   for (int i = 0; i < max_list; ++i) {
     fetch_fid[i] = (i < nf) ? static_cast<int32_t>(base + ranked[i]) : -1;
     fetch_slot[i] = (i < nf) ? cand[i] : -1;
+  }
+  return 0;
+}
+
+// n_steps consecutive resolve calls on one layer with one phi; step s reads
+// ids + s*T*k and writes slot_ids + s*T*k, num_fetch[s], and max_list fetch
+// entries at fetch_fid/fetch_slot + s*max_list.  Returns the first failing
+// step's -1, else 0.
+int orc_resolve_many(int L, int E, int S, int32_t* slot_owner, int32_t* map, int64_t* usage,
+                     int64_t* recency, int64_t* step, int layer, const int32_t* ids, int T,
+                     int k, int32_t phi, int n_steps, int32_t* slot_ids, int32_t* num_fetch,
+                     int32_t* fetch_fid, int32_t* fetch_slot, int max_list) {
+  const int64_t n = static_cast<int64_t>(T) * k;
+  for (int s = 0; s < n_steps; ++s) {
+    int rc = orc_resolve(L, E, S, slot_owner, map, usage, recency, step, layer, ids + s * n, T, k,
+                         phi, slot_ids + s * n, num_fetch + s, fetch_fid + static_cast<int64_t>(s) * max_list,
+                         fetch_slot + static_cast<int64_t>(s) * max_list, max_list);
+    if (rc != 0) return rc;
   }
   return 0;
 }

@@ -1,0 +1,490 @@
+// cache.cu -- the global slot cache on the device: the Q16 q* split, the
+// one-kernel resolve (dedup, residency, q*, recency-ranked fetch choice,
+// single-scan K-victim selection, id rewrite) and the fetch copy.
+//
+// Sources: "FreeToken 딥다이브" (fiv.co.kr), design patterns 2, 3, 5;
+// "FreeToken: 让消费级电脑跑起 284B MoE" (fengjutian.github.io), secs. 4, 6.
+#include "ft_common.cuh"
+
+namespace ft {
+namespace {
+
+constexpr int kResThreads = 1024;
+constexpr int kResMaxE = 4096;
+constexpr int kResMaxN = 4096;
+
+// The q* rule in Q16 fixed point: lo = floor(m*phi / 2^16); fetch lo or lo+1,
+// whichever gives the smaller slower-branch time max(f*(2^16-phi), (m-f)*phi)
+// (ties to lo), capped at m.  phi == 0 applies no cap.  64-bit intermediates.
+__device__ __forceinline__ int32_t split_q16_dev(int32_t m, int32_t phi) {
+  if (m <= 0) return 0;
+  if (phi <= 0) return m;
+  const int64_t q = 65536;
+  const int64_t M = m, P = phi;
+  const int64_t lo = (M * P) >> 16;
+  const int64_t c_lo = max(lo * (q - P), (M - lo) * P);
+  const int64_t c_hi = max((lo + 1) * (q - P), (M - lo - 1) * P);
+  const int64_t f = (c_lo <= c_hi) ? lo : lo + 1;
+  return static_cast<int32_t>(min(M, f));
+}
+
+__global__ void split_q16_kernel(const int32_t* __restrict__ m, int32_t n, int32_t phi,
+                                 int32_t* __restrict__ out) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+    out[i] = split_q16_dev(m[i], phi);
+}
+
+struct ResolveArgs {
+  int32_t E, S, layer, n, phi, max_list;
+  int32_t* slot_owner;
+  int32_t* map;
+  int64_t* usage;
+  int64_t* recency;
+  int64_t* step;
+  const int32_t* ids;
+  int32_t* slot_ids;
+  int32_t* num_fetch;
+  int32_t* fetch_fid;
+  int32_t* fetch_slot;
+  int32_t* dev_status;
+};
+
+__host__ __device__ inline size_t resolve_smem_bytes(int E, int n) {
+  const int cap = n < E ? n : E;
+  // inU[E] slotOf[E] U[cap] M[cap] fe[cap] vs[cap] vs2[cap] | mrec[cap] vu[cap] vu2[cap]
+  size_t ints = 2 * static_cast<size_t>(E) + 5 * static_cast<size_t>(cap);
+  ints = (ints + 1) & ~static_cast<size_t>(1);
+  return ints * 4 + 3 * static_cast<size_t>(cap) * 8;
+}
+
+// Is slot s owned by an expert of this call that is already resident (a hit)?
+__device__ __forceinline__ bool is_hit_slot(const int32_t* __restrict__ owner, int s, int base,
+                                            int E, const int* inU) {
+  const int o = owner[s];
+  return o >= base && o < base + E && inU[o - base] != 0;
+}
+
+__device__ __forceinline__ uint64_t ukey(int64_t u) {
+  return static_cast<uint64_t>(u) ^ 0x8000000000000000ull;
+}
+
+__global__ void __launch_bounds__(kResThreads, 1) resolve_kernel(ResolveArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int E = a.E, n = a.n, S = a.S;
+  const int cap = n < E ? n : E;
+  int* inU = reinterpret_cast<int*>(smem);
+  int* slotOf = inU + E;
+  int* U = slotOf + E;
+  int* M = U + cap;
+  int* fe = M + cap;
+  int* vs = fe + cap;
+  int* vs2 = vs + cap;
+  size_t ints = 2 * static_cast<size_t>(E) + 5 * static_cast<size_t>(cap);
+  ints = (ints + 1) & ~static_cast<size_t>(1);
+  int64_t* mrec = reinterpret_cast<int64_t*>(smem + ints * 4);
+  int64_t* vu = mrec + cap;
+  int64_t* vu2 = vu + cap;
+
+  __shared__ int scan_scratch[33];
+  __shared__ int s_bad, s_nU, s_m, s_nf, s_cnt;
+  __shared__ unsigned int hist[256];
+  __shared__ unsigned long long s_kmin, s_kmax, s_prefix;
+  __shared__ int s_krem, s_cmin;
+  __shared__ long long s_now;
+
+  const int tid = threadIdx.x;
+  const int nt = blockDim.x;
+  const int base = a.layer * E;
+
+  for (int e = tid; e < E; e += nt) {
+    inU[e] = 0;
+    slotOf[e] = -1;
+  }
+  if (tid == 0) {
+    s_bad = 0;
+    s_now = *a.step;
+  }
+  __syncthreads();
+  for (int i = tid; i < n; i += nt) {
+    const int e = a.ids[i];
+    if (e < 0 || e >= E)
+      s_bad = 1;
+    else
+      inU[e] = 1;
+  }
+  __syncthreads();
+  if (s_bad) {
+    for (int i = tid; i < n; i += nt) a.slot_ids[i] = -1;
+    for (int i = tid; i < a.max_list; i += nt) {
+      a.fetch_fid[i] = -1;
+      a.fetch_slot[i] = -1;
+    }
+    if (tid == 0) {
+      *a.num_fetch = 0;
+      record_status(a.dev_status, FT_ERR_BAD_ID);
+    }
+    return;
+  }
+
+  // 1. U = distinct experts, ascending (ordered compaction over contiguous ranges)
+  {
+    const int per = (E + nt - 1) / nt;
+    const int lo = min(E, tid * per), hi = min(E, lo + per);
+    int cnt = 0;
+    for (int e = lo; e < hi; ++e) cnt += inU[e];
+    int total;
+    int off = block_excl_scan(cnt, scan_scratch, &total);
+    for (int e = lo; e < hi; ++e)
+      if (inU[e]) U[off++] = e;
+    if (tid == 0) s_nU = total;
+  }
+  __syncthreads();
+  const int nU = s_nU;
+
+  // 2. hits / misses; misses keep ascending order
+  {
+    const int per = (nU + nt - 1) / nt;
+    const int lo = min(nU, tid * per), hi = min(nU, lo + per);
+    int cnt = 0;
+    for (int i = lo; i < hi; ++i) {
+      const int e = U[i];
+      const int s = a.map[base + e];
+      slotOf[e] = s;
+      cnt += (s < 0);
+    }
+    int total;
+    int off = block_excl_scan(cnt, scan_scratch, &total);
+    for (int i = lo; i < hi; ++i) {
+      const int e = U[i];
+      if (slotOf[e] < 0) {
+        M[off] = e;
+        mrec[off] = a.recency[base + e];
+        ++off;
+      }
+    }
+    if (tid == 0) {
+      s_m = total;
+      const int nhit = nU - total;
+      const int evictable = S - nhit;
+      int nf = split_q16_dev(total, a.phi);
+      nf = min(nf, evictable);
+      s_nf = max(nf, 0);
+    }
+  }
+  __syncthreads();
+  const int m = s_m, nf = s_nf;
+
+  // 3. the fetched misses: rank by (recency desc, id asc)
+  for (int j = tid; j < m; j += nt) {
+    const int64_t rj = mrec[j];
+    const int ej = M[j];
+    int r = 0;
+    for (int j2 = 0; j2 < m; ++j2) {
+      const int64_t r2 = mrec[j2];
+      r += (r2 > rj) || (r2 == rj && M[j2] < ej);
+    }
+    if (r < nf) fe[r] = ej;
+  }
+
+  // 4. the victims: the nf smallest (usage, slot) among non-hit slots
+  if (nf > 0) {
+    unsigned long long kmin = ~0ull, kmax = 0ull;
+    for (int s = tid; s < S; s += nt) {
+      if (is_hit_slot(a.slot_owner, s, base, E, inU)) continue;
+      const unsigned long long k = ukey(a.usage[s]);
+      kmin = min(kmin, k);
+      kmax = max(kmax, k);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+      kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+    }
+    if (tid == 0) {
+      s_kmin = ~0ull;
+      s_kmax = 0ull;
+      s_cmin = 0;
+    }
+    __syncthreads();
+    if ((tid & 31) == 0) {
+      atomicMin(&s_kmin, kmin);
+      atomicMax(&s_kmax, kmax);
+    }
+    __syncthreads();
+    const unsigned long long gmin = s_kmin, gmax = s_kmax;
+    int c = 0;
+    for (int s = tid; s < S; s += nt)
+      if (!is_hit_slot(a.slot_owner, s, base, E, inU) && ukey(a.usage[s]) == gmin) ++c;
+    atomicAdd(&s_cmin, c);
+    if (tid == 0) {
+      s_prefix = 0ull;
+      s_krem = nf;
+    }
+    __syncthreads();
+    unsigned long long tau;
+    if (s_cmin >= nf || gmax == gmin) {
+      tau = gmin;
+    } else {
+      // radix select over d = key - min, 8 bits per pass from the top digit
+      const unsigned long long range = gmax - gmin;
+      const int nbits = 64 - __clzll(static_cast<long long>(range));
+      for (int shift = ((nbits - 1) / 8) * 8; shift >= 0; shift -= 8) {
+        for (int b = tid; b < 256; b += nt) hist[b] = 0;
+        __syncthreads();
+        const unsigned long long pre = s_prefix;
+        for (int s = tid; s < S; s += nt) {
+          if (is_hit_slot(a.slot_owner, s, base, E, inU)) continue;
+          const unsigned long long d = ukey(a.usage[s]) - gmin;
+          const bool match = (shift + 8 >= 64) ? true : ((d >> (shift + 8)) == pre);
+          if (match) atomicAdd(&hist[(d >> shift) & 255ull], 1u);
+        }
+        __syncthreads();
+        if (tid == 0) {
+          int krem = s_krem;
+          int b = 0;
+          unsigned int cum = 0;
+          for (; b < 256; ++b) {
+            if (cum + hist[b] >= static_cast<unsigned int>(krem)) break;
+            cum += hist[b];
+          }
+          s_krem = krem - static_cast<int>(cum);
+          s_prefix = (pre << 8) | static_cast<unsigned long long>(b);
+        }
+        __syncthreads();
+      }
+      tau = gmin + s_prefix;
+    }
+    // keys below tau: all taken (unordered append)
+    if (tid == 0) s_cnt = 0;
+    __syncthreads();
+    for (int s = tid; s < S; s += nt) {
+      if (is_hit_slot(a.slot_owner, s, base, E, inU)) continue;
+      const int64_t u = a.usage[s];
+      if (ukey(u) < tau) {
+        const int p = atomicAdd(&s_cnt, 1);
+        if (p < nf) {
+          vs[p] = s;
+          vu[p] = u;
+        }
+      }
+    }
+    __syncthreads();
+    const int nless = min(s_cnt, nf);
+    const int need = nf - nless;
+    // keys equal to tau: the lowest slots first (ordered scan over slots)
+    int running = 0;
+    for (int t0 = 0; t0 < S && running < need; t0 += nt) {
+      const int s = t0 + tid;
+      int flag = 0;
+      int64_t u = 0;
+      if (s < S && !is_hit_slot(a.slot_owner, s, base, E, inU)) {
+        u = a.usage[s];
+        flag = (ukey(u) == tau);
+      }
+      int total;
+      const int pos = block_excl_scan(flag, scan_scratch, &total) + running;
+      if (flag && pos < need) {
+        vs[nless + pos] = s;
+        vu[nless + pos] = u;
+      }
+      running += total;
+    }
+    __syncthreads();
+    // order the victims by (usage asc, slot asc)
+    for (int i = tid; i < nf; i += nt) {
+      const int64_t ui = vu[i];
+      const int si = vs[i];
+      int r = 0;
+      for (int j = 0; j < nf; ++j) r += (vu[j] < ui) || (vu[j] == ui && vs[j] < si);
+      vs2[r] = si;
+      vu2[r] = ui;
+    }
+  }
+  __syncthreads();
+
+  // 5. state update
+  const int64_t now = s_now;
+  for (int i = tid; i < nU; i += nt) {
+    const int s = slotOf[U[i]];
+    if (s >= 0) a.usage[s] = now;
+  }
+  for (int i = tid; i < nf; i += nt) {
+    const int v = vs2[i];
+    const int old = a.slot_owner[v];
+    if (old >= 0) a.map[old] = -1;
+  }
+  __syncthreads();
+  for (int i = tid; i < nf; i += nt) {
+    const int e = fe[i];
+    const int v = vs2[i];
+    a.slot_owner[v] = base + e;
+    a.map[base + e] = v;
+    a.usage[v] = now;
+    slotOf[e] = v;
+  }
+  for (int i = tid; i < nU; i += nt) a.recency[base + U[i]] = now;
+  __syncthreads();
+
+  // 6. outputs
+  for (int i = tid; i < n; i += nt) a.slot_ids[i] = slotOf[a.ids[i]];
+  for (int i = tid; i < a.max_list; i += nt) {
+    a.fetch_fid[i] = (i < nf) ? base + fe[i] : -1;
+    a.fetch_slot[i] = (i < nf) ? vs2[i] : -1;
+  }
+  if (tid == 0) {
+    *a.num_fetch = nf;
+    *a.step = now + 1;
+  }
+}
+
+// Copy fetched expert blocks pool[fid] -> cache[slot] for i < *num_fetch.
+// A grid-stride loop over (fetch index, 32 KiB chunk) items; each thread moves
+// eight 16-byte vectors with all loads issued before the stores.
+constexpr int kFetchThreads = 256;
+constexpr int kFetchVec = 8;
+
+__global__ void __launch_bounds__(kFetchThreads) fetch_kernel(
+    const uint8_t* __restrict__ pool, uint64_t pstride, uint8_t* __restrict__ cache,
+    uint64_t cstride, uint64_t n16, const int32_t* __restrict__ num_fetch,
+    const int32_t* __restrict__ ffid, const int32_t* __restrict__ fslot, int32_t max_list,
+    int64_t n_pool, int64_t n_cache, int32_t* dev_status) {
+  const int nf = min(*num_fetch, max_list);
+  const uint64_t per = static_cast<uint64_t>(kFetchThreads) * kFetchVec;
+  const uint64_t nchunks = (n16 + per - 1) / per;
+  const uint64_t items = static_cast<uint64_t>(nf > 0 ? nf : 0) * nchunks;
+  for (uint64_t item = blockIdx.x; item < items; item += gridDim.x) {
+    const int i = static_cast<int>(item / nchunks);
+    const uint64_t c = item % nchunks;
+    const int fid = ffid[i], slot = fslot[i];
+    if (fid < 0 || fid >= n_pool || slot < 0 || slot >= n_cache) {
+      if (c == 0 && threadIdx.x == 0) record_status(dev_status, FT_ERR_BAD_ID);
+      continue;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(pool + static_cast<uint64_t>(fid) * pstride);
+    uint4* dst = reinterpret_cast<uint4*>(cache + static_cast<uint64_t>(slot) * cstride);
+    uint4 r[kFetchVec];
+#pragma unroll
+    for (int u = 0; u < kFetchVec; ++u) {
+      const uint64_t idx = c * per + static_cast<uint64_t>(u) * kFetchThreads + threadIdx.x;
+      if (idx < n16) r[u] = src[idx];
+    }
+#pragma unroll
+    for (int u = 0; u < kFetchVec; ++u) {
+      const uint64_t idx = c * per + static_cast<uint64_t>(u) * kFetchThreads + threadIdx.x;
+      if (idx < n16) dst[idx] = r[u];
+    }
+  }
+}
+
+int g_num_sms = 0;
+
+int num_sms() {
+  if (g_num_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_num_sms <= 0) g_num_sms = 148;
+  }
+  return g_num_sms;
+}
+
+}  // namespace
+}  // namespace ft
+
+extern "C" {
+
+ft_status ft_moe_split_q16(const int32_t* num_missing, int32_t n, int32_t frac_q16,
+                           int32_t* num_fetch, void* stream) {
+  FT_REQUIRE(n >= 0, "split_q16: n < 0");
+  FT_REQUIRE(frac_q16 >= 0 && frac_q16 <= 65536, "split_q16: frac_q16 %d outside [0, 65536]",
+             frac_q16);
+  if (n == 0) return FT_OK;
+  FT_REQUIRE(num_missing != nullptr && num_fetch != nullptr, "split_q16: NULL pointer");
+  const int threads = 256;
+  const int blocks = min((n + threads - 1) / threads, 4096);
+  ft::split_q16_kernel<<<blocks, threads, 0, ft::as_stream(stream)>>>(num_missing, n, frac_q16,
+                                                                     num_fetch);
+  return ft::launch_check("split_q16");
+}
+
+ft_status ft_moe_resolve_slots(const ft_cache_state* st, int32_t layer, const int32_t* topk_ids,
+                               int32_t T, int32_t k, int32_t frac_q16, int32_t* slot_ids,
+                               int32_t* num_fetch, int32_t* fetch_fid, int32_t* fetch_slot,
+                               int32_t max_list, int32_t* dev_status, void* stream) {
+  FT_REQUIRE(st != nullptr, "resolve: state is NULL");
+  FT_REQUIRE(st->L > 0 && st->E > 0 && st->S >= 0, "resolve: bad L/E/S %d/%d/%d", st->L, st->E,
+             st->S);
+  FT_REQUIRE(st->E <= ft::kResMaxE, "resolve: E %d > %d", st->E, ft::kResMaxE);
+  FT_REQUIRE(static_cast<int64_t>(st->L) * st->E < (1ll << 31), "resolve: L*E overflows int32");
+  FT_REQUIRE(layer >= 0 && layer < st->L, "resolve: layer %d outside [0, %d)", layer, st->L);
+  FT_REQUIRE(T >= 0 && k >= 1, "resolve: T=%d k=%d", T, k);
+  const int64_t n64 = static_cast<int64_t>(T) * k;
+  FT_REQUIRE(n64 <= ft::kResMaxN, "resolve: T*k = %lld > %d", static_cast<long long>(n64),
+             ft::kResMaxN);
+  FT_REQUIRE(frac_q16 >= 0 && frac_q16 <= 65536, "resolve: frac_q16 %d outside [0, 65536]",
+             frac_q16);
+  const int n = static_cast<int>(n64);
+  const int need = n < st->S ? n : st->S;
+  FT_REQUIRE(max_list >= need, "resolve: max_list %d < min(T*k, S) = %d", max_list, need);
+  FT_REQUIRE(st->map && st->recency && st->step && num_fetch && fetch_fid && fetch_slot,
+             "resolve: NULL pointer");
+  FT_REQUIRE(st->S == 0 || (st->slot_owner && st->usage), "resolve: NULL slot arrays");
+  FT_REQUIRE(n == 0 || (topk_ids && slot_ids), "resolve: NULL ids");
+  ft::ResolveArgs a;
+  a.E = st->E;
+  a.S = st->S;
+  a.layer = layer;
+  a.n = n;
+  a.phi = frac_q16;
+  a.max_list = max_list;
+  a.slot_owner = st->slot_owner;
+  a.map = st->map;
+  a.usage = st->usage;
+  a.recency = st->recency;
+  a.step = st->step;
+  a.ids = topk_ids;
+  a.slot_ids = slot_ids;
+  a.num_fetch = num_fetch;
+  a.fetch_fid = fetch_fid;
+  a.fetch_slot = fetch_slot;
+  a.dev_status = dev_status;
+  const size_t smem = ft::resolve_smem_bytes(st->E, n);
+  if (smem > 48 * 1024) {
+    static const size_t kMax = ft::resolve_smem_bytes(ft::kResMaxE, ft::kResMaxN);
+    cudaError_t e = cudaFuncSetAttribute(ft::resolve_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kMax));
+    if (e != cudaSuccess)
+      return ft::fail(FT_ERR_CUDA, "resolve: smem attribute: %s", cudaGetErrorString(e));
+  }
+  ft::resolve_kernel<<<1, ft::kResThreads, smem, ft::as_stream(stream)>>>(a);
+  return ft::launch_check("resolve_slots");
+}
+
+ft_status ft_moe_fetch(const ft_bank* pool, const ft_bank* cache, const int32_t* num_fetch,
+                       const int32_t* fetch_fid, const int32_t* fetch_slot, int32_t max_list,
+                       int32_t* dev_status, void* stream) {
+  ft::Layout Lp, Lc;
+  ft_status s = ft::check_bank(pool, "fetch pool", &Lp);
+  if (s != FT_OK) return s;
+  s = ft::check_bank(cache, "fetch cache", &Lc);
+  if (s != FT_OK) return s;
+  FT_REQUIRE(pool->fmt == cache->fmt && pool->H == cache->H && pool->I == cache->I &&
+                 pool->group == cache->group,
+             "fetch: pool and cache shapes differ");
+  FT_REQUIRE(max_list >= 0, "fetch: max_list < 0");
+  if (max_list == 0) return FT_OK;
+  FT_REQUIRE(num_fetch && fetch_fid && fetch_slot, "fetch: NULL pointer");
+  const uint64_t n16 = Lp.total / 16;
+  const uint64_t per = static_cast<uint64_t>(ft::kFetchThreads) * ft::kFetchVec;
+  const uint64_t nchunks = (n16 + per - 1) / per;
+  const uint64_t items = nchunks * static_cast<uint64_t>(max_list);
+  const int grid = static_cast<int>(std::min<uint64_t>(items, static_cast<uint64_t>(ft::num_sms()) * 4));
+  ft::fetch_kernel<<<grid, ft::kFetchThreads, 0, ft::as_stream(stream)>>>(
+      static_cast<const uint8_t*>(pool->base), pool->stride,
+      static_cast<uint8_t*>(const_cast<void*>(cache->base)), cache->stride, n16, num_fetch,
+      fetch_fid, fetch_slot, max_list, pool->n_blocks, cache->n_blocks, dev_status);
+  return ft::launch_check("fetch");
+}
+
+}  // extern "C"

@@ -1,0 +1,245 @@
+// route.cu -- the router on the GPU: logits = x . W^T (fp32 accumulation),
+// softmax over all experts, top-k by probability (ties to the lower id).
+//
+// Source: "FreeToken: 让消费级电脑跑起 284B MoE" (fengjutian.github.io),
+// sec. 2 (the router runs on the GPU and feeds the hit / miss split).
+//
+// Two logits kernels: a weight-streaming GEMV for small token counts (the
+// router matrix is read once, every warp owns one expert row) and a tiled
+// SIMT GEMM for long prompts.  Then one warp per token does the softmax and
+// the top-k selection.
+#include "ft_common.cuh"
+
+namespace ft {
+namespace {
+
+constexpr int kGemvMaxT = 16;
+constexpr int kRouteMaxK = 32;
+
+// One warp per expert row; lanes stride the hidden axis 8 elements at a time.
+template <int TMAX>
+__global__ void __launch_bounds__(256) route_gemv_kernel(const uint16_t* __restrict__ x, int T,
+                                                         int H, const float* __restrict__ W,
+                                                         int E, float* __restrict__ logits) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 8 + warp;
+  if (e >= E) return;
+  float acc[TMAX];
+#pragma unroll
+  for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
+  const float4* wrow = reinterpret_cast<const float4*>(W + static_cast<size_t>(e) * H);
+  const int nch = H / 8;
+  for (int c0 = 0; c0 < nch; c0 += 32 * 4) {
+    float4 wa[4], wb[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + u * 32 + lane;
+      if (c < nch) {
+        wa[u] = __ldg(wrow + 2 * c);
+        wb[u] = __ldg(wrow + 2 * c + 1);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + u * 32 + lane;
+      if (c >= nch) break;
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t) {
+        if (t >= T) break;
+        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H) + c);
+        float s = acc[t];
+        s = fmaf(bf16_lo(xv.x), wa[u].x, s);
+        s = fmaf(bf16_hi(xv.x), wa[u].y, s);
+        s = fmaf(bf16_lo(xv.y), wa[u].z, s);
+        s = fmaf(bf16_hi(xv.y), wa[u].w, s);
+        s = fmaf(bf16_lo(xv.z), wb[u].x, s);
+        s = fmaf(bf16_hi(xv.z), wb[u].y, s);
+        s = fmaf(bf16_lo(xv.w), wb[u].z, s);
+        s = fmaf(bf16_hi(xv.w), wb[u].w, s);
+        acc[t] = s;
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < TMAX; ++t) {
+    if (t >= T) break;
+    const float s = warp_sum(acc[t]);
+    if (lane == 0) logits[static_cast<size_t>(t) * E + e] = s;
+  }
+}
+
+// Tiled SIMT GEMM: a 64-token x 64-expert tile per CTA, 256 threads with 4x4
+// outputs each, K staged 32 at a time through shared memory.
+constexpr int kTM = 64, kTN = 64, kTK = 32;
+
+__global__ void __launch_bounds__(256) route_tiled_kernel(const uint16_t* __restrict__ x, int T,
+                                                          int H, const float* __restrict__ W,
+                                                          int E, float* __restrict__ logits) {
+  __shared__ float xs[kTK][kTM + 4];
+  __shared__ float ws[kTK][kTN + 4];
+  const int t0 = blockIdx.y * kTM, e0 = blockIdx.x * kTN;
+  const int tid = threadIdx.x;
+  const int tr = (tid / 16) * 4, tc = (tid % 16) * 4;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < H; k0 += kTK) {
+    // x tile: 64 rows x 32 k as bf16 -> 256 threads x 8 elements
+    {
+      const int row = tid / 4, kk = (tid % 4) * 8;
+      const int t = t0 + row;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (t < T) v = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H + k0 + kk));
+      xs[kk + 0][row] = bf16_lo(v.x);
+      xs[kk + 1][row] = bf16_hi(v.x);
+      xs[kk + 2][row] = bf16_lo(v.y);
+      xs[kk + 3][row] = bf16_hi(v.y);
+      xs[kk + 4][row] = bf16_lo(v.z);
+      xs[kk + 5][row] = bf16_hi(v.z);
+      xs[kk + 6][row] = bf16_lo(v.w);
+      xs[kk + 7][row] = bf16_hi(v.w);
+    }
+    // W tile: 64 experts x 32 k fp32 -> 256 threads x 2 float4
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int idx = tid + u * 256;
+      const int row = idx / 8, kk = (idx % 8) * 4;
+      const int e = e0 + row;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e < E) v = __ldg(reinterpret_cast<const float4*>(W + static_cast<size_t>(e) * H + k0 + kk));
+      ws[kk + 0][row] = v.x;
+      ws[kk + 1][row] = v.y;
+      ws[kk + 2][row] = v.z;
+      ws[kk + 3][row] = v.w;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < kTK; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = xs[kk][tr + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = ws[kk][tc + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + tr + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + tc + j;
+      if (e < E) logits[static_cast<size_t>(t) * E + e] = acc[i][j];
+    }
+  }
+}
+
+// (a before b) in the routing order: larger logit first, ties to the lower id.
+__device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+// One warp per token: max, softmax denominator, then k rounds of "best
+// element ranked after the previous winner" (a selection with no taken set).
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T,
+                                                         int E, int k, int renorm,
+                                                         int32_t* __restrict__ ids,
+                                                         float* __restrict__ wts) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  const float* l = logits + static_cast<size_t>(t) * E;
+  float mx = -INFINITY;
+  for (int e = lane; e < E; e += 32) mx = fmaxf(mx, l[e]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float z = 0.f;
+  for (int e = lane; e < E; e += 32) z += expf(l[e] - mx);
+  z = warp_sum(z);
+  float pv = INFINITY;
+  int pi = -1;
+  float sel_sum = 0.f;
+  float my_w = 0.f;
+  int my_id = 0;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int e = lane; e < E; e += 32) {
+      const float v = l[e];
+      if (ranks_before(pv, pi, v, e) && ranks_before(v, e, bv, bi)) {
+        bv = v;
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ranks_before(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    pv = bv;
+    pi = bi;
+    const float p = expf(bv - mx) / z;
+    sel_sum += p;
+    if (lane == j) {
+      my_w = p;
+      my_id = bi;
+    }
+  }
+  if (lane < k) {
+    ids[static_cast<size_t>(t) * k + lane] = my_id;
+    wts[static_cast<size_t>(t) * k + lane] = renorm ? my_w / sel_sum : my_w;
+  }
+}
+
+}  // namespace
+}  // namespace ft
+
+extern "C" {
+
+size_t ft_moe_route_workspace(int32_t T, int32_t E) {
+  if (T <= 0 || E <= 0) return 0;
+  return (static_cast<size_t>(T) * E * sizeof(float) + 255) & ~static_cast<size_t>(255);
+}
+
+ft_status ft_moe_route(const uint16_t* x, int32_t T, int32_t H, const float* w_router, int32_t E,
+                       int32_t k, int32_t renorm, int32_t* topk_ids, float* topk_w, void* ws,
+                       size_t ws_bytes, void* stream) {
+  FT_REQUIRE(T >= 0, "route: T < 0");
+  FT_REQUIRE(E >= 1 && E <= 4096, "route: E %d outside [1, 4096]", E);
+  FT_REQUIRE(k >= 1 && k <= E && k <= ft::kRouteMaxK, "route: k %d outside [1, min(E, 32)]", k);
+  FT_REQUIRE(H >= 8 && H % 8 == 0, "route: H %d must be a positive multiple of 8", H);
+  if (T == 0) return FT_OK;
+  FT_REQUIRE(x && w_router && topk_ids && topk_w && ws, "route: NULL pointer");
+  FT_REQUIRE(ws_bytes >= ft_moe_route_workspace(T, E), "route: workspace %zu < %zu", ws_bytes,
+             ft_moe_route_workspace(T, E));
+  FT_REQUIRE(reinterpret_cast<uintptr_t>(x) % 16 == 0 && reinterpret_cast<uintptr_t>(w_router) % 16 == 0,
+             "route: x and w_router must be 16-byte aligned");
+  cudaStream_t s = ft::as_stream(stream);
+  float* logits = static_cast<float*>(ws);
+  if (T <= ft::kGemvMaxT) {
+    const int grid = (E + 7) / 8;
+    if (T <= 1)
+      ft::route_gemv_kernel<1><<<grid, 256, 0, s>>>(x, T, H, w_router, E, logits);
+    else if (T <= 4)
+      ft::route_gemv_kernel<4><<<grid, 256, 0, s>>>(x, T, H, w_router, E, logits);
+    else
+      ft::route_gemv_kernel<16><<<grid, 256, 0, s>>>(x, T, H, w_router, E, logits);
+  } else {
+    FT_REQUIRE(H % ft::kTK == 0, "route: H %d must be a multiple of 32 for T > 16", H);
+    dim3 grid((E + ft::kTN - 1) / ft::kTN, (T + ft::kTM - 1) / ft::kTM);
+    ft::route_tiled_kernel<<<grid, 256, 0, s>>>(x, T, H, w_router, E, logits);
+  }
+  ft_status st = ft::launch_check("route logits");
+  if (st != FT_OK) return st;
+  ft::route_topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits, T, E, k, renorm, topk_ids, topk_w);
+  return ft::launch_check("route topk");
+}
+
+}  // extern "C"
