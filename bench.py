@@ -1,0 +1,575 @@
+"""Benchmark of the routed, quantized expert-FFN MoE layer on GB300.
+
+Workload (default): the 35B-A3B-shaped int4 decode layer -- 40 layers,
+hidden 2048, 256 experts, top-8, expert intermediate 512, int4 g64 weights
+(1,671,168 B per expert), a slot cache of 2,560 experts (25% of the 10,240
+(layer, expert) pairs) warmed from a seeded Zipf(1.1) routing history, and the
+full pool (17.1 GB) in pinned host memory as the source of truth.
+
+One step = T tokens through all 40 MoE layers; each layer runs the whole hot
+path: route (logits, softmax, top-k) -> resolve (slot or -1, q* split) ->
+fetch (misses pool -> cache) -> experts (gate/up, SwiGLU, down, combine).  The
+40-layer step is captured once in a CUDA graph and replayed; inputs for every
+step are resident in HBM before timing starts.
+
+Printed: one JSON line (rank 0).  --impl reference times the CPU oracle on
+the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s; decode expert-weight HBM GB/s; prefill grouped-GEMM TFLOP/s"
+UNIT = "MoE-layer tokens/s"
+
+
+# --------------------------------------------------------------- plumbing --
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def aggregate(rank_units: float, rank_seconds: float, world: int, reduce_fn=None):
+    """Whole-job throughput: units summed over ranks / the slowest rank's time."""
+    if world == 1 or reduce_fn is None:
+        return rank_units / rank_seconds, rank_seconds, rank_units
+    units, secs = reduce_fn(rank_units, rank_seconds)
+    return units / secs, secs, units
+
+
+def torch_reduce_fn(device):
+    import torch
+    import torch.distributed as dist
+
+    def fn(units, secs):
+        u = torch.tensor([units], dtype=torch.float64, device=device)
+        s = torch.tensor([secs], dtype=torch.float64, device=device)
+        dist.all_reduce(u, op=dist.ReduceOp.SUM)
+        dist.all_reduce(s, op=dist.ReduceOp.MAX)
+        return float(u.item()), float(s.item())
+
+    return fn
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while active."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ----------------------------------------------------------- the workload --
+class DecodeWorkload:
+    """Device state of the decode benchmark for one config (built untimed)."""
+
+    def __init__(self, cfg, T: int, phi: int, n_steps: int, device, log=print):
+        import torch
+
+        import quantized_expert_ffn_router_gb300 as ft
+        import synth
+
+        self.ft, self.cfg, self.T, self.phi = ft, cfg, T, phi
+        self.dev = device
+        L, E, k, H, I, g = cfg.L, cfg.E, cfg.k, cfg.H, cfg.I, cfg.g
+        self.block, self.offs = ft.block_bytes(cfg.fmt, H, I, g)
+        stride = self.block
+        t0 = time.time()
+        # pool: the source of truth, pinned host memory, indexed by flat id
+        n_fid = L * E
+        self.pool = torch.empty((n_fid, stride), dtype=torch.uint8, pin_memory=True)
+        chunk = 128
+        tmp = torch.empty((chunk, stride), dtype=torch.uint8, device=device)
+        for f0 in range(0, n_fid, chunk):
+            n = min(chunk, n_fid - f0)
+            synth.bank_blocks_torch(cfg.seed, range(f0, f0 + n), cfg.fmt, H, I, g, tmp[:n], ref_K=cfg.ref_K)
+            self.pool[f0:f0 + n].copy_(tmp[:n])
+        torch.cuda.synchronize()
+        log(f"pool {n_fid} x {stride} B generated in {time.time() - t0:.1f}s")
+        ts = synth.tensor_scales(cfg.fmt, H, I, n_fid)
+        self.tscale = None if ts is None else torch.from_numpy(ts).to(device)
+        self.S = cfg.slots
+        self.cache = torch.zeros((self.S, stride), dtype=torch.uint8, device=device)
+        self.pool_b = ft.make_bank(cfg.fmt, H, I, g, self.pool, self.tscale)
+        self.cache_b = ft.make_bank(cfg.fmt, H, I, g, self.cache, self.tscale)
+        # router weights with the Zipf bias feature (column 0)
+        self.W = torch.stack([torch.from_numpy(synth.router_weights(cfg.seed, l, E, H, cfg.router_std,
+                                                                    zipf_bias=cfg.zipf))
+                              for l in range(L)]).to(device)
+        # cache state: replay the seeded Zipf history through the GPU resolve
+        self.state = ft.DeviceCacheState(L, E, self.S, device=device)
+        t0 = time.time()
+        hist = synth.zipf_history(cfg.seed, L, E, k, cfg.history_steps)
+        hd = torch.from_numpy(hist).to(device)
+        sl = torch.empty((1, k), dtype=torch.int32, device=device)
+        nf = torch.zeros(1, dtype=torch.int32, device=device)
+        ff = torch.empty(k, dtype=torch.int32, device=device)
+        fs = torch.empty(k, dtype=torch.int32, device=device)
+        for s in range(cfg.history_steps):
+            for l in range(L):
+                ft.resolve_slots(self.state, l, hd[s, l:l + 1], 65536, sl, nf, ff, fs)
+        # fill the cache with its owners' blocks (one fetch over all slots)
+        owner = self.state.slot_owner[: self.S]
+        idx = torch.nonzero(owner >= 0).flatten().to(torch.int32)
+        nfill = torch.tensor([idx.numel()], dtype=torch.int32, device=device)
+        ft.fetch(self.pool_b, self.cache_b, nfill, owner[idx.long()].contiguous(), idx.contiguous())
+        torch.cuda.synchronize()
+        log(f"cache warmed ({int(idx.numel())} slots) from {cfg.history_steps} history steps in "
+            f"{time.time() - t0:.1f}s")
+        # per-step inputs: x ~ N(0,1) bf16 with feature 0 = 1.0 (the bias feature)
+        xs = synth.normal_bf16(synth.stream_key(cfg.seed, "bench-x", T), (n_steps, L, T, H))
+        xs[..., 0] = synth.bf16_bits(np.array([1.0], np.float32))[0]
+        self.x_host = torch.from_numpy(xs.view(np.int16)).pin_memory()
+        self.x_all = self.x_host.to(device)
+        self.x_stage = torch.empty((L, T, H), dtype=torch.int16, device=device)
+        self.out = torch.empty((L, T, H), dtype=torch.int16, device=device)
+        # per-layer buffers
+        self.ids = torch.empty((L, T, k), dtype=torch.int32, device=device)
+        self.w = torch.empty((L, T, k), dtype=torch.float32, device=device)
+        self.slot = torch.empty((L, T, k), dtype=torch.int32, device=device)
+        self.nf = torch.zeros((L, 1), dtype=torch.int32, device=device)
+        self.ml = T * k
+        self.ff = torch.empty((L, self.ml), dtype=torch.int32, device=device)
+        self.fs = torch.empty((L, self.ml), dtype=torch.int32, device=device)
+        self.rws = torch.empty(ft.route_workspace(T, E), dtype=torch.uint8, device=device)
+        self.ews = torch.empty(ft.experts_workspace(ft.FT_DECODE, T, k, H, I, E), dtype=torch.uint8,
+                               device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.events = None
+
+    # one pass of the hot path over all layers (enqueue only)
+    def step(self, events=None):
+        ft, cfg, T = self.ft, self.cfg, self.T
+        for l in range(cfg.L):
+            if events is not None:
+                events[l][0].record()
+            ft.route(self.x_stage[l], self.W[l], cfg.k, self.ids[l], self.w[l], self.rws)
+            if events is not None:
+                events[l][1].record()
+            ft.resolve_slots(self.state, l, self.ids[l], self.phi, self.slot[l], self.nf[l], self.ff[l],
+                             self.fs[l], self.status)
+            if events is not None:
+                events[l][2].record()
+            ft.fetch(self.pool_b, self.cache_b, self.nf[l], self.ff[l], self.fs[l], self.status)
+            if events is not None:
+                events[l][3].record()
+            ft.experts_fwd(self.cache_b, self.pool_b, l, cfg.E, self.x_stage[l], T, cfg.k, self.slot[l],
+                           self.ids[l], self.w[l], self.out[l], self.ews, dev_status=self.status)
+            if events is not None:
+                events[l][4].record()
+
+    def capture(self):
+        import torch
+
+        try:
+            self.events = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
+                           for _ in range(self.cfg.L)]
+        except TypeError:
+            self.events = None
+        self.x_stage.copy_(self.x_all[0])
+        self.step()  # eager warm-up (attributes, lazy init) before capture
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.step(self.events)
+        torch.cuda.synchronize()
+
+    def kernel_times(self):
+        """Per-op device time (us, summed over layers) of the last replay."""
+        if self.events is None:
+            return None
+        names = ["route", "resolve", "fetch", "experts"]
+        tot = {n: 0.0 for n in names}
+        for ev in self.events:
+            for i, n in enumerate(names):
+                tot[n] += ev[i].elapsed_time(ev[i + 1]) * 1e3
+        return tot
+
+    def distinct_expert_bytes(self):
+        """Algorithmic expert bytes of the last step: distinct experts per layer
+        (cache and pool reads alike) x block bytes."""
+        ids = self.ids.cpu().numpy()
+        return sum(len(set(ids[l].ravel().tolist())) for l in range(self.cfg.L)) * self.block
+
+    def fetch_bytes(self):
+        return int(self.nf.sum().item()) * self.block
+
+    def misses(self):
+        sl = self.slot.cpu().numpy()
+        return int(self.nf.sum().item()), int((sl < 0).sum())
+
+
+def time_device(wl, steps: int, warmup: int, reduce_fn, world: int, clocks=None):
+    import torch
+
+    s = torch.cuda.current_stream()
+    for i in range(warmup):
+        wl.x_stage.copy_(wl.x_all[i % wl.x_all.shape[0]])
+        wl.graph.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for i in range(steps):
+        wl.x_stage.copy_(wl.x_all[(warmup + i) % wl.x_all.shape[0]])
+        wl.graph.replay()
+    e1.record(s)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.stop()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+    return e0.elapsed_time(e1) / 1e3
+
+
+def time_e2e(wl, steps: int, warmup: int):
+    """Host buffers in, host buffers out: pinned H2D of the step's inputs,
+    graph replay, D2H of the step's outputs, all inside the timed region."""
+    import torch
+
+    out_host = torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory()
+    s = torch.cuda.current_stream()
+    for i in range(warmup):
+        wl.x_stage.copy_(wl.x_host[i % wl.x_host.shape[0]], non_blocking=True)
+        wl.graph.replay()
+        out_host.copy_(wl.out, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for i in range(steps):
+        wl.x_stage.copy_(wl.x_host[(warmup + i) % wl.x_host.shape[0]], non_blocking=True)
+        wl.graph.replay()
+        out_host.copy_(wl.out, non_blocking=True)
+    e1.record(s)
+    torch.cuda.synchronize()
+    h2d = wl.x_stage.numel() * wl.x_stage.element_size()
+    d2h = wl.out.numel() * wl.out.element_size()
+    return e0.elapsed_time(e1) / 1e3, h2d, d2h
+
+
+# --------------------------------------------------------------- the oracle --
+class OracleLayer:
+    """The CPU oracle on the same decode workload: route, resolve, fetch (a
+    copy) and the fp64 experts for one layer call."""
+
+    def __init__(self, cfg, T: int, phi: int, layers=(0, 1)):
+        import oracle
+        import synth
+
+        self.o, self.cfg, self.T, self.phi = oracle, cfg, T, phi
+        L, E, k, H, I, g = cfg.L, cfg.E, cfg.k, cfg.H, cfg.I, cfg.g
+        self.layers = list(layers)
+        _, self.stride = synth.block_layout(cfg.fmt, H, I, g)
+        # pool slice for the sampled layers, as the oracle reads it (flat ids)
+        import torch
+
+        self.blocks = {}
+        for l in self.layers:
+            blk = torch.empty((E, self.stride), dtype=torch.uint8)
+            synth.bank_blocks_torch(cfg.seed, range(l * E, (l + 1) * E), cfg.fmt, H, I, g, blk, ref_K=cfg.ref_K)
+            for e in range(E):
+                self.blocks[l * E + e] = blk[e].numpy()
+        self.W = {l: synth.router_weights(cfg.seed, l, E, H, cfg.router_std, zipf_bias=cfg.zipf)
+                  for l in self.layers}
+        self.st = oracle.CacheState(L, E, cfg.slots)
+        hist = synth.zipf_history(cfg.seed, L, E, k, cfg.history_steps)
+        for s in range(cfg.history_steps):
+            for l in range(L):
+                oracle.resolve(self.st, l, hist[s, l:l + 1], 65536, k)
+        xs = synth.normal_bf16(synth.stream_key(cfg.seed, "bench-x", T), (64, L, T, H))
+        xs[..., 0] = synth.bf16_bits(np.array([1.0], np.float32))[0]
+        self.xs = xs
+        self.ts = synth.tensor_scales(cfg.fmt, H, I, L * E)
+
+    def layer_call(self, i: int):
+        cfg, o = self.cfg, self.o
+        l = self.layers[i % len(self.layers)]
+        x = self.xs[i % self.xs.shape[0], l]
+        ids, w = o.route(x, self.W[l], cfg.k)
+        sl, nf, ff, fs = o.resolve(self.st, l, ids, self.phi)
+        out = np.zeros((self.T, cfg.H))
+        xv = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        for t in range(self.T):
+            for j in range(cfg.k):
+                f = l * cfg.E + int(ids[t, j])
+                y = o.expert(self.blocks[f], cfg.fmt, cfg.H, cfg.I, cfg.g, xv[t],
+                             None if self.ts is None else self.ts[f])
+                out[t] += float(np.float32(w[t, j])) * y
+        return out
+
+
+def oracle_rate(cfg, T, phi, budget_s: float = 15.0, min_calls: int = 2, max_calls: int = 10 ** 6):
+    ol = OracleLayer(cfg, T, phi)
+    t0 = time.perf_counter()
+    n = 0
+    while n < min_calls or (time.perf_counter() - t0 < budget_s and n < max_calls):
+        ol.layer_call(n)
+        n += 1
+    dt = time.perf_counter() - t0
+    return T * n / dt, n, dt
+
+
+def run_reference(args, cfg, T):
+    """The CPU oracle as the reference arm: each step one layer call for T tokens."""
+    import oracle
+
+    oracle.build()
+    ol = OracleLayer(cfg, T, args.phi)
+    for i in range(args.warmup):
+        ol.layer_call(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        ol.layer_call(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = T * args.steps / dt
+    sample = f"{args.steps} single-layer calls of {T} token(s) on layers {ol.layers} (of {cfg.L})"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{cfg.name} decode (35B-A3B-shaped int4 g64, 40x256 experts, top-8, "
+                               f"H2048, I512), T={T}, phi={args.phi}",
+                   "parallelism": "replicas" if args.gpus > 1 else "single"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------- main --
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--tokens", type=int, default=1, help="decode batch (1 or 8)")
+    ap.add_argument("--phi", type=int, default=65536, help="frac_q16 of the q* split")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--extra-batch", type=int, default=8, help="also time this batch (0: off)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    import synth
+
+    cfg = synth.get_config("d35b")
+    world, rank, local = dist_info()
+    log = (lambda *a: print(*a, file=sys.stderr, flush=True)) if rank == 0 else (lambda *a: None)
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, cfg, args.tokens)
+        return
+
+    import torch
+
+    import quantized_expert_ffn_router_gb300 as ft
+
+    from quantized_expert_ffn_router_gb300 import build as ftbuild
+
+    ftbuild.build()
+    ft.load()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    reduce_fn = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=device)
+        reduce_fn = torch_reduce_fn(device)
+
+    n_steps = args.steps + args.warmup
+    results = {}
+    batches = [args.tokens] + ([args.extra_batch] if args.extra_batch and args.extra_batch != args.tokens else [])
+    wl = None
+    for bi, T in enumerate(batches):
+        if wl is None:
+            wl = DecodeWorkload(cfg, T, args.phi, n_steps, device, log)
+        else:
+            wl = reshape_workload(wl, T, n_steps)
+        wl.capture()
+        clocks = ClockSampler(local) if bi == 0 else None
+        secs = time_device(wl, args.steps, args.warmup, reduce_fn, world, clocks)
+        units = T * cfg.L * args.steps
+        value, secs_max, units_all = aggregate(units, secs, world, reduce_fn)
+        kt = wl.kernel_times()
+        ebytes = wl.distinct_expert_bytes()
+        nfetch, host_pairs = wl.misses()
+        e2e_secs, h2d, d2h = time_e2e(wl, args.steps, args.warmup)
+        e2e_val, _, _ = aggregate(units, e2e_secs, world, reduce_fn)
+        results[T] = dict(value=value, secs=secs_max, kt=kt, ebytes=ebytes, nfetch=nfetch,
+                          host_pairs=host_pairs, e2e=e2e_val, h2d=h2d, d2h=d2h,
+                          clocks=clocks.summary() if clocks else None)
+        st = ft.get_status(wl.status)
+        if st != 0:
+            raise RuntimeError(f"device status {st} during the benchmark")
+        log(f"T={T}: {value:.1f} {UNIT}, {secs_max / args.steps * 1e3:.3f} ms/step, kernels {kt}")
+
+    if rank != 0:
+        return
+    peaks, peak_kind = measured_peaks()
+    r = results[args.tokens]
+    kt = r["kt"] or {}
+    dom = max(kt, key=kt.get) if kt else "experts"
+    exp_us = kt.get("experts")
+    roof = None
+    if exp_us:
+        achieved = r["ebytes"] / (exp_us * 1e-6) / 1e9  # GB/s over the 40 launches of the last step
+        roof = {"bound": "hbm", "kernel": "ft_moe_experts_fwd decode (gate/up + down)",
+                "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                "peak_kind": peak_kind, "frac_of_8tbs_nominal": achieved / 8000.0,
+                "algorithmic_bytes_per_launch": r["ebytes"] / cfg.L,
+                "dominant_op_by_time": dom}
+    cpu = None
+    if not args.no_cpu_baseline:
+        rate, n, dt = oracle_rate(cfg, args.tokens, args.phi)
+        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{n} single-layer calls of {args.tokens} token(s) (route, resolve, fp64 experts) "
+                         f"on 2 of 40 layers, {dt:.1f} s, single-threaded C++"}
+    launches_per_step = cfg.L * 6
+    line = {
+        "metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": r["secs"] / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int4-w/bf16-x/f32-acc", "data": "synthetic",
+        "config": {"workload": f"35B-A3B-shaped decode: 40 layers x 256 experts, top-8, H2048, I512, "
+                               f"int4 g64 (1,671,168 B/expert), cache 2560 slots (25%) from a Zipf(1.1) "
+                               f"history, pool in pinned host memory, T={args.tokens} tokens/step, "
+                               f"frac_q16={args.phi}",
+                   "tokens_per_step": args.tokens, "layers": cfg.L,
+                   "l2": "inputs larger than L2: each step streams "
+                         f"{r['ebytes'] / 1e6:.0f} MB of expert bytes (L2 129 MB)",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "clocks": r["clocks"],
+        "e2e": {"value": r["e2e"], "unit": UNIT, "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "detail": {
+            "model_tokens_per_s": r["value"] / cfg.L,
+            "per_op_us_per_step": kt,
+            "expert_bytes_per_step": r["ebytes"],
+            "fetched_experts_per_step": r["nfetch"],
+            "host_path_pairs_per_step": r["host_pairs"],
+            "other_batches": {str(T): {"value": v["value"], "ms_per_step": v["secs"] / args.steps * 1e3,
+                                       "per_op_us_per_step": v["kt"], "expert_bytes_per_step": v["ebytes"],
+                                       "e2e": v["e2e"]}
+                              for T, v in results.items() if T != args.tokens},
+        },
+    }
+    print(json.dumps(line), flush=True)
+
+
+def reshape_workload(wl, T, n_steps):
+    """Reuse pool, cache, router and warmed state for another batch size."""
+    import torch
+
+    import synth
+
+    cfg, dev, ft = wl.cfg, wl.dev, wl.ft
+    L, E, k, H = cfg.L, cfg.E, cfg.k, cfg.H
+    wl.T = T
+    xs = synth.normal_bf16(synth.stream_key(cfg.seed, "bench-x", T), (n_steps, L, T, H))
+    xs[..., 0] = synth.bf16_bits(np.array([1.0], np.float32))[0]
+    wl.x_host = torch.from_numpy(xs.view(np.int16)).pin_memory()
+    wl.x_all = wl.x_host.to(dev)
+    wl.x_stage = torch.empty((L, T, H), dtype=torch.int16, device=dev)
+    wl.out = torch.empty((L, T, H), dtype=torch.int16, device=dev)
+    wl.ids = torch.empty((L, T, k), dtype=torch.int32, device=dev)
+    wl.w = torch.empty((L, T, k), dtype=torch.float32, device=dev)
+    wl.slot = torch.empty((L, T, k), dtype=torch.int32, device=dev)
+    wl.ml = T * k
+    wl.ff = torch.empty((L, wl.ml), dtype=torch.int32, device=dev)
+    wl.fs = torch.empty((L, wl.ml), dtype=torch.int32, device=dev)
+    wl.rws = torch.empty(ft.route_workspace(T, E), dtype=torch.uint8, device=dev)
+    wl.ews = torch.empty(ft.experts_workspace(ft.FT_DECODE, T, k, H, cfg.I, E), dtype=torch.uint8, device=dev)
+    return wl
+
+
+if __name__ == "__main__":
+    main()

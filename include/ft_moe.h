@@ -72,7 +72,8 @@ enum {
   FT_ERR_UNSUPPORTED = 2,
   FT_ERR_CUDA = 3,
   FT_ERR_TIMEOUT = 4,   /* device: a bounded wait ran out */
-  FT_ERR_BAD_ID = 5     /* device: an expert id outside [0, E) */
+  FT_ERR_BAD_ID = 5,    /* device: an expert id outside [0, E) */
+  FT_ERR_RANGE = 6      /* device: an intermediate left the f16 range (|h| > 2^20) */
 };
 
 /* Expert weight formats. */
@@ -83,6 +84,7 @@ enum {
 
 enum { FT_DECODE = 0, FT_PREFILL = 1 };
 enum { FT_OUT_F32 = 0, FT_OUT_BF16 = 1 };
+enum { FT_XP_BF16 = 0, FT_XP_F16 = 1 };  /* permuted-batch formats of ft_moe_permute */
 
 /*
  * A bank: consecutive expert blocks (the pool indexed by flat id
@@ -219,18 +221,22 @@ FT_API ft_status ft_moe_fetch(const ft_bank* pool_host, const ft_bank* cache_hos
  *   FT_OUT_BF16) = sum over computed pairs of topk_w * y, combine fused.
  *   Each distinct expert's bytes are read once for all its tokens.  h is
  *   kept in fp32.  Limits: T*k <= 256, T <= 16.  offsets unused (NULL).
- * FT_PREFILL: x is the permuted batch Xp [T*k, H] bf16 from ft_moe_permute,
- *   offsets [E+1] its expert segments; slot_ids is a per-expert table [E]
- *   (block of expert e: cache[slot_ids[e]] when >= 0, else
- *   pool[layer*E + e]); raw_ids and topk_w unused (NULL); out = Yp
- *   [T*k, H] bf16 (FT_OUT_BF16), the unweighted expert rows, h rounded to
- *   bf16.  NVFP4 only.
+ * FT_PREFILL: x is the permuted batch Xp [T*k, H] in f16 as ft_moe_permute
+ *   writes it with FT_XP_F16, x_scale [T*k] its per-row factors; offsets
+ *   [E+1] its expert segments; slot_ids is a per-expert table [E] (the block
+ *   of expert e is cache[slot_ids[e]]; every expert with rows must be
+ *   resident, a -1 records FT_ERR_UNSUPPORTED); raw_ids and topk_w unused
+ *   (NULL); out = Yp [T*k, H] bf16 (FT_OUT_BF16), the unweighted expert
+ *   rows.  Runs on tcgen05 tensor cores with f16 operands: E2M1 x E4M3 is
+ *   exact in f16, h is kept as f16(h / 16) (FT_ERR_RANGE if |h| > 2^20).
+ *   NVFP4 only; H and I multiples of 256.
  * ws: device scratch of ft_moe_experts_workspace(...) bytes.
  */
 FT_API size_t ft_moe_experts_workspace(int32_t mode, int32_t T, int32_t k, int32_t H, int32_t I,
                                 int32_t E);
 FT_API ft_status ft_moe_experts_fwd(const ft_bank* cache_host, const ft_bank* pool_host, int32_t layer,
-                             int32_t E, const uint16_t* x, int32_t T, const int32_t* slot_ids,
+                             int32_t E, const uint16_t* x, const float* x_scale, int32_t T,
+                             const int32_t* slot_ids,
                              const int32_t* raw_ids, const float* topk_w, int32_t k,
                              int32_t mode, const int32_t* offsets, void* out, int32_t out_dtype,
                              void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
@@ -241,15 +247,18 @@ FT_API ft_status ft_moe_experts_fwd(const ft_bank* cache_host, const ft_bank* po
  * (NVMe post, step 5: the whole prompt through a layer's experts at once;
  * Edge0 "How it works": dedup, stack, gather).
  * topk_ids [T,k]; perm [T*k] (pair index t*k+j at each position); inv [T,k]
- * (position of each pair); offsets [E+1]; x [T,H] bf16 -> xp [T*k,H] bf16
- * (xp may be NULL to skip the gather).  ws: ft_moe_permute_workspace(T,k,E)
- * bytes.  An id outside [0, E) records FT_ERR_BAD_ID.  Limits: E <= 4096.
+ * (position of each pair); offsets [E+1]; x [T,H] bf16 -> xp [T*k,H]
+ * (NULL skips the gather).  xp_format FT_XP_BF16 copies the rows; FT_XP_F16
+ * writes f16(x * 2^-s) with s >= 0 the smallest power of two keeping the
+ * row below 2^15, and xp_scale[pos] = 2^s (exact; the grouped experts kernel
+ * multiplies its results by it).  ws: ft_moe_permute_workspace(T,k,E) bytes.
+ * An id outside [0, E) records FT_ERR_BAD_ID.  Limits: E <= 4096.
  */
 FT_API size_t ft_moe_permute_workspace(int32_t T, int32_t k, int32_t E);
 FT_API ft_status ft_moe_permute(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E,
                          const uint16_t* x, int32_t H, int32_t* perm, int32_t* inv,
-                         int32_t* offsets, uint16_t* xp, void* ws, size_t ws_bytes,
-                         int32_t* dev_status, void* stream);
+                         int32_t* offsets, uint16_t* xp, int32_t xp_format, float* xp_scale,
+                         void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /*
  * ft_moe_combine -- out[t] = sum_j topk_w[t,j] * yp[inv[t,j]] in j order,

@@ -99,6 +99,9 @@ def lib():
             L.orc_expert.restype = c.c_int
             L.orc_expert.argtypes = [c.c_void_p, c.c_int, c.c_int, c.c_int, c.c_int,
                                      c.c_void_p, c.c_void_p, c.c_void_p]
+            L.orc_expert_batch.restype = c.c_int
+            L.orc_expert_batch.argtypes = [c.c_void_p, c.c_int, c.c_int, c.c_int, c.c_int,
+                                           c.c_void_p, c.c_void_p, c.c_int, c.c_void_p]
             L.orc_moe_experts.restype = c.c_int
             L.orc_moe_experts.argtypes = [c.c_void_p, c.c_uint64, c.c_void_p, c.c_int, c.c_int,
                                           c.c_int, c.c_int, c.c_int, c.c_int, c.c_void_p,
@@ -282,6 +285,19 @@ def expert(block: np.ndarray, fmt: int, H: int, I: int, g: int, x: np.ndarray,
     if rc != 0:
         raise ValueError("bad expert arguments")
     return y
+
+
+def expert_batch(block: np.ndarray, fmt: int, H: int, I: int, g: int, X: np.ndarray,
+                 tscale3=None) -> np.ndarray:
+    """expert(x) for every row of X [n, H] (fp64), one dequantisation."""
+    block = _c(block, np.uint8)
+    X = _c(X, np.float64)
+    ts = None if tscale3 is None else _c(tscale3, np.float32)
+    Y = np.empty_like(X)
+    rc = lib().orc_expert_batch(_ptr(block), fmt, H, I, g, _ptr(ts), _ptr(X), X.shape[0], _ptr(Y))
+    if rc != 0:
+        raise ValueError("bad expert_batch arguments")
+    return Y
 
 
 def moe_experts(pool: np.ndarray, stride: int, tscales, fmt: int, H: int, I: int, g: int,

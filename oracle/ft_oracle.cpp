@@ -438,6 +438,40 @@ int orc_expert(const uint8_t* block, int fmt, int H, int I, int g,
   return 0;
 }
 
+// The same expert on n input vectors (rows of x, fp64): y[r] = expert(x[r]).
+// One dequantisation serves all rows; the per-row arithmetic is expert_forward's.
+int orc_expert_batch(const uint8_t* block, int fmt, int H, int I, int g, const float* tscale3,
+                     const double* x, int n, double* y) {
+  Layout L;
+  if (!make_layout(fmt, H, I, g, &L)) return -1;
+  std::vector<double> G(static_cast<size_t>(I) * H), U(G.size()), D(G.size());
+  double ts[3] = {1.0, 1.0, 1.0};
+  if (fmt == FMT_NVFP4 && tscale3)
+    for (int i = 0; i < 3; ++i) ts[i] = tscale3[i];
+  dequant_matrix(fmt, block + L.off[0], block + L.off[3], I, H, g, ts[0], G.data());
+  dequant_matrix(fmt, block + L.off[1], block + L.off[4], I, H, g, ts[1], U.data());
+  dequant_matrix(fmt, block + L.off[2], block + L.off[5], H, I, g, ts[2], D.data());
+  std::vector<double> h(I);
+  for (int r = 0; r < n; ++r) {
+    const double* xr = x + static_cast<size_t>(r) * H;
+    for (int i = 0; i < I; ++i) {
+      double gs = 0.0, us = 0.0;
+      for (int c = 0; c < H; ++c) {
+        gs += G[static_cast<size_t>(i) * H + c] * xr[c];
+        us += U[static_cast<size_t>(i) * H + c] * xr[c];
+      }
+      h[i] = silu(gs) * us;
+    }
+    double* yr = y + static_cast<size_t>(r) * H;
+    for (int c = 0; c < H; ++c) {
+      double acc = 0.0;
+      for (int i = 0; i < I; ++i) acc += D[static_cast<size_t>(c) * I + i] * h[i];
+      yr[c] = acc;
+    }
+  }
+  return 0;
+}
+
 // The routed layer output over a pool bank (the source of truth): for every
 // pair (t, j) with include[t*k+j] != 0 (all pairs when include is NULL),
 //   out[t] += w[t,j] * expert(layer*E + ids[t,j]) (x[t]),

@@ -15,10 +15,11 @@ import os
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libft_moe.so")
 
-FT_OK, FT_ERR_INVALID, FT_ERR_UNSUPPORTED, FT_ERR_CUDA, FT_ERR_TIMEOUT, FT_ERR_BAD_ID = range(6)
+FT_OK, FT_ERR_INVALID, FT_ERR_UNSUPPORTED, FT_ERR_CUDA, FT_ERR_TIMEOUT, FT_ERR_BAD_ID, FT_ERR_RANGE = range(7)
 FT_INT4, FT_NVFP4 = 0, 1
 FT_DECODE, FT_PREFILL = 0, 1
 FT_OUT_F32, FT_OUT_BF16 = 0, 1
+FT_XP_BF16, FT_XP_F16 = 0, 1
 
 _lib = None
 
@@ -54,10 +55,11 @@ _SIGS = {
     "ft_moe_resolve_slots": (_I32, [_V, _I32, _V, _I32, _I32, _I32, _V, _V, _V, _V, _I32, _V, _V]),
     "ft_moe_fetch": (_I32, [_V, _V, _V, _V, _V, _I32, _V, _V]),
     "ft_moe_experts_workspace": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
-    "ft_moe_experts_fwd": (_I32, [_V, _V, _I32, _I32, _V, _I32, _V, _V, _V, _I32, _I32, _V, _V,
+    "ft_moe_experts_fwd": (_I32, [_V, _V, _I32, _I32, _V, _V, _I32, _V, _V, _V, _I32, _I32, _V, _V,
                                   _I32, _V, _SZ, _V, _V]),
     "ft_moe_permute_workspace": (_SZ, [_I32, _I32, _I32]),
-    "ft_moe_permute": (_I32, [_V, _I32, _I32, _I32, _V, _I32, _V, _V, _V, _V, _V, _SZ, _V, _V]),
+    "ft_moe_permute": (_I32, [_V, _I32, _I32, _I32, _V, _I32, _V, _V, _V, _V, _I32, _V, _V, _SZ, _V,
+                              _V]),
     "ft_moe_combine": (_I32, [_V, _V, _V, _I32, _I32, _I32, _V, _V, _V]),
 }
 
@@ -183,12 +185,12 @@ def experts_workspace(mode: int, T: int, k: int, H: int, I: int, E: int) -> int:
 
 
 def experts_fwd(cache: FtBank, pool, layer: int, E: int, x, T: int, k: int, slot_ids, raw_ids, topk_w,
-                out, ws, mode: int = FT_DECODE, offsets=None, dev_status=None, stream=None):
+                out, ws, mode: int = FT_DECODE, offsets=None, dev_status=None, stream=None, x_scale=None):
     import torch
 
     out_dtype = FT_OUT_BF16 if out.dtype in (torch.bfloat16, torch.int16, torch.uint16) else FT_OUT_F32
     _check(load().ft_moe_experts_fwd(ctypes.byref(cache), None if pool is None else ctypes.byref(pool),
-                                     layer, E, _ptr(x), T, _ptr(slot_ids), _ptr(raw_ids),
+                                     layer, E, _ptr(x), _ptr(x_scale), T, _ptr(slot_ids), _ptr(raw_ids),
                                      _ptr(topk_w), k, mode, _ptr(offsets), _ptr(out), out_dtype,
                                      _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status),
                                      _stream(stream)))
@@ -198,12 +200,15 @@ def permute_workspace(T: int, k: int, E: int) -> int:
     return int(load().ft_moe_permute_workspace(T, k, E))
 
 
-def permute(topk_ids, E: int, x, perm, inv, offsets, xp, ws, dev_status=None, stream=None):
+def permute(topk_ids, E: int, x, perm, inv, offsets, xp, ws, dev_status=None, stream=None,
+            xp_scale=None):
+    """xp_scale given: xp is written as f16 with per-row power-of-two factors."""
     T, k = topk_ids.shape
     H = 0 if x is None else x.shape[1]
+    fmt = FT_XP_BF16 if xp_scale is None else FT_XP_F16
     _check(load().ft_moe_permute(_ptr(topk_ids), T, k, E, _ptr(x), H, _ptr(perm), _ptr(inv),
-                                 _ptr(offsets), _ptr(xp), _ptr(ws), ws.numel() * ws.element_size(),
-                                 _ptr(dev_status), _stream(stream)))
+                                 _ptr(offsets), _ptr(xp), fmt, _ptr(xp_scale), _ptr(ws),
+                                 ws.numel() * ws.element_size(), _ptr(dev_status), _stream(stream)))
 
 
 def combine(yp, inv, topk_w, out, host_partial=None, stream=None):

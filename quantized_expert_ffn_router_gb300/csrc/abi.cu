@@ -97,6 +97,7 @@ const char* ft_status_string(ft_status s) {
     case FT_ERR_CUDA: return "CUDA launch error";
     case FT_ERR_TIMEOUT: return "device wait timed out";
     case FT_ERR_BAD_ID: return "expert id out of range";
+    case FT_ERR_RANGE: return "intermediate outside the f16 range";
     default: return "unknown status";
   }
 }

@@ -479,7 +479,7 @@ ft_status ft_moe_fetch(const ft_bank* pool, const ft_bank* cache, const int32_t*
   const uint64_t per = static_cast<uint64_t>(ft::kFetchThreads) * ft::kFetchVec;
   const uint64_t nchunks = (n16 + per - 1) / per;
   const uint64_t items = nchunks * static_cast<uint64_t>(max_list);
-  const int grid = static_cast<int>(std::min<uint64_t>(items, static_cast<uint64_t>(ft::num_sms()) * 4));
+  const int grid = static_cast<int>(std::min<uint64_t>(items, static_cast<uint64_t>(ft::num_sms())));
   ft::fetch_kernel<<<grid, ft::kFetchThreads, 0, ft::as_stream(stream)>>>(
       static_cast<const uint8_t*>(pool->base), pool->stride,
       static_cast<uint8_t*>(const_cast<void*>(cache->base)), cache->stride, n16, num_fetch,

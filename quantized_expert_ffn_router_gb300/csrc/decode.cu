@@ -21,125 +21,15 @@
 // Every expert's bytes cross HBM exactly once per call.
 #include <cuda_fp16.h>
 
-#include "ft_common.cuh"
+#include "ft_decode.cuh"
 
 namespace ft {
 namespace {
 
-constexpr int kMaxPairs = 256;
-constexpr int kMaxTok = 16;
 constexpr int kRowsPerCta = 16;  // 8 warps x 2 rows
 constexpr int kThreads = 256;
 constexpr int kPad = 36;         // floats per 32-element chunk in shared memory (bank spread)
 constexpr size_t kSmemLimit = 160 * 1024;
-
-struct DecArgs {
-  const uint8_t* cache;
-  uint64_t cstride;
-  int64_t cblocks;
-  const uint8_t* pool;  // may be null
-  uint64_t pstride;
-  int64_t pblocks;
-  const float* tscale;  // [n_fids, 3] or null
-  uint64_t off[6];
-  int H, I, group, layer, E, T, k;
-  const uint16_t* x;
-  const int32_t* slot_ids;
-  const int32_t* raw_ids;
-  const float* topk_w;
-  float* h;             // [T*k, I] fp32
-  void* out;
-  int out_bf16;
-  int32_t* dev_status;
-};
-
-// The pair -> distinct-expert grouping, rebuilt by every CTA in shared memory.
-struct Groups {
-  int nD;
-  int nValid;
-  int dStart[kMaxPairs + 1];
-  int dExpert[kMaxPairs];
-  const uint8_t* dBlock[kMaxPairs];
-  int sortedPair[kMaxPairs];  // valid pairs ordered by (distinct expert, pair)
-};
-
-__device__ void build_groups(const DecArgs& a, Groups& g) {
-  __shared__ int s_e[kMaxPairs];
-  __shared__ int s_first[kMaxPairs];
-  __shared__ int s_d[kMaxPairs];
-  __shared__ const uint8_t* s_blk[kMaxPairs];
-  const int n = a.T * a.k;
-  for (int p = threadIdx.x; p < n; p += blockDim.x) {
-    int e = a.raw_ids[p];
-    const int s = a.slot_ids[p];
-    const uint8_t* blk = nullptr;
-    if (e < 0 || e >= a.E) {
-      if (blockIdx.x == 0) record_status(a.dev_status, FT_ERR_BAD_ID);
-      e = -1;
-    } else if (s >= 0) {
-      if (s < a.cblocks)
-        blk = a.cache + static_cast<uint64_t>(s) * a.cstride;
-      else if (blockIdx.x == 0)
-        record_status(a.dev_status, FT_ERR_BAD_ID);
-    } else if (a.pool != nullptr) {
-      const int64_t fid = static_cast<int64_t>(a.layer) * a.E + e;
-      if (fid < a.pblocks)
-        blk = a.pool + static_cast<uint64_t>(fid) * a.pstride;
-      else if (blockIdx.x == 0)
-        record_status(a.dev_status, FT_ERR_BAD_ID);
-    }
-    if (blk == nullptr) e = -1;  // skipped pair: masked or invalid
-    s_e[p] = e;
-    s_blk[p] = blk;
-  }
-  __syncthreads();
-  for (int p = threadIdx.x; p < n; p += blockDim.x) {
-    const int e = s_e[p];
-    int first = (e >= 0);
-    for (int q = 0; q < p && first; ++q) first = (s_e[q] != e);
-    s_first[p] = first;
-  }
-  __syncthreads();
-  for (int p = threadIdx.x; p < n; p += blockDim.x) {
-    const int e = s_e[p];
-    int d = -1;
-    if (e >= 0) {
-      d = 0;
-      for (int q = 0; q < n; ++q) d += (s_first[q] && s_e[q] < e);
-    }
-    s_d[p] = d;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int nD = 0, nV = 0;
-    for (int p = 0; p < n; ++p) {
-      nD += s_first[p];
-      nV += (s_e[p] >= 0);
-    }
-    g.nD = nD;
-    g.nValid = nV;
-  }
-  // per-distinct start offsets: count of valid pairs with a smaller d
-  for (int p = threadIdx.x; p < n; p += blockDim.x) {
-    if (!s_first[p]) continue;
-    const int d = s_d[p];
-    int start = 0;
-    for (int q = 0; q < n; ++q) start += (s_d[q] >= 0 && s_d[q] < d);
-    g.dStart[d] = start;
-    g.dExpert[d] = s_e[p];
-    g.dBlock[d] = s_blk[p];
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) g.dStart[g.nD] = g.nValid;
-  for (int p = threadIdx.x; p < n; p += blockDim.x) {
-    const int d = s_d[p];
-    if (d < 0) continue;
-    int r = 0;
-    for (int q = 0; q < p; ++q) r += (s_d[q] == d);
-    g.sortedPair[g.dStart[d] + r] = p;
-  }
-  __syncthreads();
-}
 
 // ------------------------------------------------------------ dequant-dot --
 // Dot of one 16-byte chunk (32 codes) with 32 fp32 inputs in shared memory.
@@ -255,20 +145,9 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(DecArgs a) {
   const int d = blockIdx.x / tiles, rb = blockIdx.x % tiles;
   if (d >= g.nD) return;
   const uint8_t* blk = g.dBlock[d];
-  const int p0 = g.dStart[d], nt = g.dStart[d + 1] - p0;
+  const int p0all = g.dStart[d], npairs = g.dStart[d + 1] - p0all;
   const int HC = a.H / 32;  // 32-element chunks per row
   const int xstride = HC * kPad;
-  // stage x of this expert's tokens as fp32, chunk-padded
-  for (int i = threadIdx.x; i < nt * (a.H / 8); i += blockDim.x) {
-    const int t = i / (a.H / 8), c8 = i % (a.H / 8);
-    const int tok = g.sortedPair[p0 + t] / a.k;
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(tok) * a.H) + c8);
-    const int kk = c8 * 8;
-    float* dst = xs + t * xstride + (kk / 32) * kPad + (kk % 32);
-    *reinterpret_cast<float4*>(dst) = make_float4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y));
-    *reinterpret_cast<float4*>(dst + 4) = make_float4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w));
-  }
-  __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float tsg = 1.f, tsu = 1.f;
   if constexpr (FMT == FT_NVFP4) {
@@ -279,47 +158,63 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(DecArgs a) {
   const uint64_t srow_bytes = (FMT == FT_INT4) ? static_cast<uint64_t>(a.H / a.group) * 2
                                                : static_cast<uint64_t>(a.H / 16);
   constexpr int kMaxIt = 4;  // H <= 4096
-  for (int rr = 0; rr < 2; ++rr) {
-    const int r = rb * kRowsPerCta + warp * 2 + rr;
-    const uint8_t* grow = blk + a.off[0] + static_cast<uint64_t>(r) * (a.H / 2);
-    const uint8_t* urow = blk + a.off[1] + static_cast<uint64_t>(r) * (a.H / 2);
-    const uint8_t* gsrow = blk + a.off[3] + r * srow_bytes;
-    const uint8_t* usrow = blk + a.off[4] + r * srow_bytes;
-    uint4 wg[kMaxIt], wu[kMaxIt];
-    uint32_t sg[kMaxIt], su[kMaxIt];
-#pragma unroll
-    for (int it = 0; it < kMaxIt; ++it) {
-      const int c = lane + 32 * it;
-      if (c < HC) {
-        wg[it] = __ldg(reinterpret_cast<const uint4*>(grow) + c);
-        wu[it] = __ldg(reinterpret_cast<const uint4*>(urow) + c);
-        sg[it] = load_scale<FMT>(gsrow, c, a.group);
-        su[it] = load_scale<FMT>(usrow, c, a.group);
-      }
+  // The pairs of this expert, NT at a time (more than NT only when one token
+  // lists the same expert twice): x of those pairs is staged as fp32.
+  for (int c0 = 0; c0 < npairs; c0 += NT) {
+    const int p0 = p0all + c0, nt = min(NT, npairs - c0);
+    __syncthreads();
+    for (int i = threadIdx.x; i < nt * (a.H / 8); i += blockDim.x) {
+      const int t = i / (a.H / 8), c8 = i % (a.H / 8);
+      const int tok = g.sortedPair[p0 + t] / a.k;
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(tok) * a.H) + c8);
+      const int kk = c8 * 8;
+      float* dst = xs + t * xstride + (kk / 32) * kPad + (kk % 32);
+      *reinterpret_cast<float4*>(dst) = make_float4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y));
+      *reinterpret_cast<float4*>(dst + 4) = make_float4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w));
     }
-    float ag[NT], au[NT];
+    __syncthreads();
+    for (int rr = 0; rr < 2; ++rr) {
+      const int r = rb * kRowsPerCta + warp * 2 + rr;
+      const uint8_t* grow = blk + a.off[0] + static_cast<uint64_t>(r) * (a.H / 2);
+      const uint8_t* urow = blk + a.off[1] + static_cast<uint64_t>(r) * (a.H / 2);
+      const uint8_t* gsrow = blk + a.off[3] + r * srow_bytes;
+      const uint8_t* usrow = blk + a.off[4] + r * srow_bytes;
+      uint4 wg[kMaxIt], wu[kMaxIt];
+      uint32_t sg[kMaxIt], su[kMaxIt];
 #pragma unroll
-    for (int t = 0; t < NT; ++t) ag[t] = au[t] = 0.f;
+      for (int it = 0; it < kMaxIt; ++it) {
+        const int c = lane + 32 * it;
+        if (c < HC) {
+          wg[it] = __ldg(reinterpret_cast<const uint4*>(grow) + c);
+          wu[it] = __ldg(reinterpret_cast<const uint4*>(urow) + c);
+          sg[it] = load_scale<FMT>(gsrow, c, a.group);
+          su[it] = load_scale<FMT>(usrow, c, a.group);
+        }
+      }
+      float ag[NT], au[NT];
 #pragma unroll
-    for (int it = 0; it < kMaxIt; ++it) {
-      const int c = lane + 32 * it;
-      if (c >= HC) break;
+      for (int t = 0; t < NT; ++t) ag[t] = au[t] = 0.f;
+#pragma unroll
+      for (int it = 0; it < kMaxIt; ++it) {
+        const int c = lane + 32 * it;
+        if (c >= HC) break;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          if (t >= nt) break;
+          const float* xc = xs + t * xstride + c * kPad;
+          ag[t] += chunk_dot<FMT>(wg[it], sg[it], xc);
+          au[t] += chunk_dot<FMT>(wu[it], su[it], xc);
+        }
+      }
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
         if (t >= nt) break;
-        const float* xc = xs + t * xstride + c * kPad;
-        ag[t] += chunk_dot<FMT>(wg[it], sg[it], xc);
-        au[t] += chunk_dot<FMT>(wu[it], su[it], xc);
-      }
-    }
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      if (t >= nt) break;
-      const float gv = warp_sum(ag[t]) * tsg;
-      const float uv = warp_sum(au[t]) * tsu;
-      if (lane == 0) {
-        const int p = g.sortedPair[p0 + t];
-        a.h[static_cast<size_t>(p) * a.I + r] = silu(gv) * uv;
+        const float gv = warp_sum(ag[t]) * tsg;
+        const float uv = warp_sum(au[t]) * tsu;
+        if (lane == 0) {
+          const int p = g.sortedPair[p0 + t];
+          a.h[static_cast<size_t>(p) * a.I + r] = silu(gv) * uv;
+        }
       }
     }
   }
@@ -328,14 +223,12 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(DecArgs a) {
 // ------------------------------------------------------------------ down ---
 template <int FMT, int NT>
 __global__ void __launch_bounds__(kThreads) down_kernel(DecArgs a) {
-  extern __shared__ __align__(16) float hs[];
   __shared__ Groups g;
   __shared__ float s_w[kMaxPairs];
   __shared__ int s_tok[kMaxPairs];
   __shared__ float s_tsd[kMaxPairs];
   build_groups(a, g);
   const int IC = a.I / 32;
-  const int hstride = IC * kPad;
   const int nV = g.nValid;
   for (int q = threadIdx.x; q < nV; q += blockDim.x) {
     const int p = g.sortedPair[q];
@@ -346,12 +239,6 @@ __global__ void __launch_bounds__(kThreads) down_kernel(DecArgs a) {
     float ts = 1.f;
     if constexpr (FMT == FT_NVFP4) ts = __ldg(a.tscale + 3 * (static_cast<int64_t>(a.layer) * a.E + g.dExpert[d]) + 2);
     s_tsd[d] = ts;
-  }
-  for (int i = threadIdx.x; i < nV * (a.I / 4); i += blockDim.x) {
-    const int q = i / (a.I / 4), c4 = i % (a.I / 4);
-    const float4 v = *reinterpret_cast<const float4*>(a.h + static_cast<size_t>(g.sortedPair[q]) * a.I + c4 * 4);
-    const int kk = c4 * 4;
-    *reinterpret_cast<float4*>(hs + q * hstride + (kk / 32) * kPad + (kk % 32)) = v;
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -383,7 +270,8 @@ __global__ void __launch_bounds__(kThreads) down_kernel(DecArgs a) {
         const int d = it / IC, c = it % IC;
         const float ts = s_tsd[d];
         for (int q = g.dStart[d]; q < g.dStart[d + 1]; ++q) {
-          const float part = chunk_dot<FMT>(w[u], sc[u], hs + q * hstride + c * kPad);
+          // h rows are read straight from the workspace (L1-cached)
+          const float part = chunk_dot<FMT>(w[u], sc[u], a.h + static_cast<size_t>(g.sortedPair[q]) * a.I + 32 * c);
           const int tok = s_tok[q];
           const float wt = s_w[q] * ts;
 #pragma unroll
@@ -409,22 +297,23 @@ __global__ void __launch_bounds__(kThreads) down_kernel(DecArgs a) {
 template <int FMT, int NT>
 ft_status launch_decode(const DecArgs& a, cudaStream_t s) {
   const int n = a.T * a.k;
-  const size_t xsm = static_cast<size_t>(NT) * (a.H / 32) * kPad * sizeof(float);
-  const size_t hsm = static_cast<size_t>(n) * (a.I / 32) * kPad * sizeof(float);
+  const size_t xsm = static_cast<size_t>(NT < 8 ? NT : 8) * (a.H / 32) * kPad * sizeof(float);
   static bool attr_done = false;
   if (!attr_done) {
-    cudaFuncSetAttribute(gateup_kernel<FMT, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(gateup_kernel<FMT, (NT < 8 ? NT : 8)>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(kSmemLimit));
     cudaFuncSetAttribute(down_kernel<FMT, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(kSmemLimit));
     attr_done = true;
   }
   const int grid1 = n * (a.I / kRowsPerCta);
-  gateup_kernel<FMT, NT><<<grid1, kThreads, xsm, s>>>(a);
+  // gate/up stages x for at most 8 tokens at a time (more pairs take passes)
+  constexpr int NTX = NT < 8 ? NT : 8;
+  gateup_kernel<FMT, NTX><<<grid1, kThreads, xsm, s>>>(a);
   ft_status st = launch_check("experts decode gate/up");
   if (st != FT_OK) return st;
   const int grid2 = a.H / kRowsPerCta;
-  down_kernel<FMT, NT><<<grid2, kThreads, hsm, s>>>(a);
+  down_kernel<FMT, NT><<<grid2, kThreads, 0, s>>>(a);
   return launch_check("experts decode down");
 }
 
@@ -432,9 +321,9 @@ ft_status launch_decode(const DecArgs& a, cudaStream_t s) {
 
 // Prefill (grouped GEMM) lives in prefill.cu.
 ft_status experts_prefill(const ft_bank* cache, const ft_bank* pool, int32_t layer, int32_t E,
-                          const uint16_t* xp, int32_t T, int32_t k, const int32_t* slot_of_expert,
-                          const int32_t* offsets, uint16_t* yp, void* ws, size_t ws_bytes,
-                          int32_t* dev_status, cudaStream_t s);
+                          const uint16_t* xp, const float* x_scale, int32_t T, int32_t k,
+                          const int32_t* slot_of_expert, const int32_t* offsets, uint16_t* yp, void* ws,
+                          size_t ws_bytes, int32_t* dev_status, cudaStream_t s);
 size_t experts_prefill_workspace(int32_t T, int32_t k, int32_t H, int32_t I, int32_t E);
 
 }  // namespace ft
@@ -449,7 +338,7 @@ size_t ft_moe_experts_workspace(int32_t mode, int32_t T, int32_t k, int32_t H, i
 }
 
 ft_status ft_moe_experts_fwd(const ft_bank* cache, const ft_bank* pool, int32_t layer, int32_t E,
-                             const uint16_t* x, int32_t T, const int32_t* slot_ids,
+                             const uint16_t* x, const float* x_scale, int32_t T, const int32_t* slot_ids,
                              const int32_t* raw_ids, const float* topk_w, int32_t k, int32_t mode,
                              const int32_t* offsets, void* out, int32_t out_dtype, void* ws,
                              size_t ws_bytes, int32_t* dev_status, void* stream) {
@@ -471,7 +360,7 @@ ft_status ft_moe_experts_fwd(const ft_bank* cache, const ft_bank* pool, int32_t 
     FT_REQUIRE(out_dtype == FT_OUT_BF16, "experts prefill: output must be bf16");
     if (T == 0) return FT_OK;
     FT_REQUIRE(x && slot_ids && offsets && out && ws, "experts prefill: NULL pointer");
-    return ft::experts_prefill(cache, pool, layer, E, x, T, k, slot_ids, offsets,
+    return ft::experts_prefill(cache, pool, layer, E, x, x_scale, T, k, slot_ids, offsets,
                                static_cast<uint16_t*>(out), ws, ws_bytes, dev_status, s);
   }
   FT_REQUIRE(mode == FT_DECODE, "experts: unknown mode %d", mode);
@@ -488,10 +377,9 @@ ft_status ft_moe_experts_fwd(const ft_bank* cache, const ft_bank* pool, int32_t 
   FT_REQUIRE(ws_bytes >= ft_moe_experts_workspace(FT_DECODE, T, k, cache->H, cache->I, E),
              "experts decode: workspace too small");
   const int NT = T <= 1 ? 1 : (T <= 4 ? 4 : 16);
-  const size_t xsm = static_cast<size_t>(NT) * (cache->H / 32) * ft::kPad * sizeof(float);
-  const size_t hsm = static_cast<size_t>(n) * (cache->I / 32) * ft::kPad * sizeof(float);
-  if (xsm > ft::kSmemLimit || hsm > ft::kSmemLimit)
-    return ft::fail(FT_ERR_UNSUPPORTED, "experts decode: T*H or T*k*I too large for one pass");
+  const size_t xsm = static_cast<size_t>(NT < 8 ? NT : 8) * (cache->H / 32) * ft::kPad * sizeof(float);
+  if (xsm > ft::kSmemLimit)
+    return ft::fail(FT_ERR_UNSUPPORTED, "experts decode: T*H too large for one pass");
   ft::DecArgs a;
   a.cache = static_cast<const uint8_t*>(cache->base);
   a.cstride = cache->stride;
@@ -500,6 +388,7 @@ ft_status ft_moe_experts_fwd(const ft_bank* cache, const ft_bank* pool, int32_t 
   a.pstride = pool ? pool->stride : 0;
   a.pblocks = pool ? pool->n_blocks : 0;
   a.tscale = cache->tensor_scale;
+  a.fmt = cache->fmt;
   for (int i = 0; i < 6; ++i) a.off[i] = L.off[i];
   a.H = cache->H;
   a.I = cache->I;
@@ -516,6 +405,8 @@ ft_status ft_moe_experts_fwd(const ft_bank* cache, const ft_bank* pool, int32_t 
   a.out = out;
   a.out_bf16 = (out_dtype == FT_OUT_BF16);
   a.dev_status = dev_status;
+  st = ft::decode_streaming(a, s);
+  if (st != FT_ERR_UNSUPPORTED) return st;
   if (cache->fmt == FT_INT4) {
     if (NT == 1) return ft::launch_decode<FT_INT4, 1>(a, s);
     if (NT == 4) return ft::launch_decode<FT_INT4, 4>(a, s);

@@ -50,6 +50,16 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
   return static_cast<uint16_t>(u >> 16);
 }
 
+// Power-of-two factor that keeps |v| * factor below 2^16 in f16 (1 when it
+// already is): exact scaling, undone by the caller with 1/factor.
+__device__ __forceinline__ float f16_prescale(float amax) {
+  if (!(amax < 32768.f)) {
+    if (!isfinite(amax)) return 1.f;
+    return ldexpf(1.f, 14 - ilogbf(amax));
+  }
+  return 1.f;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

@@ -12,6 +12,8 @@
 // three passes over 256-pair chunks: per-chunk histograms, one scan over the
 // (expert, chunk) table in expert-major order, and an in-order scatter in
 // which the chunk's warps take turns so equal experts keep pair order.
+#include <cuda_fp16.h>
+
 #include "ft_common.cuh"
 
 namespace ft {
@@ -19,6 +21,11 @@ namespace {
 
 constexpr int kChunk = 256;
 constexpr int kMaxE = 4096;
+
+__device__ __forceinline__ uint32_t __halves2half2_bits(float lo, float hi) {
+  return static_cast<uint32_t>(__half_as_ushort(__float2half_rn(lo))) |
+         (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(hi))) << 16);
+}
 
 __global__ void __launch_bounds__(kChunk) perm_count_kernel(const int32_t* __restrict__ ids, int n,
                                                             int E, int nchunks,
@@ -112,6 +119,40 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
   }
 }
 
+// xp[pos] = f16(x[perm[pos] / k] * f), f the power of two that keeps the row
+// below 2^15 (1 for ordinary rows), xp_scale[pos] = 1/f.  One warp per row.
+__global__ void __launch_bounds__(256) gather_f16_kernel(const uint16_t* __restrict__ x, int H, int k,
+                                                         const int32_t* __restrict__ perm, int n,
+                                                         uint16_t* __restrict__ xp,
+                                                         float* __restrict__ xp_scale) {
+  const int lane = threadIdx.x & 31;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  for (int pos = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; pos < n; pos += nw) {
+    const int t = perm[pos] / k;
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
+    float m = 0.f;
+    for (int c = lane; c < H / 8; c += 32) {
+      const uint4 v = __ldg(src + c);
+      m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))), fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y)))));
+      m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z))), fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w)))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float f = f16_prescale(m);
+    uint4* dst = reinterpret_cast<uint4*>(xp + static_cast<size_t>(pos) * H);
+    for (int c = lane; c < H / 8; c += 32) {
+      const uint4 v = __ldg(src + c);
+      uint4 o;
+      o.x = __halves2half2_bits(bf16_lo(v.x) * f, bf16_hi(v.x) * f);
+      o.y = __halves2half2_bits(bf16_lo(v.y) * f, bf16_hi(v.y) * f);
+      o.z = __halves2half2_bits(bf16_lo(v.z) * f, bf16_hi(v.z) * f);
+      o.w = __halves2half2_bits(bf16_lo(v.w) * f, bf16_hi(v.w) * f);
+      dst[c] = o;
+    }
+    if (lane == 0) xp_scale[pos] = 1.f / f;
+  }
+}
+
 // out[t] = host_partial[t] + sum_j w[t,j] * yp[inv[t,j]] (j order, fp32), bf16.
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ yp,
                                                       const int32_t* __restrict__ inv,
@@ -173,8 +214,8 @@ size_t ft_moe_permute_workspace(int32_t T, int32_t k, int32_t E) {
 
 ft_status ft_moe_permute(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E,
                          const uint16_t* x, int32_t H, int32_t* perm, int32_t* inv,
-                         int32_t* offsets, uint16_t* xp, void* ws, size_t ws_bytes,
-                         int32_t* dev_status, void* stream) {
+                         int32_t* offsets, uint16_t* xp, int32_t xp_format, float* xp_scale,
+                         void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
   FT_REQUIRE(T >= 0 && k >= 1, "permute: T=%d k=%d", T, k);
   FT_REQUIRE(E >= 1 && E <= ft::kMaxE, "permute: E %d outside [1, %d]", E, ft::kMaxE);
   const int64_t n64 = static_cast<int64_t>(T) * k;
@@ -189,7 +230,9 @@ ft_status ft_moe_permute(const int32_t* topk_ids, int32_t T, int32_t k, int32_t 
   FT_REQUIRE(topk_ids && perm && inv && ws, "permute: NULL pointer");
   FT_REQUIRE(ws_bytes >= ft_moe_permute_workspace(T, k, E), "permute: workspace %zu < %zu",
              ws_bytes, ft_moe_permute_workspace(T, k, E));
+  FT_REQUIRE(xp_format == FT_XP_BF16 || xp_format == FT_XP_F16, "permute: unknown xp_format %d", xp_format);
   if (xp) {
+    FT_REQUIRE(xp_format == FT_XP_BF16 || xp_scale != nullptr, "permute: FT_XP_F16 needs xp_scale");
     FT_REQUIRE(x != nullptr && H > 0 && H % 8 == 0, "permute: gather needs x and H %% 8 == 0");
     FT_REQUIRE(reinterpret_cast<uintptr_t>(x) % 16 == 0 && reinterpret_cast<uintptr_t>(xp) % 16 == 0,
                "permute: x and xp must be 16-byte aligned");
@@ -208,7 +251,12 @@ ft_status ft_moe_permute(const int32_t* topk_ids, int32_t T, int32_t k, int32_t 
   if (xp) {
     const size_t total = static_cast<size_t>(n) * (H / 8);
     const int grid = static_cast<int>(std::min<size_t>((total + 255) / 256, static_cast<size_t>(ft::sms()) * 16));
-    ft::gather_kernel<<<grid, 256, 0, s>>>(x, H, k, perm, n, xp);
+    if (xp_format == FT_XP_BF16) {
+      ft::gather_kernel<<<grid, 256, 0, s>>>(x, H, k, perm, n, xp);
+    } else {
+      const int g2 = std::min((n + 7) / 8, ft::sms() * 16);
+      ft::gather_f16_kernel<<<g2, 256, 0, s>>>(x, H, k, perm, n, xp, xp_scale);
+    }
     if ((st = ft::launch_check("permute gather")) != FT_OK) return st;
   }
   return FT_OK;

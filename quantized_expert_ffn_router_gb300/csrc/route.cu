@@ -4,10 +4,11 @@
 // Source: "FreeToken: 让消费级电脑跑起 284B MoE" (fengjutian.github.io),
 // sec. 2 (the router runs on the GPU and feeds the hit / miss split).
 //
-// Two logits kernels: a weight-streaming GEMV for small token counts (the
-// router matrix is read once, every warp owns one expert row) and a tiled
-// SIMT GEMM for long prompts.  Then one warp per token does the softmax and
-// the top-k selection.
+// Two logits kernels: a weight-streaming GEMV for small token counts (one CTA
+// per expert row) and a tiled SIMT GEMM for long prompts.  Then one warp per
+// token does the softmax and the top-k selection, launched as a programmatic
+// dependent so it is resident before the logits are done.
+#include "ft_async.cuh"
 #include "ft_common.cuh"
 
 namespace ft {
@@ -16,32 +17,35 @@ namespace {
 constexpr int kGemvMaxT = 16;
 constexpr int kRouteMaxK = 32;
 
-// One warp per expert row; lanes stride the hidden axis 8 elements at a time.
+// Small token counts: one CTA per expert row, its 8 warps splitting the
+// hidden axis, so the whole router matrix is requested by the whole GPU at
+// once; partial sums meet in shared memory (fixed order).
 template <int TMAX>
-__global__ void __launch_bounds__(256) route_gemv_kernel(const uint16_t* __restrict__ x, int T,
-                                                         int H, const float* __restrict__ W,
-                                                         int E, float* __restrict__ logits) {
+__global__ void __launch_bounds__(256) route_rows_kernel(const uint16_t* __restrict__ x, int T, int H,
+                                                         const float* __restrict__ W, int E,
+                                                         float* __restrict__ logits) {
+  __shared__ float part[8][TMAX];
+  pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = blockIdx.x * 8 + warp;
-  if (e >= E) return;
+  const int e = blockIdx.x;
+  const float4* wrow = reinterpret_cast<const float4*>(W + static_cast<size_t>(e) * H);
+  const int nch = H / 8;  // 8-element chunks
   float acc[TMAX];
 #pragma unroll
   for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
-  const float4* wrow = reinterpret_cast<const float4*>(W + static_cast<size_t>(e) * H);
-  const int nch = H / 8;
-  for (int c0 = 0; c0 < nch; c0 += 32 * 4) {
-    float4 wa[4], wb[4];
+  for (int c0 = warp * 32; c0 < nch; c0 += 256 * 2) {
+    float4 wa[2], wb[2];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int c = c0 + u * 32 + lane;
+    for (int u = 0; u < 2; ++u) {
+      const int c = c0 + u * 256 + lane;
       if (c < nch) {
         wa[u] = __ldg(wrow + 2 * c);
         wb[u] = __ldg(wrow + 2 * c + 1);
       }
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int c = c0 + u * 32 + lane;
+    for (int u = 0; u < 2; ++u) {
+      const int c = c0 + u * 256 + lane;
       if (c >= nch) break;
 #pragma unroll
       for (int t = 0; t < TMAX; ++t) {
@@ -63,8 +67,15 @@ __global__ void __launch_bounds__(256) route_gemv_kernel(const uint16_t* __restr
 #pragma unroll
   for (int t = 0; t < TMAX; ++t) {
     if (t >= T) break;
-    const float s = warp_sum(acc[t]);
-    if (lane == 0) logits[static_cast<size_t>(t) * E + e] = s;
+    const float v = warp_sum(acc[t]);
+    if (lane == 0) part[warp][t] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x < T) {
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) v += part[w][threadIdx.x];
+    logits[static_cast<size_t>(threadIdx.x) * E + e] = v;
   }
 }
 
@@ -148,6 +159,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
                                                          int E, int k, int renorm,
                                                          int32_t* __restrict__ ids,
                                                          float* __restrict__ wts) {
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
@@ -224,13 +236,12 @@ ft_status ft_moe_route(const uint16_t* x, int32_t T, int32_t H, const float* w_r
   cudaStream_t s = ft::as_stream(stream);
   float* logits = static_cast<float*>(ws);
   if (T <= ft::kGemvMaxT) {
-    const int grid = (E + 7) / 8;
     if (T <= 1)
-      ft::route_gemv_kernel<1><<<grid, 256, 0, s>>>(x, T, H, w_router, E, logits);
+      ft::route_rows_kernel<1><<<E, 256, 0, s>>>(x, T, H, w_router, E, logits);
     else if (T <= 4)
-      ft::route_gemv_kernel<4><<<grid, 256, 0, s>>>(x, T, H, w_router, E, logits);
+      ft::route_rows_kernel<4><<<E, 256, 0, s>>>(x, T, H, w_router, E, logits);
     else
-      ft::route_gemv_kernel<16><<<grid, 256, 0, s>>>(x, T, H, w_router, E, logits);
+      ft::route_rows_kernel<16><<<E, 256, 0, s>>>(x, T, H, w_router, E, logits);
   } else {
     FT_REQUIRE(H % ft::kTK == 0, "route: H %d must be a multiple of 32 for T > 16", H);
     dim3 grid((E + ft::kTN - 1) / ft::kTN, (T + ft::kTM - 1) / ft::kTM);
@@ -238,7 +249,19 @@ ft_status ft_moe_route(const uint16_t* x, int32_t T, int32_t H, const float* w_r
   }
   ft_status st = ft::launch_check("route logits");
   if (st != FT_OK) return st;
-  ft::route_topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits, T, E, k, renorm, topk_ids, topk_w);
+  // the top-k grid starts while the logits grid drains (programmatic launch)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((T + 7) / 8);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const float* lg = logits;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, ft::route_topk_kernel, lg, T, E, k, renorm, topk_ids, topk_w);
+  if (e != cudaSuccess) return ft::fail(FT_ERR_CUDA, "route topk: %s", cudaGetErrorString(e));
   return ft::launch_check("route topk");
 }
 

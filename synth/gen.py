@@ -13,7 +13,7 @@ import math
 
 import numpy as np
 
-from .rng import stream_key, u64_stream_np, u64_stream_torch, uniform01_np
+from .rng import stream_key, u64_stream_np, uniform01_np
 
 FMT_INT4 = 0
 FMT_NVFP4 = 1
@@ -96,10 +96,12 @@ def bank_block_np(seed: int, fid: int, fmt: int, H: int, I: int, g: int = 16,
 
 
 def bank_blocks_torch(seed: int, fids, fmt: int, H: int, I: int, g: int, out, ref_K=None,
-                      chunk: int = 64):
+                      chunk: int = 32):
     """Fill out[i] (uint8 torch tensor [n, >= block bytes], any device) with the
     block of fids[i]; bit-identical to bank_block_np."""
     import torch
+
+    from .rng import u64_stream_torch_keys
 
     off, total = block_layout(fmt, H, I, g)
     nib = off[3]
@@ -116,19 +118,18 @@ def bank_blocks_torch(seed: int, fids, fmt: int, H: int, I: int, g: int, out, re
     for c0 in range(0, len(fids), chunk):
         sub = fids[c0:c0 + chunk]
         rows = out[c0:c0 + len(sub)]
-        for r, fid in enumerate(sub):
-            z = u64_stream_torch(stream_key(seed, "nib", fid), 0, words, device=dev)
-            rows[r, :nib] = z.view(torch.uint8)[:nib]
-            zs = u64_stream_torch(stream_key(seed, "scale", fid), 0, n_s, device=dev)
-            if fmt == FMT_INT4:
-                u = ((zs >> 40) & ((1 << 24) - 1)).to(torch.float32) * (2.0 ** -24)
-                s = u * float(np.float32(hi - lo))
-                s = s + float(np.float32(lo))
-                s = s * fac
-                rows[r, nib:total] = s.to(torch.float16).view(torch.uint8)
-            else:
-                codes = E4M3_CODE_LO + ((zs >> 33) & ((1 << 31) - 1)) % E4M3_CODE_COUNT
-                rows[r, nib:total] = codes.to(torch.uint8)
+        z = u64_stream_torch_keys([stream_key(seed, "nib", f) for f in sub], words, device=dev)
+        rows[:, :nib] = z.view(torch.uint8).view(len(sub), words * 8)[:, :nib]
+        zs = u64_stream_torch_keys([stream_key(seed, "scale", f) for f in sub], n_s, device=dev)
+        if fmt == FMT_INT4:
+            u = ((zs >> 40) & ((1 << 24) - 1)).to(torch.float32) * (2.0 ** -24)
+            s = u * float(np.float32(hi - lo))
+            s = s + float(np.float32(lo))
+            s = s * fac[None, :]
+            rows[:, nib:total] = s.to(torch.float16).view(torch.uint8).view(len(sub), 2 * n_s)
+        else:
+            codes = E4M3_CODE_LO + ((zs >> 33) & ((1 << 31) - 1)) % E4M3_CODE_COUNT
+            rows[:, nib:total] = codes.to(torch.uint8)
     return out
 
 

@@ -59,6 +59,18 @@ def u64_stream_torch(key: int, start: int, count: int, device="cpu"):
     return z
 
 
+def u64_stream_torch_keys(keys, count: int, device="cpu"):
+    """Rows of streams: out[r, i] = value i of stream keys[r] (int64 tensor)."""
+    import torch
+
+    k = torch.tensor([_signed(int(v)) for v in keys], dtype=torch.int64, device=device)[:, None]
+    idx = torch.arange(1, count + 1, dtype=torch.int64, device=device)[None, :]
+    z = idx * _signed(GOLDEN) + k
+    z = (z ^ _lsr(z, 30)) * _signed(_C1)
+    z = (z ^ _lsr(z, 27)) * _signed(_C2)
+    return z ^ _lsr(z, 31)
+
+
 def uniform01_np(key: int, start: int, count: int) -> np.ndarray:
     """Doubles in [0, 1) with 53 random bits."""
     return (u64_stream_np(key, start, count) >> np.uint64(11)).astype(np.float64) * 2.0 ** -53

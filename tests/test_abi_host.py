@@ -72,21 +72,23 @@ def test_host_validation_without_gpu(ft):
     assert lib.ft_moe_resolve_slots(*args(0, 100, 1)) == ft.FT_ERR_INVALID
     # experts: unsupported bank format / misaligned base
     bad = ft.FtBank(0, 2048, 512, 48, dummy, 1 << 21, 4, None)
-    assert lib.ft_moe_experts_fwd(ctypes.byref(bad), None, 0, 8, dummy, 1, dummy, dummy, dummy, 2, 0,
+    assert lib.ft_moe_experts_fwd(ctypes.byref(bad), None, 0, 8, dummy, None, 1, dummy, dummy, dummy, 2, 0,
                                   None, dummy, 0, dummy, 1 << 20, None, None) == ft.FT_ERR_UNSUPPORTED
     mis = ft.FtBank(0, 256, 128, 32, V(8), 55296, 4, None)
-    assert lib.ft_moe_experts_fwd(ctypes.byref(mis), None, 0, 8, dummy, 1, dummy, dummy, dummy, 2, 0,
+    assert lib.ft_moe_experts_fwd(ctypes.byref(mis), None, 0, 8, dummy, None, 1, dummy, dummy, dummy, 2, 0,
                                   None, dummy, 0, dummy, 1 << 20, None, None) == ft.FT_ERR_INVALID
     nvfp4_no_scale = ft.FtBank(1, 2560, 640, 16, dummy, 2764800, 4, None)
     assert lib.ft_moe_fetch(ctypes.byref(nvfp4_no_scale), ctypes.byref(nvfp4_no_scale), dummy, dummy,
                             dummy, 1, None, None) == ft.FT_ERR_INVALID
     # decode limits: too many pairs
     ok = ft.FtBank(0, 256, 128, 32, dummy, 55296, 4, None)
-    assert lib.ft_moe_experts_fwd(ctypes.byref(ok), None, 0, 16, dummy, 200, dummy, dummy, dummy, 2, 0,
+    assert lib.ft_moe_experts_fwd(ctypes.byref(ok), None, 0, 16, dummy, None, 200, dummy, dummy, dummy, 2, 0,
                                   None, dummy, 0, dummy, 1 << 30, None, None) == ft.FT_ERR_INVALID
     # permute / combine shapes
-    assert lib.ft_moe_permute(dummy, 4, 2, 5000, None, 0, dummy, dummy, dummy, None, dummy, 1 << 20,
-                              None, None) == ft.FT_ERR_INVALID
+    assert lib.ft_moe_permute(dummy, 4, 2, 5000, None, 0, dummy, dummy, dummy, None, 0, None, dummy,
+                              1 << 20, None, None) == ft.FT_ERR_INVALID
+    assert lib.ft_moe_permute(dummy, 4, 2, 8, dummy, 16, dummy, dummy, dummy, dummy, 1, None, dummy,
+                              1 << 20, None, None) == ft.FT_ERR_INVALID  # f16 gather without xp_scale
     assert lib.ft_moe_combine(dummy, dummy, dummy, 4, 2, 12, None, dummy, None) == ft.FT_ERR_INVALID
     assert ft.load().ft_status_string(ft.FT_ERR_BAD_ID).decode() == "expert id out of range"
 

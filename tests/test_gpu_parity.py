@@ -305,8 +305,10 @@ def _decode_case(ft, cfg, T, layer, cached_frac, use_pool, pool_pinned=False, ou
     return got, ref, x, ids, w32, slot_np, blocks, ts_np
 
 
-@pytest.mark.parametrize("name,T", [("tiny", 8), ("d35b", 1), ("d35b", 8), ("flash", 1), ("flash", 2)])
+@pytest.mark.parametrize("name,T", [("tiny", 8), ("tiny", 12), ("d35b", 1), ("d35b", 3), ("d35b", 8),
+                                    ("d35b", 16), ("flash", 1), ("flash", 2), ("flash", 9)])
 def test_experts_decode_all_cached(cuda_lib, name, T):
+    """T <= 8 runs the streaming kernels, larger batches the general ones."""
     cfg = synth.get_config(name)
     got, ref, *_ = _decode_case(cuda_lib, cfg, T, layer=1 % cfg.L, cached_frac=1.0, use_pool=False)
     assert_close(got, ref, f"{name} T={T}")
@@ -335,6 +337,34 @@ def test_experts_decode_two_banks(cuda_lib, name, T, pinned):
     got, ref, *_ = _decode_case(cuda_lib, cfg, T, layer=0, cached_frac=0.4, use_pool=True,
                                 pool_pinned=pinned, out_bf16=True)
     assert_close(got, ref, f"{name} two banks")
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 2), ("tiny", 10), ("flash", 1)])
+def test_experts_decode_duplicate_ids_in_a_token(cuda_lib, name, T):
+    """A token may list the same expert more than once: every pair is still
+    computed once and weighted separately."""
+    ft = cuda_lib
+    cfg = synth.get_config(name)
+    E, k, layer = cfg.E, cfg.k, 0
+    rng = np.random.default_rng(77)
+    ids = rng.integers(0, 3, (T, k)).astype(np.int32)  # few experts, many repeats
+    w = rng.uniform(0.05, 0.3, (T, k)).astype(np.float32)
+    x = synth.normal_bf16(synth.stream_key(5, "dup", T), (T, cfg.H))
+    fids = [layer * E + e for e in range(3)]
+    blocks = {f: b for f, b in zip(fids, pool_blocks(cfg, fids))}
+    _, stride = synth.block_layout(cfg.fmt, cfg.H, cfg.I, cfg.g)
+    cache = torch.from_numpy(np.stack([blocks[f] for f in fids])).to(DEV)
+    ts_np = synth.tensor_scales(cfg.fmt, cfg.H, cfg.I, cfg.L * E)
+    ts = None if ts_np is None else _t(ts_np)
+    cb = ft.make_bank(cfg.fmt, cfg.H, cfg.I, cfg.g, cache, ts)
+    out = torch.empty((T, cfg.H), dtype=torch.float32, device=DEV)
+    ws = torch.empty(ft.experts_workspace(0, T, k, cfg.H, cfg.I, E), dtype=torch.uint8, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ft.experts_fwd(cb, None, layer, E, _t(x), T, k, _t(ids), _t(ids), _t(w), out, ws, dev_status=status)
+    torch.cuda.synchronize()
+    assert ft.get_status(status) == 0
+    ref = oracle_pairs_output(blocks, cfg, ts_np, x, ids, w, layer)
+    assert_close(out.cpu().numpy(), ref, f"{name} duplicates", ref_max=None)
 
 
 def test_experts_decode_bad_ids_flagged(cuda_lib):

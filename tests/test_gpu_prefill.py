@@ -1,0 +1,161 @@
+"""GPU parity of the prefill path: route -> permute (f16 gather) -> grouped
+SwiGLU experts on tcgen05 -> combine, against the CPU oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_helpers import assert_close, bf16_to_f64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+FMT = synth.gen.FMT_NVFP4
+
+
+def _t(a):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(a).to(DEV)
+
+
+def _run_prefill(ft, H, I, E, k, ids, x, layer=0, seed=0, bank=None, slot_of=None):
+    """Permute + grouped experts on the GPU; returns (yp bf16 bits, perm, offsets, bank)."""
+    T = ids.shape[0]
+    n = T * k
+    _, stride = synth.block_layout(FMT, H, I, 16)
+    if bank is None:
+        bank = torch.empty((E, stride), dtype=torch.uint8, device=DEV)
+        synth.bank_blocks_torch(seed, range(layer * E, (layer + 1) * E), FMT, H, I, 16, bank)
+    if slot_of is None:
+        slot_of = np.arange(E, dtype=np.int32)
+    ts = _t(synth.tensor_scales(FMT, H, I, (layer + 1) * E))
+    cb = ft.make_bank(FMT, H, I, 16, bank, ts)
+    perm = torch.empty(n, dtype=torch.int32, device=DEV)
+    inv = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    off = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    xp = torch.empty((n, H), dtype=torch.int16, device=DEV)
+    xs = torch.empty(n, dtype=torch.float32, device=DEV)
+    pws = torch.empty(ft.permute_workspace(T, k, E), dtype=torch.uint8, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    d_ids = _t(ids)
+    ft.permute(d_ids, E, _t(x), perm, inv, off, xp, pws, dev_status=status, xp_scale=xs)
+    yp = torch.empty((n, H), dtype=torch.int16, device=DEV)
+    ews = torch.empty(ft.experts_workspace(ft.FT_PREFILL, T, k, H, I, E), dtype=torch.uint8, device=DEV)
+    ft.experts_fwd(cb, None, layer, E, xp, T, k, _t(slot_of), None, None, yp, ews, mode=ft.FT_PREFILL,
+                   offsets=off, dev_status=status, x_scale=xs)
+    torch.cuda.synchronize()
+    assert ft.get_status(status) == 0
+    return yp, perm, inv, off, bank, ts
+
+
+def _oracle_rows(bank_np_by_e, H, I, E, layer, x, perm, k, offsets, rows, ts_np):
+    """Oracle Yp for the given permuted rows, grouped by expert (one dequant each)."""
+    xv = bf16_to_f64(x)
+    out = np.empty((len(rows), H))
+    ex = np.searchsorted(offsets, rows, side="right") - 1
+    for e in np.unique(ex):
+        sel = np.nonzero(ex == e)[0]
+        X = xv[perm[rows[sel]] // k]
+        out[sel] = oracle.expert_batch(bank_np_by_e(e), FMT, H, I, 16, X, ts_np[layer * E + e])
+    return out
+
+
+def test_permute_f16_gather_is_exact():
+    import quantized_expert_ffn_router_gb300 as ft
+
+    ft.load()
+    T, k, E, H = 64, 3, 8, 256
+    rng = np.random.default_rng(3)
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    xf = rng.standard_normal((T, H)).astype(np.float32)
+    xf[5] *= 3e5     # a row beyond the f16 range gets a power-of-two prescale
+    xf[6] *= 1e-3
+    x = synth.bf16_bits(xf)
+    n = T * k
+    perm = torch.empty(n, dtype=torch.int32, device=DEV)
+    inv = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    off = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    xp = torch.empty((n, H), dtype=torch.int16, device=DEV)
+    xs = torch.empty(n, dtype=torch.float32, device=DEV)
+    ws = torch.empty(ft.permute_workspace(T, k, E), dtype=torch.uint8, device=DEV)
+    ft.permute(_t(ids), E, _t(x), perm, inv, off, xp, ws, xp_scale=xs)
+    torch.cuda.synchronize()
+    p = perm.cpu().numpy()
+    s_np = xs.cpu().numpy()[:, None]
+    vals = xp.cpu().numpy().view(np.float16).astype(np.float64) * s_np
+    ref = bf16_to_f64(x)[p // k]
+    normal = np.abs(ref / s_np) >= 2.0 ** -14  # f16 normal range: exact
+    assert np.array_equal(vals[normal], ref[normal])
+    assert (np.abs(vals - ref) <= 2.0 ** -25 * s_np).all()  # subnormal: within half an f16 ulp
+    s = xs.cpu().numpy()
+    assert (s[p // k == 5] > 1).all() and (s[p // k != 5] == 1).all()
+    assert (np.log2(s) == np.round(np.log2(s))).all()
+
+
+@pytest.mark.parametrize("H,I,E,k,T", [(512, 256, 8, 2, 40), (256, 512, 3, 2, 300), (768, 256, 16, 4, 33)])
+def test_prefill_experts_small(cuda_lib, H, I, E, k, T):
+    """Every permuted row against the oracle: ragged segments, empty experts,
+    segments longer than one 256-token pass."""
+    ft = cuda_lib
+    rng = np.random.default_rng(H + I + T)
+    p = np.array([0.5, 0.3] + [0.2 / max(E - 2, 1)] * (E - 2))[:E]
+    p = p / p.sum()
+    ids = np.stack([rng.choice(E, k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    x = synth.normal_bf16(synth.stream_key(0, "pf-x", H, T), (T, H))
+    yp, perm, inv, off, bank, ts = _run_prefill(ft, H, I, E, k, ids, x)
+    bank_np = bank.cpu().numpy()
+    for e in range(E):  # the device bank holds the generator's bytes
+        assert np.array_equal(bank_np[e], synth.bank_block_np(0, e, FMT, H, I, 16))
+    offsets = off.cpu().numpy()
+    assert np.array_equal(offsets, oracle.permute(ids, E)[2])
+    rows = np.arange(T * k)
+    ref = _oracle_rows(lambda e: bank_np[e], H, I, E, 0, x, perm.cpu().numpy(), k, offsets, rows,
+                       synth.tensor_scales(FMT, H, I, E))
+    got = bf16_to_f64(yp.cpu().numpy().view(np.uint16))
+    assert_close(got, ref, f"prefill rows {H}x{I}")
+
+
+def test_prefill_full_layer_sampled(cuda_lib):
+    """The whole-layer prefill shape (H 4096, I 2048, 256 experts, top-6,
+    T = 2048): route on the GPU, permute, grouped experts and combine; every row
+    of four sampled experts checked against the oracle, and the combine on
+    sampled tokens."""
+    ft = cuda_lib
+    cfg = synth.get_config("prefill")
+    H, I, E, k, T = cfg.H, cfg.I, cfg.E, cfg.k, 2048
+    W = synth.router_weights(cfg.seed, 0, E, H, cfg.router_std)
+    x = synth.normal_bf16(synth.stream_key(cfg.seed, "prefill-x", T), (T, H))
+    ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    rws = torch.empty(ft.route_workspace(T, E), dtype=torch.uint8, device=DEV)
+    ft.route(_t(x), _t(W), k, ids, w, rws)
+    torch.cuda.synchronize()
+    ids_np = ids.cpu().numpy()
+    yp, perm, inv, off, bank, ts = _run_prefill(ft, H, I, E, k, ids_np, x, seed=cfg.seed)
+    offsets = off.cpu().numpy()
+    counts = np.diff(offsets)
+    assert (counts > 0).sum() >= 0.9 * E  # nearly every expert is active
+    perm_np = perm.cpu().numpy()
+    experts = [int(np.argmax(counts)), int(np.argmin(np.where(counts > 0, counts, 10 ** 9))), 17, 200]
+    blocks = {}
+    for e in experts:
+        blk = synth.bank_block_np(cfg.seed, e, FMT, H, I, 16)
+        assert np.array_equal(bank[e].cpu().numpy(), blk)
+        blocks[e] = blk
+    rows = np.concatenate([np.arange(offsets[e], offsets[e + 1]) for e in experts])
+    ref = _oracle_rows(lambda e: blocks[e], H, I, E, 0, x, perm_np, k, offsets, rows,
+                       synth.tensor_scales(FMT, H, I, E))
+    got = bf16_to_f64(yp.cpu().numpy().view(np.uint16)[rows])
+    assert_close(got, ref, "prefill full-size rows")
+    # combine: out[t] = sum_j w[t,j] Yp[inv[t,j]] for sampled tokens
+    out = torch.empty((T, H), dtype=torch.int16, device=DEV)
+    ft.combine(yp, inv, w, out)
+    torch.cuda.synchronize()
+    toks = np.array([0, 5, 1000, T - 1])
+    inv_np = inv.cpu().numpy()
+    ref_c = oracle.combine(yp.cpu().numpy().view(np.uint16), inv_np[toks], w.cpu().numpy()[toks])
+    got_c = bf16_to_f64(out.cpu().numpy().view(np.uint16)[toks])
+    assert_close(got_c, ref_c, "prefill combine", ref_max=None)

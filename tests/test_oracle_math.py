@@ -323,3 +323,12 @@ def test_grouped_rows_match_per_pair_experts():
         t, j = divmod(int(perm[pos]), cfg.k)
         y = oracle.expert(pool[ids[t, j]], cfg.fmt, cfg.H, cfg.I, cfg.g, xv[t])
         assert np.array_equal(yp[pos], y)
+
+
+def test_expert_batch_equals_single_calls():
+    cfg = synth.get_config("tiny")
+    blk = synth.bank_block_np(1, 2, cfg.fmt, cfg.H, cfg.I, cfg.g)
+    X = np.random.default_rng(4).standard_normal((3, cfg.H))
+    Y = oracle.expert_batch(blk, cfg.fmt, cfg.H, cfg.I, cfg.g, X)
+    for r in range(3):
+        assert np.array_equal(Y[r], oracle.expert(blk, cfg.fmt, cfg.H, cfg.I, cfg.g, X[r]))
