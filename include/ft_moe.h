@@ -242,6 +242,26 @@ FT_API ft_status ft_moe_experts_fwd(const ft_bank* cache_host, const ft_bank* po
                              void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /*
+ * ft_moe_experts_decode_static -- ft_moe_experts_fwd in FT_DECODE mode with
+ * no workspace argument: the scratch lives in a 1 MiB array of device memory
+ * that the library owns (the source pages have no counterpart to this call).
+ * It serves callers that cannot allocate device memory themselves -- code
+ * running inside a stream capture, hosts whose GPU memory belongs to another
+ * framework's pool, loops that cannot afford an allocation's synchronisation.
+ * Same arguments and results as the decode mode above, minus ws.  Limits and
+ * rules: T*k*I*4 must not exceed 1 MiB (else FT_ERR_INVALID, nothing
+ * launched); every GPU that loads the library keeps the array until exit;
+ * calls that may overlap on the GPU share the array and race, so the caller
+ * serialises them; the first call on a device looks the array up (with that
+ * device current) and should happen before any stream capture.
+ */
+FT_API ft_status ft_moe_experts_decode_static(const ft_bank* cache_host, const ft_bank* pool_host,
+                                              int32_t layer, int32_t E, const uint16_t* x, int32_t T,
+                                              const int32_t* slot_ids, const int32_t* raw_ids,
+                                              const float* topk_w, int32_t k, void* out,
+                                              int32_t out_dtype, int32_t* dev_status, void* stream);
+
+/*
  * ft_moe_permute -- stable sort of the T*k (token, rank) pairs by expert
  * (expert asc, then token, then rank) and gather of the permuted batch
  * (NVMe post, step 5: the whole prompt through a layer's experts at once;

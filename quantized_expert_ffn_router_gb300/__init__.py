@@ -57,6 +57,8 @@ _SIGS = {
     "ft_moe_experts_workspace": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
     "ft_moe_experts_fwd": (_I32, [_V, _V, _I32, _I32, _V, _V, _I32, _V, _V, _V, _I32, _I32, _V, _V,
                                   _I32, _V, _SZ, _V, _V]),
+    "ft_moe_experts_decode_static": (_I32, [_V, _V, _I32, _I32, _V, _I32, _V, _V, _V, _I32, _V, _I32,
+                                            _V, _V]),
     "ft_moe_permute_workspace": (_SZ, [_I32, _I32, _I32]),
     "ft_moe_permute": (_I32, [_V, _I32, _I32, _I32, _V, _I32, _V, _V, _V, _V, _I32, _V, _V, _SZ, _V,
                               _V]),
@@ -194,6 +196,20 @@ def experts_fwd(cache: FtBank, pool, layer: int, E: int, x, T: int, k: int, slot
                                      _ptr(topk_w), k, mode, _ptr(offsets), _ptr(out), out_dtype,
                                      _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status),
                                      _stream(stream)))
+
+
+def experts_decode_static(cache: FtBank, pool, layer: int, E: int, x, T: int, k: int, slot_ids, raw_ids,
+                          topk_w, out, dev_status=None, stream=None):
+    """Decode experts with the library's own 1 MiB device scratch: for callers
+    that cannot allocate a workspace (inside a stream capture, under another
+    framework's memory pool).  Calls share the scratch: do not overlap them."""
+    import torch
+
+    out_dtype = FT_OUT_BF16 if out.dtype in (torch.bfloat16, torch.int16, torch.uint16) else FT_OUT_F32
+    _check(load().ft_moe_experts_decode_static(ctypes.byref(cache), None if pool is None else ctypes.byref(pool),
+                                               layer, E, _ptr(x), T, _ptr(slot_ids), _ptr(raw_ids),
+                                               _ptr(topk_w), k, _ptr(out), out_dtype, _ptr(dev_status),
+                                               _stream(stream)))
 
 
 def permute_workspace(T: int, k: int, E: int) -> int:
