@@ -1,33 +1,38 @@
-// decode2.cu -- the streaming decode experts kernels (T <= 8 tokens).
+// decode2.cu -- the pair-major decode experts kernels (T <= 16 tokens).
 //
-// Decode reads every routed expert's bytes once and does little arithmetic
-// per byte, so the whole layer is a race to keep HBM busy.  Each of the two
-// kernels runs one CTA per SM; every CTA owns a contiguous slice of the
-// work and, before computing anything, issues TMA bulk copies
-// (cp.async.bulk) of its whole slice into a shared-memory ring, so the
-// layer's bytes are in flight at once.  Warps compute as stages land
-// (mbarrier per stage, bounded waits).
+// At decode sizes a layer reads a few MB of expert weights and does little
+// arithmetic per byte: the layer is a race against memory latency.  These
+// kernels therefore keep every warp independent and put all of a warp's
+// weight loads in flight before anything waits:
 //
-//   gate/up: units of RA rows of one distinct expert's gate and up matrices.
-//     Each warp owns whole rows; lanes split the row in 32-element chunks,
-//     dequantise to f16 in registers and accumulate in fp32 with
-//     fma.rn.f32.f16 against the token's activations (f16, exact power-of-two
-//     prescale per token); a warp-shuffle reduction finishes the row and
-//     h = silu(g) * u goes to the workspace in fp32.
-//   down: units of RB rows of H, covering every distinct expert's down rows,
-//     launched as a programmatic dependent of gate/up: its weight copies are
-//     issued before griddepcontrol.wait, so they stream while gate/up still
-//     runs.  After the wait the CTA stages h (f16, per-pair prescale) and
-//     each warp produces whole output rows, summing all top-k experts of each
-//     token in a fixed order (combine fused, no atomics).
+//   gate/up: grid (I / rows per CTA) x (T*k pairs).  A warp owns RPW rows of
+//     one (token, rank) pair's expert; each lane loads its 16-byte chunks of
+//     those gate and up rows and their scales at once, then converts the
+//     token's activations to f16 in registers (exact per-token power-of-two
+//     prescale), dots, reduces with shuffles, and lane r writes row r's
+//     h = silu(g) * u to the fp32 workspace.
+//   down: a programmatic dependent of gate/up, grid (H / rows per CTA) x T.
+//     A CTA owns rows of one token's output.  Its lanes first load their
+//     chunks of the down rows of the token's k experts (these do not depend
+//     on h, so they stream while gate/up still runs), then griddepcontrol.wait,
+//     stage the token's k intermediates in shared memory as f16 (exact
+//     power-of-two prescale per pair), and accumulate the top-k weighted sum
+//     of every row in a fixed order (the combine is fused, no atomics).
 //
-// int4: a nibble q becomes the f16 value 1 + q/16 by placing it in the
-// mantissa; sum (q - 8) a = 16 * sum (1 + q/16) a - 24 * sum a, with sum a per
-// 32-element chunk precomputed.  NVFP4: the hardware e2m1x2 -> f16x2 convert,
-// one E4M3 scale per 16 elements.  All products are exact; accumulation fp32.
+// Pairs are not grouped by expert: two pairs of one expert read its rows
+// twice, and the second read is served by L2 since both are in flight
+// together.  Masked pairs (slot and pool entry both absent) contribute
+// nothing.
+//
+// Dequantisation: an int4 code q in 0..15 is also the E4M3 code of q * 2^-9
+// exactly (the subnormals and the first binade of E4M3 are evenly spaced), so
+// cvt.rn.f16x2.e4m3x2 turns two nibbles spread to bytes into f16 q * 2^-9, and
+// sum (q - 8) a = 512 * sum (q 2^-9) a - 8 * sum a, with sum a per 32-element
+// chunk precomputed.  NVFP4 codes go through cvt.rn.f16x2.e2m1x2.  Products
+// are exact (fma.rn.f32.f16) and accumulate in fp32.
 //
 // Experts whose block lives in the host pool (the -1 path read in place) are
-// never bulk-copied: their rows are read directly with ordinary loads.
+// read with the same loads through the host mapping.
 //
 // Sources: "SSD 가중치층으로 35B MoE를 ..." (onedev.kr), "How it works";
 // "NVMe에서 전문가(experts)를 ... 133GB MoE" (molayo1419.me), step 4;
@@ -40,51 +45,29 @@
 namespace ft {
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kV2Threads = (kConsumerWarps + 1) * 32;  // + one producer warp
-constexpr int kMaxStages = 32;
-constexpr int kChunkBytes = 80;  // 32 f16 activations + 16 B pad (conflict-free 16-B reads)
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kDownLoads = 8;     // down: 16-byte weight loads a lane holds at once
+constexpr int kChunkBytes = 80;   // 32 f16 values + 16 B pad (conflict-free 16-byte reads)
 
-struct V2Geo {
-  int RA, RB;       // rows per gate/up unit, per down unit
-  int sbA, sbB;     // scale bytes per row: gate/up, down
-  int stageA;       // bytes of one gate/up stage
-  int nsA;          // gate/up ring stages
-  int segB;         // bytes of one expert's rows in a down stage
-  int ringB;        // bytes of the down ring
-  int xbytes;       // activation area of gate/up (T x H/32 chunks)
-  int hbytes;       // activation area of down (pairs x I/32 chunks)
-};
-
-// ------------------------------------------------------- f16 dequant-dot ---
-__device__ __forceinline__ void fma2_f16(float& a0, float& a1, uint32_t w, uint32_t x) {
-  asm("{\n .reg .b16 wl, wh, xl, xh;\n mov.b32 {wl, wh}, %2;\n mov.b32 {xl, xh}, %3;\n"
-      " fma.rn.f32.f16 %0, wl, xl, %0;\n fma.rn.f32.f16 %1, wh, xh, %1;\n}"
-      : "+f"(a0), "+f"(a1)
-      : "r"(w), "r"(x));
+// ----------------------------------------------------------- conversions ---
+__device__ __forceinline__ uint32_t cvt_e4m3x2(uint32_t two_bytes) {
+  uint32_t h;
+  const unsigned short b = static_cast<unsigned short>(two_bytes);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(b));
+  return h;
 }
 
-// int4 chunk: sum over 32 codes of (1 + q/16) * a, a in the word-permuted
-// order [a0 a4 a1 a5 a2 a6 a3 a7] per 8 codes.
-__device__ __forceinline__ float dot_i4_f16(const uint4 w, const uint8_t* xa) {
-  const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-  float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint4 xv = *reinterpret_cast<const uint4*>(xa + 16 * j);
-    const uint32_t v = wv[j];
-    const uint32_t p0 = ((v << 6) & 0x03C003C0u) | 0x3C003C00u;  // codes 0, 4
-    const uint32_t p1 = ((v << 2) & 0x03C003C0u) | 0x3C003C00u;  // codes 1, 5
-    const uint32_t p2 = ((v >> 2) & 0x03C003C0u) | 0x3C003C00u;  // codes 2, 6
-    const uint32_t p3 = ((v >> 6) & 0x03C003C0u) | 0x3C003C00u;  // codes 3, 7
-    fma2_f16(s0, s1, p0, xv.x);
-    fma2_f16(s0, s1, p1, xv.y);
-    fma2_f16(s0, s1, p2, xv.z);
-    fma2_f16(s0, s1, p3, xv.w);
-  }
-  return s0 + s1;
+// 8 int4 codes of a word -> f16 q * 2^-9 in the pairs (c0,c2) (c4,c6) (c1,c3) (c5,c7).
+__device__ __forceinline__ void int4x8(uint32_t v, uint32_t h[4]) {
+  const uint32_t lo = v & 0x0F0F0F0Fu, hi = (v >> 4) & 0x0F0F0F0Fu;
+  h[0] = cvt_e4m3x2(lo);
+  h[1] = cvt_e4m3x2(lo >> 16);
+  h[2] = cvt_e4m3x2(hi);
+  h[3] = cvt_e4m3x2(hi >> 16);
 }
 
+// 8 E2M1 codes of a word -> f16 in the pairs (c0,c1) (c2,c3) (c4,c5) (c6,c7).
 __device__ __forceinline__ void e2m1x8(uint32_t v, uint32_t h[4]) {
   asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
       " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
@@ -93,440 +76,416 @@ __device__ __forceinline__ void e2m1x8(uint32_t v, uint32_t h[4]) {
       : "r"(v));
 }
 
-__device__ __forceinline__ float2 e4m3x2_f32(uint32_t two) {
-  uint32_t h2;
-  const unsigned short b = static_cast<unsigned short>(two);
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(b));
-  return __half22float2(*reinterpret_cast<const __half2*>(&h2));
+// a0 += w.lo * x.lo, a1 += w.hi * x.hi in fp32 (f16 operands, exact products).
+__device__ __forceinline__ void fma2_f16(float& a0, float& a1, uint32_t w, uint32_t x) {
+  asm("{\n .reg .b16 wl, wh, xl, xh;\n mov.b32 {wl, wh}, %2;\n mov.b32 {xl, xh}, %3;\n"
+      " fma.rn.f32.f16 %0, wl, xl, %0;\n fma.rn.f32.f16 %1, wh, xh, %1;\n}"
+      : "+f"(a0), "+f"(a1)
+      : "r"(w), "r"(x));
 }
 
-// NVFP4 chunk: s0 * sum_{i<16} e2m1_i a_i + s1 * sum_{i>=16} e2m1_i a_i, a in
-// natural order.
-__device__ __forceinline__ float dot_fp4_f16(const uint4 w, uint32_t sc2, const uint8_t* xa) {
+// The scale word of one chunk: int4 -> its fp16 group scale; NVFP4 -> its two
+// E4M3 block scales (16 elements each) in the low 16 bits.
+template <int FMT>
+__device__ __forceinline__ uint32_t load_scale(const uint8_t* srow, int c, int gshift) {
+  if constexpr (FMT == FT_INT4)
+    return __ldg(reinterpret_cast<const unsigned short*>(srow) + (c >> gshift));
+  else
+    return __ldg(reinterpret_cast<const unsigned short*>(srow) + c);
+}
+
+// One 32-element chunk: 16 bytes of codes, the chunk's scale word, 16 f16x2
+// activation words in the format's order and (int4) the sum of those values.
+template <int FMT>
+__device__ __forceinline__ float chunk_dot(const uint4 w, uint32_t sc, const uint32_t* xa, float asum) {
   const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-  float part[2];
+  if constexpr (FMT == FT_INT4) {
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    float s0 = 0.f, s1 = 0.f;
+    for (int j = 0; j < 4; ++j) {
+      uint32_t h[4];
+      int4x8(wv[j], h);
+      fma2_f16(s0, s1, h[0], xa[4 * j + 0]);
+      fma2_f16(s2, s3, h[1], xa[4 * j + 1]);
+      fma2_f16(s0, s1, h[2], xa[4 * j + 2]);
+      fma2_f16(s2, s3, h[3], xa[4 * j + 3]);
+    }
+    const float s = __half2float(__ushort_as_half(static_cast<unsigned short>(sc)));
+    return s * fmaf(512.f, (s0 + s1) + (s2 + s3), -8.f * asum);
+  } else {
+    float p0 = 0.f, p1 = 0.f, q0 = 0.f, q1 = 0.f;
 #pragma unroll
-    for (int jj = 0; jj < 2; ++jj) {
-      const int j = half * 2 + jj;
-      const uint4 xv = *reinterpret_cast<const uint4*>(xa + 16 * j);
+    for (int j = 0; j < 4; ++j) {
       uint32_t h[4];
       e2m1x8(wv[j], h);
-      fma2_f16(s0, s1, h[0], xv.x);
-      fma2_f16(s0, s1, h[1], xv.y);
-      fma2_f16(s0, s1, h[2], xv.z);
-      fma2_f16(s0, s1, h[3], xv.w);
+      float& a0 = (j < 2) ? p0 : q0;
+      float& a1 = (j < 2) ? p1 : q1;
+      fma2_f16(a0, a1, h[0], xa[4 * j + 0]);
+      fma2_f16(a0, a1, h[1], xa[4 * j + 1]);
+      fma2_f16(a0, a1, h[2], xa[4 * j + 2]);
+      fma2_f16(a0, a1, h[3], xa[4 * j + 3]);
     }
-    part[half] = s0 + s1;
-  }
-  const float2 s = e4m3x2_f32(sc2);
-  return fmaf(part[0], s.x, part[1] * s.y);
-}
-
-// One 32-element chunk: codes (16 B), its scale bytes, activations (f16 in
-// the format's order) and their sum (int4 only).
-template <int FMT>
-__device__ __forceinline__ float chunk(const uint8_t* codes, const uint8_t* srow, int c, int group,
-                                       const uint8_t* xa, float asum) {
-  const uint4 w = *reinterpret_cast<const uint4*>(codes + 16 * c);
-  if constexpr (FMT == FT_INT4) {
-    const float s = __half2float(__ushort_as_half(
-        *reinterpret_cast<const unsigned short*>(srow + 2 * ((c * 32) / group))));
-    return s * fmaf(16.f, dot_i4_f16(w, xa), -24.f * asum);
-  } else {
-    const uint32_t sc2 = *reinterpret_cast<const unsigned short*>(srow + 2 * c);
-    return dot_fp4_f16(w, sc2, xa);
+    const uint32_t h2 = cvt_e4m3x2(sc);
+    const float2 s = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+    return fmaf(p0 + p1, s.x, (q0 + q1) * s.y);
   }
 }
 
-// Convert 32 fp32 activations (times `mul`) to f16 in the format's order,
-// write them (64 B) at dst, return their sum as used.
-template <int FMT>
-__device__ __forceinline__ float pack_chunk(const float* v, float mul, uint8_t* dst) {
-  __half hv[32];
+// Element i of a chunk: from 32 fp32 values or from 16 bf16x2 words.
+__device__ __forceinline__ float elem(const float* v, int i) { return v[i]; }
+__device__ __forceinline__ float elem(const uint32_t* b, int i) {
+  return (i & 1) ? bf16_hi(b[i >> 1]) : bf16_lo(b[i >> 1]);
+}
+
+// 32 values (times `mul`) -> 16 f16x2 words in the format's order; returns
+// the sum of the f16 values as used.
+template <int FMT, typename V>
+__device__ __forceinline__ float pack32(const V* v, float mul, uint32_t* out) {
   float s = 0.f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    hv[i] = __float2half_rn(v[i] * mul);
-    s += __half2float(hv[i]);
-  }
-  uint32_t out[16];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-      // int4 order per 8 codes: pairs (0,4) (1,5) (2,6) (3,7); NVFP4: (0,1) (2,3) ...
-      const int lo = (FMT == FT_INT4) ? 8 * j + m : 8 * j + 2 * m;
-      const int hi = (FMT == FT_INT4) ? 8 * j + m + 4 : 8 * j + 2 * m + 1;
-      out[4 * j + m] = static_cast<uint32_t>(__half_as_ushort(hv[lo])) |
-                       (static_cast<uint32_t>(__half_as_ushort(hv[hi])) << 16);
+      // int4 pairs per 8 codes: (0,2) (4,6) (1,3) (5,7); NVFP4: (0,1) (2,3) (4,5) (6,7)
+      const int lo = (FMT == FT_INT4) ? 8 * j + ((m & 1) ? 4 : 0) + ((m & 2) ? 1 : 0) : 8 * j + 2 * m;
+      const int hi = (FMT == FT_INT4) ? lo + 2 : lo + 1;
+      const __half a = __float2half_rn(elem(v, lo) * mul), b = __float2half_rn(elem(v, hi) * mul);
+      s += __half2float(a) + __half2float(b);
+      out[4 * j + m] = static_cast<uint32_t>(__half_as_ushort(a)) | (static_cast<uint32_t>(__half_as_ushort(b)) << 16);
     }
   }
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-    *reinterpret_cast<uint4*>(dst + 16 * j) = make_uint4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
   return s;
 }
 
+__device__ __forceinline__ float warp_max(float m) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  return m;
+}
+
+// The block a pair reads: its cache slot, else its pool entry, else none
+// (masked).  Bad ids are recorded when `report` is set.
+__device__ __forceinline__ const uint8_t* pair_block(const DecArgs& a, int p, bool report) {
+  const int e = a.raw_ids[p];
+  const int s = a.slot_ids[p];
+  if (e < 0 || e >= a.E) {
+    if (report) record_status(a.dev_status, FT_ERR_BAD_ID);
+    return nullptr;
+  }
+  if (s >= 0) {
+    if (s < a.cblocks) return a.cache + static_cast<uint64_t>(s) * a.cstride;
+    if (report) record_status(a.dev_status, FT_ERR_BAD_ID);
+    return nullptr;
+  }
+  if (a.pool == nullptr) return nullptr;
+  const int64_t fid = static_cast<int64_t>(a.layer) * a.E + e;
+  if (fid < a.pblocks) return a.pool + static_cast<uint64_t>(fid) * a.pstride;
+  if (report) record_status(a.dev_status, FT_ERR_BAD_ID);
+  return nullptr;
+}
+
 // --------------------------------------------------------------- gate/up ---
-template <int FMT>
-__global__ void __launch_bounds__(kV2Threads, 1) v2_gateup_kernel(DecArgs a, V2Geo geo) {
-  extern __shared__ __align__(128) uint8_t sm[];
-  __shared__ Groups g;
-  __shared__ __align__(8) uint64_t full[kMaxStages];
-  __shared__ __align__(8) uint64_t empty[kMaxStages];
-  __shared__ float s_inv[kV2MaxTok];
+// CPL = 32-element chunks per lane (H <= 1024 * CPL), RPW = rows per warp.
+template <int FMT, int CPL, int RPW>
+__global__ void __launch_bounds__(kThreads, 2) pm_gateup_kernel(DecArgs a, int gshift) {
   pdl_launch_dependents();
-  if (prior_timeout(a.dev_status)) return;
-  build_groups(a, g);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int H = a.H, HC = H / 32, RA = geo.RA, nsA = geo.nsA;
-  uint8_t* ring = sm;
-  uint8_t* xsm = sm + static_cast<size_t>(nsA) * geo.stageA;
-  float* xsum = reinterpret_cast<float*>(xsm + geo.xbytes);
-  if (tid == 0) {
-    for (int s = 0; s < nsA; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
-    }
-    fence_barrier_init();
-  }
-  // activations: per-token prescale, f16 chunks in the format's order, sums
-  for (int t = warp; t < a.T; t += kConsumerWarps + 1) {
-    float m = 0.f;
-    for (int i = lane; i < H; i += 32) m = fmaxf(m, fabsf(bf16_val(a.x[static_cast<size_t>(t) * H + i])));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) s_inv[t] = f16_prescale(m);
-  }
-  __syncthreads();
-  for (int i = tid; i < a.T * HC; i += blockDim.x) {
-    const int t = i / HC, c = i % HC;
-    const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * H + 32 * c);
-    float v[32];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint4 q = __ldg(src + j);
-      v[8 * j + 0] = bf16_lo(q.x); v[8 * j + 1] = bf16_hi(q.x);
-      v[8 * j + 2] = bf16_lo(q.y); v[8 * j + 3] = bf16_hi(q.y);
-      v[8 * j + 4] = bf16_lo(q.z); v[8 * j + 5] = bf16_hi(q.z);
-      v[8 * j + 6] = bf16_lo(q.w); v[8 * j + 7] = bf16_hi(q.w);
-    }
-    xsum[i] = pack_chunk<FMT>(v, s_inv[t], xsm + static_cast<size_t>(i) * kChunkBytes);
-  }
-  __syncthreads();
-
-  const int upr = a.I / RA;
-  const int U = g.nD * upr;
-  const int u0 = static_cast<int>(static_cast<long long>(U) * blockIdx.x / gridDim.x);
-  const int u1 = static_cast<int>(static_cast<long long>(U) * (blockIdx.x + 1) / gridDim.x);
-  const int nu = u1 - u0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int p = blockIdx.y;
+  const int H = a.H, HC = H / 32;
+  const int r0 = (blockIdx.x * kWarps + warp) * RPW;
+  const uint8_t* blk = pair_block(a, p, blockIdx.x == 0 && threadIdx.x == 0);
+  if (blk == nullptr) return;  // masked: down skips this pair too
   const uint32_t rowA = static_cast<uint32_t>(H / 2);
-  const uint32_t sbA = static_cast<uint32_t>(geo.sbA);
+  const uint32_t sbA = (FMT == FT_INT4) ? static_cast<uint32_t>((H / a.group) * 2) : static_cast<uint32_t>(H / 16);
 
-  if (warp == kConsumerWarps) {
-    if (lane == 0) {
-      int issued = 0;
-      for (int i = 0; i < nu; ++i) {
-        const int st = i % nsA;
-        if (i >= nsA && !mbar_wait(&empty[st], ((i / nsA) - 1) & 1, a.dev_status)) break;
-        const int u = u0 + i, d = u / upr, r0 = (u % upr) * RA;
-        const uint8_t* blk = g.dBlock[d];
-        if (g.dCached[d]) {
-          uint8_t* dst = ring + static_cast<size_t>(st) * geo.stageA;
-          mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(geo.stageA));
-          bulk_g2s(dst, blk + a.off[0] + r0 * rowA, RA * rowA, &full[st]);
-          bulk_g2s(dst + RA * rowA, blk + a.off[1] + r0 * rowA, RA * rowA, &full[st]);
-          bulk_g2s(dst + 2 * RA * rowA, blk + a.off[3] + r0 * sbA, RA * sbA, &full[st]);
-          bulk_g2s(dst + 2 * RA * rowA + RA * sbA, blk + a.off[4] + r0 * sbA, RA * sbA, &full[st]);
-        } else {
-          mbar_arrive(&full[st]);
+  // every weight and scale load of this warp goes out first
+  uint4 w[RPW][2][CPL];
+  uint32_t sc[RPW][2][CPL];
+#pragma unroll
+  for (int rr = 0; rr < RPW; ++rr)
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      const uint8_t* row = blk + a.off[m] + static_cast<uint64_t>(r0 + rr) * rowA;
+      const uint8_t* srow = blk + a.off[3 + m] + static_cast<uint64_t>(r0 + rr) * sbA;
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) {
+        const int c = lane + 32 * j;
+        if (c < HC) {
+          w[rr][m][j] = __ldg(reinterpret_cast<const uint4*>(row) + c);
+          sc[rr][m][j] = load_scale<FMT>(srow, c, gshift);
         }
-        issued = i + 1;
       }
-      // copies still in flight must land before the CTA exits
-      for (int i = max(0, issued - nsA); i < issued; ++i)
-        if (!mbar_wait(&full[i % nsA], (i / nsA) & 1, a.dev_status)) break;
     }
-    return;
+  float ts0 = 1.f, ts1 = 1.f;
+  if constexpr (FMT == FT_NVFP4) {
+    const int64_t fid = static_cast<int64_t>(a.layer) * a.E + a.raw_ids[p];
+    ts0 = __ldg(a.tscale + 3 * fid + 0);
+    ts1 = __ldg(a.tscale + 3 * fid + 1);
   }
 
-  for (int i = 0; i < nu; ++i) {
-    const int st = i % nsA;
-    if (!mbar_wait(&full[st], (i / nsA) & 1, a.dev_status)) break;
-    const int u = u0 + i, d = u / upr, r0 = (u % upr) * RA;
-    const bool cached = g.dCached[d] != 0;
-    const uint8_t* blk = g.dBlock[d];
-    const uint8_t* stg = ring + static_cast<size_t>(st) * geo.stageA;
-    float tsg = 1.f, tsu = 1.f;
-    if constexpr (FMT == FT_NVFP4) {
-      const int64_t fid = static_cast<int64_t>(a.layer) * a.E + g.dExpert[d];
-      tsg = __ldg(a.tscale + 3 * fid + 0);
-      tsu = __ldg(a.tscale + 3 * fid + 1);
-    }
-    for (int rr = 0; rr < RA; ++rr) {
-      if (((i * RA + rr) & (kConsumerWarps - 1)) != warp) continue;
-      const int r = r0 + rr;
-      const uint8_t* gc = cached ? stg + rr * rowA : blk + a.off[0] + static_cast<uint64_t>(r) * rowA;
-      const uint8_t* uc = cached ? stg + (RA + rr) * rowA : blk + a.off[1] + static_cast<uint64_t>(r) * rowA;
-      const uint8_t* gs = cached ? stg + 2 * RA * rowA + rr * sbA : blk + a.off[3] + static_cast<uint64_t>(r) * sbA;
-      const uint8_t* us = cached ? stg + 2 * RA * rowA + (RA + rr) * sbA
-                                 : blk + a.off[4] + static_cast<uint64_t>(r) * sbA;
-      for (int q = g.dStart[d]; q < g.dStart[d + 1]; ++q) {
-        const int p = g.sortedPair[q];
-        const int t = p / a.k;
-        float ag = 0.f, au = 0.f;
-        for (int c = lane; c < HC; c += 32) {
-          const uint8_t* xa = xsm + static_cast<size_t>(t * HC + c) * kChunkBytes;
-          const float xs = xsum[t * HC + c];
-          ag += chunk<FMT>(gc, gs, c, a.group, xa, xs);
-          au += chunk<FMT>(uc, us, c, a.group, xa, xs);
+  // the token's activations -> f16 in registers, exact power-of-two prescale
+  const int t = p / a.k;
+  uint32_t xa[CPL][16];
+  float xs[CPL];
+  {
+    uint32_t raw[CPL][16];
+    float m = 0.f;
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+      const int c = lane + 32 * j;
+      if (c < HC) {
+        const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * H + 32 * c);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint4 q = __ldg(src + u);
+          raw[j][4 * u] = q.x; raw[j][4 * u + 1] = q.y; raw[j][4 * u + 2] = q.z; raw[j][4 * u + 3] = q.w;
         }
-        ag = warp_sum(ag);
-        au = warp_sum(au);
-        if (lane == 0) {
-          const float inv = 1.f / s_inv[t];
-          const float gv = ag * inv * tsg, uv = au * inv * tsu;
-          a.h[static_cast<size_t>(p) * a.I + r] = gv / (1.f + expf(-gv)) * uv;
-        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) m = fmaxf(m, fmaxf(fabsf(bf16_lo(raw[j][i])), fabsf(bf16_hi(raw[j][i]))));
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
+    const float mul = f16_prescale(warp_max(m));
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+      xs[j] = 0.f;
+      if (lane + 32 * j < HC) xs[j] = pack32<FMT>(raw[j], mul, xa[j]);
+    }
+    const float inv = 1.f / mul;
+    ts0 *= inv;
+    ts1 *= inv;
+  }
+
+  float acc[RPW][2];
+#pragma unroll
+  for (int rr = 0; rr < RPW; ++rr)
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      float s = 0.f;
+#pragma unroll
+      for (int j = 0; j < CPL; ++j)
+        if (lane + 32 * j < HC) s += chunk_dot<FMT>(w[rr][m][j], sc[rr][m][j], xa[j], xs[j]);
+      acc[rr][m] = s;
+    }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int rr = 0; rr < RPW; ++rr)
+#pragma unroll
+      for (int m = 0; m < 2; ++m) acc[rr][m] += __shfl_xor_sync(0xffffffffu, acc[rr][m], o);
+  if (lane < RPW) {
+    float gv = 0.f, uv = 0.f;
+#pragma unroll
+    for (int rr = 0; rr < RPW; ++rr)
+      if (rr == lane) {
+        gv = acc[rr][0];
+        uv = acc[rr][1];
+      }
+    gv *= ts0;
+    uv *= ts1;
+    a.h[static_cast<size_t>(p) * a.I + r0 + lane] = gv / (1.f + expf(-gv)) * uv;
   }
 }
 
 // ------------------------------------------------------------------ down ---
-template <int FMT, int NT>
-__global__ void __launch_bounds__(kV2Threads, 1) v2_down_kernel(DecArgs a, V2Geo geo) {
-  extern __shared__ __align__(128) uint8_t sm[];
-  __shared__ Groups g;
-  __shared__ __align__(8) uint64_t full[kMaxStages];
-  __shared__ __align__(8) uint64_t empty[kMaxStages];
-  __shared__ float s_w[kMaxPairs];
-  __shared__ float s_inv[kMaxPairs];
-  __shared__ int s_tok[kMaxPairs];
-  __shared__ int s_d[kMaxPairs];
-  if (prior_timeout(a.dev_status)) return;
-  build_groups(a, g);
+// LPR lanes per output row (a power of two covering I/32 chunks, CPL chunks
+// per lane); a CTA owns 8 * 32 / LPR rows of one token.
+template <int FMT, int LPR, int CPL>
+__global__ void __launch_bounds__(kThreads, 2) pm_down_kernel(DecArgs a, int gshift) {
+  constexpr int kDownPrefetch = kDownLoads / CPL;  // experts whose chunks a lane holds at once
+  extern __shared__ __align__(16) uint8_t hsm[];  // [k][I/32] f16 chunks, then [k][I/32] sums
+  __shared__ const uint8_t* s_blk[kMaxPairs];
+  __shared__ float s_wq[kMaxPairs];
+  constexpr int RPWd = 32 / LPR;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int I = a.I, IC = I / 32, RB = geo.RB, H = a.H;
-  const int nD = g.nD, nV = g.nValid;
-  const int stageB = nD * geo.segB;
-  const int nsB = max(1, min(kMaxStages, stageB > 0 ? geo.ringB / stageB : 1));
-  uint8_t* ring = sm;
-  uint8_t* hsm = sm + geo.ringB;
-  float* hsum = reinterpret_cast<float*>(hsm + geo.hbytes);
-  if (tid == 0) {
-    for (int s = 0; s < nsB; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
+  const int t = blockIdx.y, k = a.k;
+  const int H = a.H, I = a.I, IC = I / 32;
+  const int row = (blockIdx.x * kWarps + warp) * RPWd + lane / LPR;
+  const int sub = lane % LPR;
+  const uint32_t rowB = static_cast<uint32_t>(I / 2);
+  const uint32_t sbB = (FMT == FT_INT4) ? static_cast<uint32_t>((I / a.group) * 2) : static_cast<uint32_t>(I / 16);
+  float* hsum = reinterpret_cast<float*>(hsm + static_cast<size_t>(k) * IC * kChunkBytes);
+
+  // the token's k blocks (gate/up reports bad ids; nothing is reported here)
+  for (int j = tid; j < k; j += kThreads) {
+    const int p = t * k + j;
+    const uint8_t* blk = pair_block(a, p, false);
+    s_blk[j] = blk;
+    float wq = 0.f;
+    if (blk != nullptr) {
+      wq = a.topk_w[p];
+      if constexpr (FMT == FT_NVFP4)
+        wq *= __ldg(a.tscale + 3 * (static_cast<int64_t>(a.layer) * a.E + a.raw_ids[p]) + 2);
     }
-    fence_barrier_init();
+    s_wq[j] = wq;
   }
-  for (int q = tid; q < nV; q += blockDim.x) {
-    const int p = g.sortedPair[q];
-    s_w[q] = a.topk_w[p];
-    s_tok[q] = p / a.k;
-  }
-  for (int d = tid; d < nD; d += blockDim.x)
-    for (int q = g.dStart[d]; q < g.dStart[d + 1]; ++q) s_d[q] = d;
   __syncthreads();
 
-  const int U = H / RB;
-  const int u0 = static_cast<int>(static_cast<long long>(U) * blockIdx.x / gridDim.x);
-  const int u1 = static_cast<int>(static_cast<long long>(U) * (blockIdx.x + 1) / gridDim.x);
-  const int nu = u1 - u0;
-  const uint32_t rowB = static_cast<uint32_t>(I / 2);
-  const uint32_t sbB = static_cast<uint32_t>(geo.sbB);
-
-  if (warp == kConsumerWarps) {
-    // weights do not depend on the previous grid: stream them before its end
-    if (lane == 0) {
-      int ncached = 0;
-      for (int d = 0; d < nD; ++d) ncached += (g.dCached[d] != 0);
-      int issued = 0;
-      for (int i = 0; i < nu; ++i) {
-        const int st = i % nsB;
-        if (i >= nsB && !mbar_wait(&empty[st], ((i / nsB) - 1) & 1, a.dev_status)) break;
-        const int r0 = (u0 + i) * RB;
-        uint8_t* dst = ring + static_cast<size_t>(st) * stageB;
-        if (ncached > 0) {
-          mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(ncached * geo.segB));
-          for (int d = 0; d < nD; ++d) {
-            if (!g.dCached[d]) continue;
-            const uint8_t* blk = g.dBlock[d];
-            bulk_g2s(dst + d * geo.segB, blk + a.off[2] + r0 * rowB, RB * rowB, &full[st]);
-            bulk_g2s(dst + d * geo.segB + RB * rowB, blk + a.off[5] + r0 * sbB, RB * sbB, &full[st]);
+  float acc = 0.f;
+  for (int j0 = 0; j0 < k; j0 += kDownPrefetch) {
+    // weights first: they do not depend on the previous grid
+    uint4 w[kDownPrefetch][CPL];
+    uint32_t sc[kDownPrefetch][CPL];
+#pragma unroll
+    for (int e = 0; e < kDownPrefetch; ++e) {
+      const int j = j0 + e;
+      const uint8_t* blk = j < k ? s_blk[j] : nullptr;
+      if (blk != nullptr) {
+        const uint8_t* r = blk + a.off[2] + static_cast<uint64_t>(row) * rowB;
+        const uint8_t* sr = blk + a.off[5] + static_cast<uint64_t>(row) * sbB;
+#pragma unroll
+        for (int m = 0; m < CPL; ++m) {
+          const int c = sub + LPR * m;
+          if (c < IC) {
+            w[e][m] = __ldg(reinterpret_cast<const uint4*>(r) + c);
+            sc[e][m] = load_scale<FMT>(sr, c, gshift);
           }
-        } else {
-          mbar_arrive(&full[st]);
-        }
-        issued = i + 1;
-      }
-      for (int i = max(0, issued - nsB); i < issued; ++i)
-        if (!mbar_wait(&full[i % nsB], (i / nsB) & 1, a.dev_status)) break;
-    }
-    return;
-  }
-
-  // h comes from the gate/up grid: wait for it, then stage it as f16 chunks
-  pdl_wait();
-  for (int q = warp; q < nV; q += kConsumerWarps) {
-    const float* hp = a.h + static_cast<size_t>(g.sortedPair[q]) * I;
-    float m = 0.f;
-    for (int i = lane; i < I; i += 32) m = fmaxf(m, fabsf(hp[i]));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    const float mul = f16_prescale(m);
-    if (lane == 0) s_inv[q] = 1.f / mul;
-    for (int c = lane; c < IC; c += 32) {
-      float v[32];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float4 f = *reinterpret_cast<const float4*>(hp + 32 * c + 4 * j);
-        v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
-      }
-      hsum[q * IC + c] = pack_chunk<FMT>(v, mul, hsm + static_cast<size_t>(q * IC + c) * kChunkBytes);
-    }
-  }
-  asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
-
-  for (int i = 0; i < nu; ++i) {
-    const int st = i % nsB;
-    if (!mbar_wait(&full[st], (i / nsB) & 1, a.dev_status)) break;
-    const int r0 = (u0 + i) * RB;
-    const uint8_t* stg = ring + static_cast<size_t>(st) * stageB;
-    for (int rr = 0; rr < RB; ++rr) {
-      if (((i * RB + rr) & (kConsumerWarps - 1)) != warp) continue;
-      const int r = r0 + rr;
-      float acc[NT];
-#pragma unroll
-      for (int t = 0; t < NT; ++t) acc[t] = 0.f;
-      for (int it = lane; it < nV * IC; it += 32) {
-        const int q = it / IC, c = it % IC;
-        const int d = s_d[q];
-        const uint8_t* blk = g.dBlock[d];
-        const bool cached = g.dCached[d] != 0;
-        const uint8_t* dc = cached ? stg + d * geo.segB + rr * rowB : blk + a.off[2] + static_cast<uint64_t>(r) * rowB;
-        const uint8_t* ds = cached ? stg + d * geo.segB + RB * rowB + rr * sbB
-                                   : blk + a.off[5] + static_cast<uint64_t>(r) * sbB;
-        float part = chunk<FMT>(dc, ds, c, a.group, hsm + static_cast<size_t>(q * IC + c) * kChunkBytes,
-                                hsum[q * IC + c]);
-        float wq = s_w[q] * s_inv[q];
-        if constexpr (FMT == FT_NVFP4)
-          wq *= __ldg(a.tscale + 3 * (static_cast<int64_t>(a.layer) * a.E + g.dExpert[d]) + 2);
-        const int tok = s_tok[q];
-#pragma unroll
-        for (int t = 0; t < NT; ++t)
-          if (t == tok) acc[t] = fmaf(wq, part, acc[t]);
-      }
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        if (t >= a.T) break;
-        const float v = warp_sum(acc[t]);
-        if (lane == 0) {
-          if (a.out_bf16)
-            static_cast<uint16_t*>(a.out)[static_cast<size_t>(t) * H + r] = f32_to_bf16(v);
-          else
-            static_cast<float*>(a.out)[static_cast<size_t>(t) * H + r] = v;
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
+    if (j0 == 0) {
+      // h comes from the gate/up grid: wait for it, then stage this token's
+      // k rows as f16 chunks (one warp per pair)
+      pdl_wait();
+      for (int j = warp; j < k; j += kWarps) {
+        if (s_blk[j] == nullptr) continue;
+        const float* hp = a.h + static_cast<size_t>(t * k + j) * I;
+        float v[32];
+        float m = 0.f;
+        if (lane < IC) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 f = *reinterpret_cast<const float4*>(hp + 32 * lane + 4 * q);
+            v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
+        }
+        for (int c = lane + 32; c < IC; c += 32) {  // I > 1024: a first pass for the max
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 f = *reinterpret_cast<const float4*>(hp + 32 * c + 4 * q);
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
+          }
+        }
+        const float mul = f16_prescale(warp_max(m));
+        if (lane == 0) s_wq[j] /= mul;
+        uint32_t o[16];
+        if (lane < IC) {
+          hsum[j * IC + lane] = pack32<FMT>(v, mul, o);
+          uint8_t* dst = hsm + static_cast<size_t>(j * IC + lane) * kChunkBytes;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(dst + 16 * q) = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        }
+        for (int c = lane + 32; c < IC; c += 32) {  // the second read hits L1
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 f = *reinterpret_cast<const float4*>(hp + 32 * c + 4 * q);
+            v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
+          }
+          hsum[j * IC + c] = pack32<FMT>(v, mul, o);
+          uint8_t* dst = hsm + static_cast<size_t>(j * IC + c) * kChunkBytes;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(dst + 16 * q) = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        }
+      }
+      __syncthreads();
+    }
+#pragma unroll
+    for (int e = 0; e < kDownPrefetch; ++e) {
+      const int j = j0 + e;
+      if (j < k && s_blk[j] != nullptr) {
+        float s = 0.f;
+#pragma unroll
+        for (int m = 0; m < CPL; ++m) {
+          const int c = sub + LPR * m;
+          if (c < IC) {
+            const uint8_t* hp = hsm + static_cast<size_t>(j * IC + c) * kChunkBytes;
+            uint32_t ha[16];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint4 v = *reinterpret_cast<const uint4*>(hp + 16 * q);
+              ha[4 * q] = v.x; ha[4 * q + 1] = v.y; ha[4 * q + 2] = v.z; ha[4 * q + 3] = v.w;
+            }
+            s += chunk_dot<FMT>(w[e][m], sc[e][m], ha, hsum[j * IC + c]);
+          }
+        }
+        acc = fmaf(s_wq[j], s, acc);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (sub == 0) {
+    const size_t idx = static_cast<size_t>(t) * H + row;
+    if (a.out_bf16) static_cast<uint16_t*>(a.out)[idx] = f32_to_bf16(acc);
+    else static_cast<float*>(a.out)[idx] = acc;
   }
 }
 
-int pow2_rows(int row_bytes_a, int row_bytes_b) {
-  for (int r = 1; r <= 16; r *= 2)
-    if ((r * row_bytes_a) % 16 == 0 && (r * row_bytes_b) % 16 == 0) return r;
-  return 0;
+template <int FMT, int CPL, int RPW>
+ft_status launch_gateup(const DecArgs& a, int gshift, cudaStream_t s) {
+  const dim3 grid(a.I / (kWarps * RPW), a.T * a.k);
+  pm_gateup_kernel<FMT, CPL, RPW><<<grid, kThreads, 0, s>>>(a, gshift);
+  return launch_check("experts decode gate/up");
 }
 
-template <int FMT, int NT>
-ft_status launch_v2(const DecArgs& a, const V2Geo& geo, size_t smemA, size_t smemB, int grid,
-                    cudaStream_t s) {
+template <int FMT, int LPR, int CPL>
+ft_status launch_down(const DecArgs& a, int gshift, cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(a.k) * (a.I / 32) * (kChunkBytes + 4);
   static bool attr = false;
   if (!attr) {
-    cudaFuncSetAttribute(v2_gateup_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    cudaFuncSetAttribute(v2_down_kernel<FMT, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    cudaFuncSetAttribute(pm_down_kernel<FMT, LPR, CPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     attr = true;
   }
-  v2_gateup_kernel<FMT><<<grid, kV2Threads, smemA, s>>>(a, geo);
-  ft_status st = launch_check("experts decode gate/up (streaming)");
-  if (st != FT_OK) return st;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kV2Threads);
-  cfg.dynamicSmemBytes = smemB;
+  cfg.gridDim = dim3(a.H / (kWarps * (32 / LPR)), a.T);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attrs[1];
   attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attrs[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, v2_down_kernel<FMT, NT>, a, geo);
-  if (e != cudaSuccess) return fail(FT_ERR_CUDA, "experts decode down (streaming): %s", cudaGetErrorString(e));
-  return launch_check("experts decode down (streaming)");
+  cudaError_t e = cudaLaunchKernelEx(&cfg, pm_down_kernel<FMT, LPR, CPL>, a, gshift);
+  if (e != cudaSuccess) return fail(FT_ERR_CUDA, "experts decode down: %s", cudaGetErrorString(e));
+  return launch_check("experts decode down");
+}
+
+template <int FMT>
+ft_status launch_pm(const DecArgs& a, int gshift, cudaStream_t s) {
+  const int HC = a.H / 32, IC = a.I / 32;
+  ft_status st;
+  // gate/up: chunks per lane x rows per warp = 4 pairs of 16-byte loads
+  if (HC <= 32) st = launch_gateup<FMT, 1, 4>(a, gshift, s);
+  else if (HC <= 64) st = launch_gateup<FMT, 2, 2>(a, gshift, s);
+  else st = launch_gateup<FMT, 4, 1>(a, gshift, s);
+  if (st != FT_OK) return st;
+  // down: lanes per row
+  if (IC <= 8) return launch_down<FMT, 8, 1>(a, gshift, s);
+  if (IC <= 16) return launch_down<FMT, 16, 1>(a, gshift, s);
+  if (IC <= 32) return launch_down<FMT, 32, 1>(a, gshift, s);
+  if (IC <= 64) return launch_down<FMT, 32, 2>(a, gshift, s);
+  return launch_down<FMT, 32, 4>(a, gshift, s);
 }
 
 }  // namespace
 
-// Plan and launch the streaming pair of kernels; FT_ERR_UNSUPPORTED when the
-// shape does not fit them (the caller then uses the general kernels).
+// Launch the pair-major kernels; FT_ERR_UNSUPPORTED when the shape does not
+// fit them (the caller then uses the general kernels).
 ft_status decode_streaming(const DecArgs& a, cudaStream_t s) {
-  const int T = a.T, n = a.T * a.k, H = a.H, I = a.I;
-  if (T > kV2MaxTok) return FT_ERR_UNSUPPORTED;
-  V2Geo geo;
-  geo.sbA = (a.fmt == FT_INT4) ? (H / a.group) * 2 : H / 16;
-  geo.sbB = (a.fmt == FT_INT4) ? (I / a.group) * 2 : I / 16;
-  const int ra = pow2_rows(H / 2, geo.sbA), rb = pow2_rows(I / 2, geo.sbB);
-  if (ra == 0 || rb == 0) return FT_ERR_UNSUPPORTED;
-  geo.RA = max(ra, 4);
-  geo.RB = max(rb, 2);
-  if (I % geo.RA || H % geo.RB) return FT_ERR_UNSUPPORTED;
-  geo.stageA = 2 * geo.RA * (H / 2 + geo.sbA);
-  geo.segB = geo.RB * (I / 2 + geo.sbB);
-  geo.xbytes = T * (H / 32) * kChunkBytes;
-  geo.hbytes = n * (I / 32) * kChunkBytes;
-  const size_t xsum = static_cast<size_t>(T) * (H / 32) * 4;
-  const size_t hsum = static_cast<size_t>(n) * (I / 32) * 4;
-  const size_t stageBmax = static_cast<size_t>(n) * geo.segB;
-  // shared memory of one SM holds one CTA of each kernel
-  const size_t budget = 196 * 1024;
-  const size_t fixed = geo.xbytes + xsum + geo.hbytes + hsum;
-  if (fixed + geo.stageA + stageBmax > budget) return FT_ERR_UNSUPPORTED;
-  const size_t rings = budget - fixed;
-  size_t ringA = rings / 2, ringB = rings - ringA;
-  if (ringB < stageBmax) {
-    ringB = stageBmax;
-    ringA = rings - ringB;
-  }
-  geo.nsA = static_cast<int>(std::min<size_t>(kMaxStages, ringA / geo.stageA));
-  if (geo.nsA < 1) return FT_ERR_UNSUPPORTED;
-  ringB = std::min<size_t>(ringB, static_cast<size_t>(kMaxStages) * stageBmax);
-  ringB = std::max<size_t>(stageBmax, ringB & ~static_cast<size_t>(127));
-  geo.ringB = static_cast<int>(ringB);
-  const size_t smemA = static_cast<size_t>(geo.nsA) * geo.stageA + geo.xbytes + xsum;
-  const size_t smemB = geo.ringB + geo.hbytes + hsum;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int grid = sms > 0 ? sms : 148;
-  const int NT = T <= 1 ? 1 : (T <= 2 ? 2 : (T <= 4 ? 4 : 8));
-  if (a.fmt == FT_INT4) {
-    if (NT == 1) return launch_v2<FT_INT4, 1>(a, geo, smemA, smemB, grid, s);
-    if (NT == 2) return launch_v2<FT_INT4, 2>(a, geo, smemA, smemB, grid, s);
-    if (NT == 4) return launch_v2<FT_INT4, 4>(a, geo, smemA, smemB, grid, s);
-    return launch_v2<FT_INT4, 8>(a, geo, smemA, smemB, grid, s);
-  }
-  if (NT == 1) return launch_v2<FT_NVFP4, 1>(a, geo, smemA, smemB, grid, s);
-  if (NT == 2) return launch_v2<FT_NVFP4, 2>(a, geo, smemA, smemB, grid, s);
-  if (NT == 4) return launch_v2<FT_NVFP4, 4>(a, geo, smemA, smemB, grid, s);
-  return launch_v2<FT_NVFP4, 8>(a, geo, smemA, smemB, grid, s);
+  const int HC = a.H / 32, IC = a.I / 32;
+  if (HC > 128 || IC > 128 || a.T * a.k > kMaxPairs || a.T > 65535) return FT_ERR_UNSUPPORTED;
+  const int rpw = HC <= 32 ? 4 : (HC <= 64 ? 2 : 1);
+  if (a.I % (kWarps * rpw)) return FT_ERR_UNSUPPORTED;
+  const int lpr = IC <= 8 ? 8 : (IC <= 16 ? 16 : 32);
+  if (a.H % (kWarps * (32 / lpr))) return FT_ERR_UNSUPPORTED;
+  if (static_cast<size_t>(a.k) * IC * (kChunkBytes + 4) > 200 * 1024) return FT_ERR_UNSUPPORTED;
+  const int gshift = (a.fmt == FT_INT4) ? (a.group == 32 ? 0 : (a.group == 64 ? 1 : 2)) : 0;
+  if (a.fmt == FT_INT4) return launch_pm<FT_INT4>(a, gshift, s);
+  return launch_pm<FT_NVFP4>(a, gshift, s);
 }
 
 }  // namespace ft
