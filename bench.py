@@ -205,7 +205,7 @@ class DecodeWorkload:
         self.ff = torch.empty((L, self.ml), dtype=torch.int32, device=device)
         self.fs = torch.empty((L, self.ml), dtype=torch.int32, device=device)
         self.rws = torch.empty(ft.route_workspace(T, E), dtype=torch.uint8, device=device)
-        self.ews = torch.empty(ft.experts_workspace(ft.FT_DECODE, T, k, H, I, E), dtype=torch.uint8,
+        self.ews = torch.zeros(ft.experts_workspace(ft.FT_DECODE, T, k, H, I, E), dtype=torch.uint8,
                                device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.events = None
@@ -567,7 +567,7 @@ def reshape_workload(wl, T, n_steps):
     wl.ff = torch.empty((L, wl.ml), dtype=torch.int32, device=dev)
     wl.fs = torch.empty((L, wl.ml), dtype=torch.int32, device=dev)
     wl.rws = torch.empty(ft.route_workspace(T, E), dtype=torch.uint8, device=dev)
-    wl.ews = torch.empty(ft.experts_workspace(ft.FT_DECODE, T, k, H, cfg.I, E), dtype=torch.uint8, device=dev)
+    wl.ews = torch.zeros(ft.experts_workspace(ft.FT_DECODE, T, k, H, cfg.I, E), dtype=torch.uint8, device=dev)
     return wl
 
 

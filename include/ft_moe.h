@@ -219,8 +219,9 @@ FT_API ft_status ft_moe_fetch(const ft_bank* pool_host, const ft_bank* cache_hos
  *   when pool is non-NULL (the host-path pair, read in place), else the pair
  *   is skipped (masked: deep-dive pattern 3).  out [T,H] (FT_OUT_F32 or
  *   FT_OUT_BF16) = sum over computed pairs of topk_w * y, combine fused.
- *   Each distinct expert's bytes are read once for all its tokens.  h is
- *   kept in fp32.  Limits: T*k <= 256, T <= 16.  offsets unused (NULL).
+ *   h is kept in fp32.  Two pairs of one expert each read its rows (the
+ *   repeat is served from L2).  Limits:
+ *   T*k <= 256, T <= 16.  offsets unused (NULL).
  * FT_PREFILL: x is the permuted batch Xp [T*k, H] in f16 as ft_moe_permute
  *   writes it with FT_XP_F16, x_scale [T*k] its per-row factors; offsets
  *   [E+1] its expert segments; slot_ids is a per-expert table [E] (the block
@@ -249,8 +250,9 @@ FT_API ft_status ft_moe_experts_fwd(const ft_bank* cache_host, const ft_bank* po
  * running inside a stream capture, hosts whose GPU memory belongs to another
  * framework's pool, loops that cannot afford an allocation's synchronisation.
  * Same arguments and results as the decode mode above, minus ws.  Limits and
- * rules: T*k*I*4 must not exceed 1 MiB (else FT_ERR_INVALID, nothing
- * launched); every GPU that loads the library keeps the array until exit;
+ * rules: ft_moe_experts_workspace(FT_DECODE, ...) = T*k*I*4 (rounded up to
+ * 256) must not exceed 1 MiB (else FT_ERR_INVALID, nothing launched); every
+ * GPU that loads the library keeps the array until exit;
  * calls that may overlap on the GPU share the array and race, so the caller
  * serialises them; the first call on a device looks the array up (with that
  * device current) and should happen before any stream capture.

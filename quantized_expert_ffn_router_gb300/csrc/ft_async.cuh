@@ -85,6 +85,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Bulk prefetch of global memory into L2 (no destination, no completion).
+// Address 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void l2_prefetch(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Programmatic dependent launch: let the next grid in the stream start, and
 // wait for the previous grid's completion and memory.
 __device__ __forceinline__ void pdl_launch_dependents() {

@@ -183,4 +183,5 @@ __device__ __forceinline__ bool build_groups(const DecArgs& a, Groups& g) {
 // not fit them.
 ft_status decode_streaming(const DecArgs& a, cudaStream_t s);
 
+
 }  // namespace ft

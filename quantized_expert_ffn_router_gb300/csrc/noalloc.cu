@@ -14,7 +14,8 @@
 // Cost and rules:
 //   * the array is kStaticScratchBytes (1 MiB); every GPU on which the
 //     library is loaded holds it until the process exits;
-//   * calls whose T * k * I * 4 bytes exceed it are rejected (FT_ERR_INVALID);
+//   * calls whose decode workspace (T * k * I * 4 bytes, rounded up) exceeds
+//     it are rejected (FT_ERR_INVALID);
 //   * all calls share the one array: calls that may overlap on the GPU (two
 //     streams, or two threads' streams) race on it and must be serialised by
 //     the caller;
@@ -68,7 +69,7 @@ ft_status ft_moe_experts_decode_static(const ft_bank* cache_host, const ft_bank*
   FT_REQUIRE(T >= 0 && k >= 1, "experts decode (static scratch): T=%d k=%d", T, k);
   const size_t need = ft_moe_experts_workspace(FT_DECODE, T, k, cache_host->H, cache_host->I, E);
   FT_REQUIRE(need <= ft::kStaticScratchBytes,
-             "experts decode (static scratch): T*k*I*4 = %zu bytes exceeds the %zu-byte static scratch",
+             "experts decode (static scratch): the workspace (%zu bytes) exceeds the %zu-byte static scratch",
              need, ft::kStaticScratchBytes);
   void* ws = nullptr;
   ft_status st = ft::scratch_for_current_device(&ws);

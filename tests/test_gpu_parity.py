@@ -260,7 +260,8 @@ def test_fetch_copies_chosen_blocks(cuda_lib, pinned):
 
 
 # ---------------------------------------------------------- experts decode
-def _decode_case(ft, cfg, T, layer, cached_frac, use_pool, pool_pinned=False, out_bf16=False, seed_tag="dec"):
+def _decode_case(ft, cfg, T, layer, cached_frac, use_pool, pool_pinned=False, out_bf16=False, seed_tag="dec",
+                 ws=None):
     """Route with the oracle, resolve on a partially filled cache, run the
     decode experts and compare with the oracle over the covered pairs."""
     E, k = cfg.E, cfg.k
@@ -294,7 +295,8 @@ def _decode_case(ft, cfg, T, layer, cached_frac, use_pool, pool_pinned=False, ou
             pool[f].copy_(torch.from_numpy(blocks[f]))
         pb = ft.make_bank(cfg.fmt, cfg.H, cfg.I, cfg.g, pool, ts)
     out = torch.empty((T, cfg.H), dtype=torch.bfloat16 if out_bf16 else torch.float32, device=DEV)
-    ws = torch.empty(ft.experts_workspace(ft.FT_DECODE, T, k, cfg.H, cfg.I, E), dtype=torch.uint8, device=DEV)
+    if ws is None:
+        ws = torch.zeros(ft.experts_workspace(ft.FT_DECODE, T, k, cfg.H, cfg.I, E), dtype=torch.uint8, device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     ft.experts_fwd(cb, pb, layer, E, _t(x), T, k, _t(slot_np), _t(ids), _t(w32), out, ws, dev_status=status)
     torch.cuda.synchronize()
@@ -305,13 +307,27 @@ def _decode_case(ft, cfg, T, layer, cached_frac, use_pool, pool_pinned=False, ou
     return got, ref, x, ids, w32, slot_np, blocks, ts_np
 
 
-@pytest.mark.parametrize("name,T", [("tiny", 8), ("tiny", 12), ("d35b", 1), ("d35b", 3), ("d35b", 8),
+@pytest.mark.parametrize("name,T", [("tiny", 1), ("tiny", 8), ("tiny", 12), ("d35b", 1), ("d35b", 3), ("d35b", 8),
                                     ("d35b", 16), ("flash", 1), ("flash", 2), ("flash", 9)])
 def test_experts_decode_all_cached(cuda_lib, name, T):
-    """T <= 8 runs the streaming kernels, larger batches the general ones."""
+    """Every batch size up to 16 runs the pair-major kernels."""
     cfg = synth.get_config(name)
     got, ref, *_ = _decode_case(cuda_lib, cfg, T, layer=1 % cfg.L, cached_frac=1.0, use_pool=False)
     assert_close(got, ref, f"{name} T={T}")
+
+
+@pytest.mark.parametrize("name", ["tiny", "d35b"])
+def test_experts_decode_single_token_reuses_workspace(cuda_lib, name):
+    """Consecutive single-token calls on one workspace stay correct (nothing
+    of an earlier call leaks into the next)."""
+    ft = cuda_lib
+    cfg = synth.get_config(name)
+    ws = torch.zeros(ft.experts_workspace(ft.FT_DECODE, 1, cfg.k, cfg.H, cfg.I, cfg.E), dtype=torch.uint8,
+                     device=DEV)
+    for call in range(3):
+        got, ref, *_ = _decode_case(ft, cfg, 1, layer=0, cached_frac=1.0, use_pool=False,
+                                    seed_tag=f"reuse{call}", ws=ws)
+        assert_close(got, ref, f"{name} call {call}")
 
 
 @pytest.mark.parametrize("name,T", [("tiny", 8), ("d35b", 8), ("flash", 1)])
@@ -358,7 +374,7 @@ def test_experts_decode_duplicate_ids_in_a_token(cuda_lib, name, T):
     ts = None if ts_np is None else _t(ts_np)
     cb = ft.make_bank(cfg.fmt, cfg.H, cfg.I, cfg.g, cache, ts)
     out = torch.empty((T, cfg.H), dtype=torch.float32, device=DEV)
-    ws = torch.empty(ft.experts_workspace(0, T, k, cfg.H, cfg.I, E), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(ft.experts_workspace(0, T, k, cfg.H, cfg.I, E), dtype=torch.uint8, device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     ft.experts_fwd(cb, None, layer, E, _t(x), T, k, _t(ids), _t(ids), _t(w), out, ws, dev_status=status)
     torch.cuda.synchronize()
@@ -379,7 +395,7 @@ def test_experts_decode_bad_ids_flagged(cuda_lib):
     raw = torch.tensor([[0, 1], [2, 99]], dtype=torch.int32, device=DEV)  # id 99 outside E
     w = torch.ones((T, k), dtype=torch.float32, device=DEV)
     out = torch.empty((T, cfg.H), dtype=torch.float32, device=DEV)
-    ws = torch.empty(ft.experts_workspace(0, T, k, cfg.H, cfg.I, cfg.E), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(ft.experts_workspace(0, T, k, cfg.H, cfg.I, cfg.E), dtype=torch.uint8, device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     ft.experts_fwd(cb, None, 0, cfg.E, x, T, k, slot, raw, w, out, ws, dev_status=status)
     torch.cuda.synchronize()

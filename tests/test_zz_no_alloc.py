@@ -41,7 +41,7 @@ def test_static_scratch_matches_workspace_call_twice(cuda_lib, name, T):
         cb = ft.make_bank(cfg.fmt, cfg.H, cfg.I, cfg.g, blocks, ts)
         args = [torch.from_numpy(a).to(DEV) for a in (x.view(np.int16), slots, ids, w)]
         ref = torch.empty((T, cfg.H), dtype=torch.float32, device=DEV)
-        ws = torch.empty(ft.experts_workspace(ft.FT_DECODE, T, cfg.k, cfg.H, cfg.I, cfg.E),
+        ws = torch.zeros(ft.experts_workspace(ft.FT_DECODE, T, cfg.k, cfg.H, cfg.I, cfg.E),
                          dtype=torch.uint8, device=DEV)
         ft.experts_fwd(cb, None, 0, cfg.E, args[0], T, cfg.k, args[1], args[2], args[3], ref, ws)
         got = torch.empty((T, cfg.H), dtype=torch.float32, device=DEV)
