@@ -34,6 +34,10 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s; decode expert-weight HBM GB/s; prefill grouped-GEMM TFLOP/s"
+# DRAM bytes (read + write) of one experts call (gate/up + down kernels) from
+# an ncu capture of the same kernels on this workload's shape; None until
+# captured (see profiles/decode_experts_d35b.md)
+TRAFFIC_PER_CALL = {}
 UNIT = "MoE-layer tokens/s"
 
 
@@ -68,7 +72,7 @@ def torch_reduce_fn(device):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms while active."""
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms while active."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -84,7 +88,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -208,55 +212,71 @@ class DecodeWorkload:
         self.ews = torch.zeros(ft.experts_workspace(ft.FT_DECODE, T, k, H, I, E), dtype=torch.uint8,
                                device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
-        self.events = None
 
-    # one pass of the hot path over all layers (enqueue only)
-    def step(self, events=None):
+    # one pass of the hot path over all layers (enqueue only); `ev` holds
+    # per-layer events: 2 around the experts call, or 5 around every op
+    def step(self, ev=None, per_op=False):
         ft, cfg, T = self.ft, self.cfg, self.T
+
+        def mark(l, i):
+            if ev is not None and (per_op or i in (3, 4)):
+                ev[l][i if per_op else i - 3].record()
+
         for l in range(cfg.L):
-            if events is not None:
-                events[l][0].record()
+            mark(l, 0)
             ft.route(self.x_stage[l], self.W[l], cfg.k, self.ids[l], self.w[l], self.rws)
-            if events is not None:
-                events[l][1].record()
+            mark(l, 1)
             ft.resolve_slots(self.state, l, self.ids[l], self.phi, self.slot[l], self.nf[l], self.ff[l],
                              self.fs[l], self.status)
-            if events is not None:
-                events[l][2].record()
+            mark(l, 2)
             ft.fetch(self.pool_b, self.cache_b, self.nf[l], self.ff[l], self.fs[l], self.status)
-            if events is not None:
-                events[l][3].record()
+            mark(l, 3)
             ft.experts_fwd(self.cache_b, self.pool_b, l, cfg.E, self.x_stage[l], T, cfg.k, self.slot[l],
                            self.ids[l], self.w[l], self.out[l], self.ews, dev_status=self.status)
-            if events is not None:
-                events[l][4].record()
+            mark(l, 4)
 
     def capture(self):
+        """Two graphs of one step: `graph` (timed) with events only around the
+        experts calls, `graph_ops` with events around every op (breakdown)."""
         import torch
 
-        try:
-            self.events = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
-                           for _ in range(self.cfg.L)]
-        except TypeError:
-            self.events = None
+        def events(n):
+            return [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(n)]
+                    for _ in range(self.cfg.L)]
+
+        self.ev_exp, self.ev_ops = events(2), events(5)
         self.x_stage.copy_(self.x_all[0])
         self.step()  # eager warm-up (attributes, lazy init) before capture
         torch.cuda.synchronize()
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph):
-            self.step(self.events)
+            self.step(self.ev_exp)
+        self.graph_ops = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph_ops):
+            self.step(self.ev_ops, per_op=True)
         torch.cuda.synchronize()
 
-    def kernel_times(self):
-        """Per-op device time (us, summed over layers) of the last replay."""
-        if self.events is None:
-            return None
+    def experts_us(self):
+        """Device time (us) of the 40 experts calls of the last timed replay."""
+        return sum(e[0].elapsed_time(e[1]) for e in self.ev_exp) * 1e3
+
+    def op_times(self, reps: int = 5):
+        """Per-op device time (us per step, summed over layers): the median of
+        a few replays of the per-op graph, outside the timed region."""
+        import torch
+
         names = ["route", "resolve", "fetch", "experts"]
-        tot = {n: 0.0 for n in names}
-        for ev in self.events:
-            for i, n in enumerate(names):
-                tot[n] += ev[i].elapsed_time(ev[i + 1]) * 1e3
-        return tot
+        runs = []
+        for i in range(reps):
+            self.x_stage.copy_(self.x_all[i % self.x_all.shape[0]])
+            self.graph_ops.replay()
+            torch.cuda.synchronize()
+            tot = {n: 0.0 for n in names}
+            for ev in self.ev_ops:
+                for j, n in enumerate(names):
+                    tot[n] += ev[j].elapsed_time(ev[j + 1]) * 1e3
+            runs.append(tot)
+        return {n: statistics.median(r[n] for r in runs) for n in names}
 
     def distinct_expert_bytes(self):
         """Algorithmic expert bytes of the last step: distinct experts per layer
@@ -289,12 +309,14 @@ def time_device(wl, steps: int, warmup: int, reduce_fn, world: int, clocks=None)
         clocks.start()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.cudart().cudaProfilerStart()  # a profiler started with --profile-from-start off sees only this
     e0.record(s)
     for i in range(steps):
         wl.x_stage.copy_(wl.x_all[(warmup + i) % wl.x_all.shape[0]])
         wl.graph.replay()
     e1.record(s)
     torch.cuda.synchronize()
+    torch.cuda.cudart().cudaProfilerStop()
     if clocks:
         clocks.stop()
     if world > 1:
@@ -306,13 +328,17 @@ def time_device(wl, steps: int, warmup: int, reduce_fn, world: int, clocks=None)
 
 def time_e2e(wl, steps: int, warmup: int):
     """Host buffers in, host buffers out: pinned H2D of the step's inputs,
-    graph replay, D2H of the step's outputs, all inside the timed region."""
+    graph replay, D2H of the step's outputs, all inside the timed region.
+    Uses the inputs after those of the device-timed run (fresh tokens, so
+    the cache sees as many misses as there)."""
     import torch
 
     out_host = torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory()
     s = torch.cuda.current_stream()
+    first = warmup + steps
+    n_in = wl.x_host.shape[0]
     for i in range(warmup):
-        wl.x_stage.copy_(wl.x_host[i % wl.x_host.shape[0]], non_blocking=True)
+        wl.x_stage.copy_(wl.x_host[i % n_in], non_blocking=True)
         wl.graph.replay()
         out_host.copy_(wl.out, non_blocking=True)
     torch.cuda.synchronize()
@@ -320,7 +346,7 @@ def time_e2e(wl, steps: int, warmup: int):
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(s)
     for i in range(steps):
-        wl.x_stage.copy_(wl.x_host[(warmup + i) % wl.x_host.shape[0]], non_blocking=True)
+        wl.x_stage.copy_(wl.x_host[(first + i) % n_in], non_blocking=True)
         wl.graph.replay()
         out_host.copy_(wl.out, non_blocking=True)
     e1.record(s)
@@ -424,7 +450,7 @@ def run_reference(args, cfg, T):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--tokens", type=int, default=1, help="decode batch (1 or 8)")
@@ -463,7 +489,7 @@ def main():
         dist.init_process_group("nccl", device_id=device)
         reduce_fn = torch_reduce_fn(device)
 
-    n_steps = args.steps + args.warmup
+    n_steps = 2 * args.steps + args.warmup  # device-timed steps, then e2e steps
     results = {}
     batches = [args.tokens] + ([args.extra_batch] if args.extra_batch and args.extra_batch != args.tokens else [])
     wl = None
@@ -477,12 +503,13 @@ def main():
         secs = time_device(wl, args.steps, args.warmup, reduce_fn, world, clocks)
         units = T * cfg.L * args.steps
         value, secs_max, units_all = aggregate(units, secs, world, reduce_fn)
-        kt = wl.kernel_times()
+        exp_us = wl.experts_us()
         ebytes = wl.distinct_expert_bytes()
+        kt = wl.op_times()
         nfetch, host_pairs = wl.misses()
         e2e_secs, h2d, d2h = time_e2e(wl, args.steps, args.warmup)
         e2e_val, _, _ = aggregate(units, e2e_secs, world, reduce_fn)
-        results[T] = dict(value=value, secs=secs_max, kt=kt, ebytes=ebytes, nfetch=nfetch,
+        results[T] = dict(value=value, secs=secs_max, kt=kt, exp_us=exp_us, ebytes=ebytes, nfetch=nfetch,
                           host_pairs=host_pairs, e2e=e2e_val, h2d=h2d, d2h=d2h,
                           clocks=clocks.summary() if clocks else None)
         st = ft.get_status(wl.status)
@@ -496,15 +523,18 @@ def main():
     r = results[args.tokens]
     kt = r["kt"] or {}
     dom = max(kt, key=kt.get) if kt else "experts"
-    exp_us = kt.get("experts")
+    exp_us = r["exp_us"]
     roof = None
     if exp_us:
-        achieved = r["ebytes"] / (exp_us * 1e-6) / 1e9  # GB/s over the 40 launches of the last step
-        roof = {"bound": "hbm", "kernel": "ft_moe_experts_fwd decode (gate/up + down)",
+        # algorithmic bytes of the experts calls of the last timed step (each
+        # distinct expert's block once) / their event-timed duration
+        achieved = r["ebytes"] / (exp_us * 1e-6) / 1e9
+        roof = {"bound": "hbm", "kernel": "ft_moe_experts_fwd decode (gate/up + down kernels)",
                 "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                "frac": achieved / peaks["hbm_gbs"], "traffic": TRAFFIC_PER_CALL.get(args.tokens),
                 "peak_kind": peak_kind, "frac_of_8tbs_nominal": achieved / 8000.0,
                 "algorithmic_bytes_per_launch": r["ebytes"] / cfg.L,
+                "launch_us": exp_us / cfg.L,
                 "dominant_op_by_time": dom}
     cpu = None
     if not args.no_cpu_baseline:
@@ -538,6 +568,7 @@ def main():
             "host_path_pairs_per_step": r["host_pairs"],
             "other_batches": {str(T): {"value": v["value"], "ms_per_step": v["secs"] / args.steps * 1e3,
                                        "per_op_us_per_step": v["kt"], "expert_bytes_per_step": v["ebytes"],
+                                       "experts_us_per_layer": v["exp_us"] / cfg.L,
                                        "e2e": v["e2e"]}
                               for T, v in results.items() if T != args.tokens},
         },

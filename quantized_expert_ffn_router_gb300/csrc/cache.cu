@@ -9,7 +9,7 @@
 namespace ft {
 namespace {
 
-constexpr int kResThreads = 1024;
+constexpr int kResThreads = 256;
 constexpr int kResMaxE = 4096;
 constexpr int kResMaxN = 4096;
 
@@ -68,6 +68,42 @@ __device__ __forceinline__ uint64_t ukey(int64_t u) {
   return static_cast<uint64_t>(u) ^ 0x8000000000000000ull;
 }
 
+// The common small case in one warp: n <= 32 ids, all valid, and the q*
+// split fetches nothing (every distinct expert hits, or the split or the
+// evictable slots allow no fetch).  Then the state update is only the usage
+// of the hit slots and the recency of the distinct experts, and the outputs
+// are the map lookups -- the same results as the general path below.
+// Returns true (warp-uniform) when it has done the whole call.
+__device__ bool resolve_small_no_fetch(const ResolveArgs& a) {
+  const int lane = threadIdx.x & 31;
+  const int n = a.n, E = a.E, base = a.layer * a.E;
+  const int64_t now = *a.step;
+  const int e = lane < n ? a.ids[lane] : -1;
+  const bool bad = lane < n && (e < 0 || e >= E);
+  if (__any_sync(0xffffffffu, bad)) return false;
+  const int s = lane < n ? a.map[base + e] : -1;
+  const unsigned same = __match_any_sync(0xffffffffu, e);
+  const bool leader = lane < n && lane == __ffs(same) - 1;
+  const int nhit = __popc(__ballot_sync(0xffffffffu, leader && s >= 0));
+  const int m = __popc(__ballot_sync(0xffffffffu, leader && s < 0));
+  const int nf = max(0, min(split_q16_dev(m, a.phi), a.S - nhit));
+  if (nf > 0) return false;
+  if (leader) {
+    if (s >= 0) a.usage[s] = now;
+    a.recency[base + e] = now;
+  }
+  if (lane < n) a.slot_ids[lane] = s;
+  for (int i = lane; i < a.max_list; i += 32) {
+    a.fetch_fid[i] = -1;
+    a.fetch_slot[i] = -1;
+  }
+  if (lane == 0) {
+    *a.num_fetch = 0;
+    *a.step = now + 1;
+  }
+  return true;
+}
+
 __global__ void __launch_bounds__(kResThreads, 1) resolve_kernel(ResolveArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int E = a.E, n = a.n, S = a.S;
@@ -95,6 +131,16 @@ __global__ void __launch_bounds__(kResThreads, 1) resolve_kernel(ResolveArgs a) 
   const int tid = threadIdx.x;
   const int nt = blockDim.x;
   const int base = a.layer * E;
+
+  if (n <= 32) {
+    __shared__ int s_done;
+    if (tid < 32) {
+      const bool done = resolve_small_no_fetch(a);
+      if (tid == 0) s_done = done;
+    }
+    __syncthreads();
+    if (s_done) return;
+  }
 
   for (int e = tid; e < E; e += nt) {
     inU[e] = 0;

@@ -153,23 +153,31 @@ __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib)
   return va > vb || (va == vb && ia < ib);
 }
 
-// One warp per token: max, softmax denominator, then k rounds of "best
-// element ranked after the previous winner" (a selection with no taken set).
+// One warp per token.  The token's E logits are read once into this warp's
+// slice of shared memory (with the running max); then the softmax
+// denominator, then k rounds of "best element ranked after the previous
+// winner" (a selection with no taken set), all from shared memory.
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T,
                                                          int E, int k, int renorm,
                                                          int32_t* __restrict__ ids,
                                                          float* __restrict__ wts) {
+  extern __shared__ float lsm[];  // [warps][E]
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
+  const int t = blockIdx.x * (blockDim.x >> 5) + warp;
   if (t >= T) return;
   const float* l = logits + static_cast<size_t>(t) * E;
+  float* ls = lsm + static_cast<size_t>(warp) * E;
   float mx = -INFINITY;
-  for (int e = lane; e < E; e += 32) mx = fmaxf(mx, l[e]);
+  for (int e = lane; e < E; e += 32) {
+    const float v = l[e];
+    ls[e] = v;
+    mx = fmaxf(mx, v);
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   float z = 0.f;
-  for (int e = lane; e < E; e += 32) z += expf(l[e] - mx);
+  for (int e = lane; e < E; e += 32) z += expf(ls[e] - mx);
   z = warp_sum(z);
   float pv = INFINITY;
   int pi = -1;
@@ -180,7 +188,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
     float bv = -INFINITY;
     int bi = 0x7fffffff;
     for (int e = lane; e < E; e += 32) {
-      const float v = l[e];
+      const float v = ls[e];
       if (ranks_before(pv, pi, v, e) && ranks_before(v, e, bv, bi)) {
         bv = v;
         bi = e;
@@ -250,9 +258,12 @@ ft_status ft_moe_route(const uint16_t* x, int32_t T, int32_t H, const float* w_r
   ft_status st = ft::launch_check("route logits");
   if (st != FT_OK) return st;
   // the top-k grid starts while the logits grid drains (programmatic launch)
+  // one warp per token, each with E logits in shared memory (<= 32 KB per CTA)
+  const int warps = E <= 1024 ? 8 : 2;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((T + 7) / 8);
-  cfg.blockDim = dim3(256);
+  cfg.gridDim = dim3((T + warps - 1) / warps);
+  cfg.blockDim = dim3(32 * warps);
+  cfg.dynamicSmemBytes = static_cast<size_t>(warps) * E * sizeof(float);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
