@@ -137,6 +137,19 @@ def measured_peaks():
 
 
 # ----------------------------------------------------------- the workload --
+def step_inputs(cfg, T: int, n_steps: int):
+    """Pinned host inputs [n_steps, L, T, H] bf16 bits: step i's tokens depend
+    only on i (x ~ N(0,1), feature 0 = 1.0, the router's bias feature)."""
+    import torch
+
+    import synth
+
+    xs = np.stack([synth.normal_bf16(synth.stream_key(cfg.seed, "bench-x", T, i), (cfg.L, T, cfg.H))
+                   for i in range(n_steps)])
+    xs[..., 0] = synth.bf16_bits(np.array([1.0], np.float32))[0]
+    return torch.from_numpy(xs.view(np.int16)).pin_memory()
+
+
 class DecodeWorkload:
     """Device state of the decode benchmark for one config (built untimed)."""
 
@@ -194,9 +207,7 @@ class DecodeWorkload:
         log(f"cache warmed ({int(idx.numel())} slots) from {cfg.history_steps} history steps in "
             f"{time.time() - t0:.1f}s")
         # per-step inputs: x ~ N(0,1) bf16 with feature 0 = 1.0 (the bias feature)
-        xs = synth.normal_bf16(synth.stream_key(cfg.seed, "bench-x", T), (n_steps, L, T, H))
-        xs[..., 0] = synth.bf16_bits(np.array([1.0], np.float32))[0]
-        self.x_host = torch.from_numpy(xs.view(np.int16)).pin_memory()
+        self.x_host = step_inputs(cfg, T, n_steps)
         self.x_all = self.x_host.to(device)
         self.x_stage = torch.empty((L, T, H), dtype=torch.int16, device=device)
         self.out = torch.empty((L, T, H), dtype=torch.int16, device=device)
@@ -208,7 +219,7 @@ class DecodeWorkload:
         self.ml = T * k
         self.ff = torch.empty((L, self.ml), dtype=torch.int32, device=device)
         self.fs = torch.empty((L, self.ml), dtype=torch.int32, device=device)
-        self.rws = torch.empty(ft.route_workspace(T, E), dtype=torch.uint8, device=device)
+        self.rws = torch.zeros(ft.route_workspace(T, E), dtype=torch.uint8, device=device)
         self.ews = torch.zeros(ft.experts_workspace(ft.FT_DECODE, T, k, H, I, E), dtype=torch.uint8,
                                device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
@@ -260,15 +271,16 @@ class DecodeWorkload:
         """Device time (us) of the 40 experts calls of the last timed replay."""
         return sum(e[0].elapsed_time(e[1]) for e in self.ev_exp) * 1e3
 
-    def op_times(self, reps: int = 5):
+    def op_times(self, first: int, reps: int = 5):
         """Per-op device time (us per step, summed over layers): the median of
-        a few replays of the per-op graph, outside the timed region."""
+        a few replays of the per-op graph on fresh inputs (steps first, ...),
+        outside the timed region."""
         import torch
 
         names = ["route", "resolve", "fetch", "experts"]
         runs = []
         for i in range(reps):
-            self.x_stage.copy_(self.x_all[i % self.x_all.shape[0]])
+            self.x_stage.copy_(self.x_all[(first + i) % self.x_all.shape[0]])
             self.graph_ops.replay()
             torch.cuda.synchronize()
             tot = {n: 0.0 for n in names}
@@ -489,7 +501,7 @@ def main():
         dist.init_process_group("nccl", device_id=device)
         reduce_fn = torch_reduce_fn(device)
 
-    n_steps = 2 * args.steps + args.warmup  # device-timed steps, then e2e steps
+    n_steps = args.warmup + 2 * args.steps + 5  # device-timed steps, e2e steps, per-op breakdown
     results = {}
     batches = [args.tokens] + ([args.extra_batch] if args.extra_batch and args.extra_batch != args.tokens else [])
     wl = None
@@ -505,9 +517,10 @@ def main():
         value, secs_max, units_all = aggregate(units, secs, world, reduce_fn)
         exp_us = wl.experts_us()
         ebytes = wl.distinct_expert_bytes()
-        kt = wl.op_times()
+        kt = None
         nfetch, host_pairs = wl.misses()
         e2e_secs, h2d, d2h = time_e2e(wl, args.steps, args.warmup)
+        kt = wl.op_times(first=args.warmup + 2 * args.steps)
         e2e_val, _, _ = aggregate(units, e2e_secs, world, reduce_fn)
         results[T] = dict(value=value, secs=secs_max, kt=kt, exp_us=exp_us, ebytes=ebytes, nfetch=nfetch,
                           host_pairs=host_pairs, e2e=e2e_val, h2d=h2d, d2h=d2h,
@@ -585,9 +598,7 @@ def reshape_workload(wl, T, n_steps):
     cfg, dev, ft = wl.cfg, wl.dev, wl.ft
     L, E, k, H = cfg.L, cfg.E, cfg.k, cfg.H
     wl.T = T
-    xs = synth.normal_bf16(synth.stream_key(cfg.seed, "bench-x", T), (n_steps, L, T, H))
-    xs[..., 0] = synth.bf16_bits(np.array([1.0], np.float32))[0]
-    wl.x_host = torch.from_numpy(xs.view(np.int16)).pin_memory()
+    wl.x_host = step_inputs(cfg, T, n_steps)
     wl.x_all = wl.x_host.to(dev)
     wl.x_stage = torch.empty((L, T, H), dtype=torch.int16, device=dev)
     wl.out = torch.empty((L, T, H), dtype=torch.int16, device=dev)
@@ -597,7 +608,7 @@ def reshape_workload(wl, T, n_steps):
     wl.ml = T * k
     wl.ff = torch.empty((L, wl.ml), dtype=torch.int32, device=dev)
     wl.fs = torch.empty((L, wl.ml), dtype=torch.int32, device=dev)
-    wl.rws = torch.empty(ft.route_workspace(T, E), dtype=torch.uint8, device=dev)
+    wl.rws = torch.zeros(ft.route_workspace(T, E), dtype=torch.uint8, device=dev)
     wl.ews = torch.zeros(ft.experts_workspace(ft.FT_DECODE, T, k, H, cfg.I, E), dtype=torch.uint8, device=dev)
     return wl
 

@@ -153,8 +153,11 @@ FT_API ft_status ft_moe_get_status(const int32_t* dev_status, int32_t* out_host)
  *   renorm != 0).
  * x [T,H] bf16 row-major; w_router [E,H] fp32 row-major; topk_ids [T,k]
  * int32; topk_w [T,k] fp32.  ws: device scratch of ft_moe_route_workspace(T,E)
- * bytes (the logits).  Limits: 1 <= k <= min(E, 32), E <= 4096, H % 8 == 0.
- * T == 0 is a no-op.
+ * bytes: the logits, then (T <= 16, where one kernel computes the logits and
+ * its last CTA the top-k) an arrival counter; ws must be zero-filled before
+ * the first call that uses it, every call leaves the counter at zero, and
+ * calls that may overlap on the GPU need separate workspaces.  Limits:
+ * 1 <= k <= min(E, 32), E <= 4096, H % 8 == 0.  T == 0 is a no-op.
  */
 FT_API size_t ft_moe_route_workspace(int32_t T, int32_t E);
 FT_API ft_status ft_moe_route(const uint16_t* x, int32_t T, int32_t H, const float* w_router,

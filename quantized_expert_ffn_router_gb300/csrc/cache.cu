@@ -9,7 +9,7 @@
 namespace ft {
 namespace {
 
-constexpr int kResThreads = 256;
+constexpr int kResThreads = 1024;
 constexpr int kResMaxE = 4096;
 constexpr int kResMaxN = 4096;
 
@@ -503,7 +503,10 @@ ft_status ft_moe_resolve_slots(const ft_cache_state* st, int32_t layer, const in
     if (e != cudaSuccess)
       return ft::fail(FT_ERR_CUDA, "resolve: smem attribute: %s", cudaGetErrorString(e));
   }
-  ft::resolve_kernel<<<1, ft::kResThreads, smem, ft::as_stream(stream)>>>(a);
+  // small calls usually finish in the one-warp path; 256 threads keep the
+  // rest cheap to synchronise.  Larger calls get the whole block.
+  const int threads = n <= 32 ? 256 : ft::kResThreads;
+  ft::resolve_kernel<<<1, threads, smem, ft::as_stream(stream)>>>(a);
   return ft::launch_check("resolve_slots");
 }
 

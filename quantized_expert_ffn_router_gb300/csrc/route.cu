@@ -16,16 +16,29 @@ namespace {
 
 constexpr int kGemvMaxT = 16;
 constexpr int kRouteMaxK = 32;
+constexpr int kRouteMaxE = 4096;
+
+size_t route_logits_bytes(int T, int E) {
+  return (static_cast<size_t>(T) * E * sizeof(float) + 255) & ~static_cast<size_t>(255);
+}
 
 // Small token counts: one CTA per expert row, its 8 warps splitting the
 // hidden axis, so the whole router matrix is requested by the whole GPU at
-// once; partial sums meet in shared memory (fixed order).
+// once; partial sums meet in shared memory (fixed order).  The last CTA to
+// finish (an arrival counter after the logits in the workspace, back at zero
+// when the call ends) then runs the softmax and top-k of every token.
+__device__ __forceinline__ void topk_warp(const float* __restrict__ l, float* ls, int E, int k, int renorm,
+                                          int32_t* __restrict__ ids_t, float* __restrict__ wts_t);
+
 template <int TMAX>
 __global__ void __launch_bounds__(256) route_rows_kernel(const uint16_t* __restrict__ x, int T, int H,
                                                          const float* __restrict__ W, int E,
-                                                         float* __restrict__ logits) {
+                                                         float* __restrict__ logits, unsigned* counter,
+                                                         int k, int renorm, int32_t* __restrict__ ids,
+                                                         float* __restrict__ wts) {
+  extern __shared__ float lsm[];  // last CTA: [min(T, 8)][E] logits
   __shared__ float part[8][TMAX];
-  pdl_launch_dependents();
+  __shared__ int s_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x;
   const float4* wrow = reinterpret_cast<const float4*>(W + static_cast<size_t>(e) * H);
@@ -77,6 +90,17 @@ __global__ void __launch_bounds__(256) route_rows_kernel(const uint16_t* __restr
     for (int w = 0; w < 8; ++w) v += part[w][threadIdx.x];
     logits[static_cast<size_t>(threadIdx.x) * E + e] = v;
   }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();  // this CTA's logits before its arrival
+    s_last = atomicInc(counter, gridDim.x - 1) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();  // every other CTA's logits after their arrivals
+  for (int t = warp; t < T; t += 8)
+    topk_warp(logits + static_cast<size_t>(t) * E, lsm + static_cast<size_t>(warp) * E, E, k, renorm,
+              ids + static_cast<size_t>(t) * k, wts + static_cast<size_t>(t) * k);
 }
 
 // Tiled SIMT GEMM: a 64-token x 64-expert tile per CTA, 256 threads with 4x4
@@ -154,23 +178,32 @@ __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib)
 }
 
 // One warp per token.  The token's E logits are read once into this warp's
-// slice of shared memory (with the running max); then the softmax
-// denominator, then k rounds of "best element ranked after the previous
-// winner" (a selection with no taken set), all from shared memory.
-__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T,
-                                                         int E, int k, int renorm,
-                                                         int32_t* __restrict__ ids,
-                                                         float* __restrict__ wts) {
-  extern __shared__ float lsm[];  // [warps][E]
-  pdl_wait();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + warp;
-  if (t >= T) return;
-  const float* l = logits + static_cast<size_t>(t) * E;
-  float* ls = lsm + static_cast<size_t>(warp) * E;
+// slice of shared memory (with the running max), then the softmax
+// denominator.  Lane l owns the logits e = l (mod 32) and keeps the best of
+// its untaken ones; each of the k rounds takes the warp's best (value
+// descending, id ascending on ties) and only the winning lane marks it taken
+// (a NaN in shared memory, which no comparison ranks first) and rescans its
+// own logits for its next best.
+__device__ __forceinline__ void lane_best(const float* ls, int E, int lane, float& bv, int& bi) {
+  bv = -INFINITY;
+  bi = 0x7fffffff;
+  for (int e = lane; e < E; e += 32) {
+    const float v = ls[e];
+    if (ranks_before(v, e, bv, bi)) {
+      bv = v;
+      bi = e;
+    }
+  }
+}
+
+// Top-k of one token's E logits by one warp; ls is this warp's E floats of
+// shared memory.
+__device__ __forceinline__ void topk_warp(const float* __restrict__ l, float* ls, int E, int k, int renorm,
+                                          int32_t* __restrict__ ids_t, float* __restrict__ wts_t) {
+  const int lane = threadIdx.x & 31;
   float mx = -INFINITY;
   for (int e = lane; e < E; e += 32) {
-    const float v = l[e];
+    const float v = __ldcg(l + e);
     ls[e] = v;
     mx = fmaxf(mx, v);
   }
@@ -179,21 +212,15 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   float z = 0.f;
   for (int e = lane; e < E; e += 32) z += expf(ls[e] - mx);
   z = warp_sum(z);
-  float pv = INFINITY;
-  int pi = -1;
+  float lv;
+  int li;
+  lane_best(ls, E, lane, lv, li);
   float sel_sum = 0.f;
   float my_w = 0.f;
   int my_id = 0;
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    for (int e = lane; e < E; e += 32) {
-      const float v = ls[e];
-      if (ranks_before(pv, pi, v, e) && ranks_before(v, e, bv, bi)) {
-        bv = v;
-        bi = e;
-      }
-    }
+    float bv = lv;
+    int bi = li;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -203,19 +230,34 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
         bi = oi;
       }
     }
-    pv = bv;
-    pi = bi;
     const float p = expf(bv - mx) / z;
     sel_sum += p;
     if (lane == j) {
       my_w = p;
       my_id = bi;
     }
+    if (bi == li && bi < E) {  // this lane's best was taken: find its next
+      ls[bi] = __int_as_float(0x7fffffff);
+      lane_best(ls, E, lane, lv, li);
+    }
   }
   if (lane < k) {
-    ids[static_cast<size_t>(t) * k + lane] = my_id;
-    wts[static_cast<size_t>(t) * k + lane] = renorm ? my_w / sel_sum : my_w;
+    ids_t[lane] = my_id;
+    wts_t[lane] = renorm ? my_w / sel_sum : my_w;
   }
+}
+
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T,
+                                                         int E, int k, int renorm,
+                                                         int32_t* __restrict__ ids,
+                                                         float* __restrict__ wts) {
+  extern __shared__ float lsm[];  // [warps][E]
+  pdl_wait();
+  const int warp = threadIdx.x >> 5;
+  const int t = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (t >= T) return;
+  topk_warp(logits + static_cast<size_t>(t) * E, lsm + static_cast<size_t>(warp) * E, E, k, renorm,
+            ids + static_cast<size_t>(t) * k, wts + static_cast<size_t>(t) * k);
 }
 
 }  // namespace
@@ -225,7 +267,7 @@ extern "C" {
 
 size_t ft_moe_route_workspace(int32_t T, int32_t E) {
   if (T <= 0 || E <= 0) return 0;
-  return (static_cast<size_t>(T) * E * sizeof(float) + 255) & ~static_cast<size_t>(255);
+  return ft::route_logits_bytes(T, E) + 256;  // logits, then the arrival counter
 }
 
 ft_status ft_moe_route(const uint16_t* x, int32_t T, int32_t H, const float* w_router, int32_t E,
@@ -244,12 +286,24 @@ ft_status ft_moe_route(const uint16_t* x, int32_t T, int32_t H, const float* w_r
   cudaStream_t s = ft::as_stream(stream);
   float* logits = static_cast<float*>(ws);
   if (T <= ft::kGemvMaxT) {
+    // logits and top-k in one kernel; the arrival counter follows the logits
+    unsigned* counter = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + ft::route_logits_bytes(T, E));
+    const size_t smem = static_cast<size_t>(T < 8 ? T : 8) * E * sizeof(float);
+    static bool attr = false;
+    if (!attr) {
+      const int mx = 8 * ft::kRouteMaxE * static_cast<int>(sizeof(float));
+      cudaFuncSetAttribute(ft::route_rows_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+      cudaFuncSetAttribute(ft::route_rows_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+      cudaFuncSetAttribute(ft::route_rows_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+      attr = true;
+    }
     if (T <= 1)
-      ft::route_rows_kernel<1><<<E, 256, 0, s>>>(x, T, H, w_router, E, logits);
+      ft::route_rows_kernel<1><<<E, 256, smem, s>>>(x, T, H, w_router, E, logits, counter, k, renorm, topk_ids, topk_w);
     else if (T <= 4)
-      ft::route_rows_kernel<4><<<E, 256, 0, s>>>(x, T, H, w_router, E, logits);
+      ft::route_rows_kernel<4><<<E, 256, smem, s>>>(x, T, H, w_router, E, logits, counter, k, renorm, topk_ids, topk_w);
     else
-      ft::route_rows_kernel<16><<<E, 256, 0, s>>>(x, T, H, w_router, E, logits);
+      ft::route_rows_kernel<16><<<E, 256, smem, s>>>(x, T, H, w_router, E, logits, counter, k, renorm, topk_ids, topk_w);
+    return ft::launch_check("route");
   } else {
     FT_REQUIRE(H % ft::kTK == 0, "route: H %d must be a multiple of 32 for T > 16", H);
     dim3 grid((E + ft::kTN - 1) / ft::kTN, (T + ft::kTM - 1) / ft::kTM);
