@@ -35,9 +35,10 @@ if ROOT not in sys.path:
 
 METRIC = "MoE-layer tokens/s; decode expert-weight HBM GB/s; prefill grouped-GEMM TFLOP/s"
 # DRAM bytes (read + write) of one experts call (gate/up + down kernels) from
-# an ncu capture of the same kernels on this workload's shape; None until
-# captured (see profiles/decode_experts_d35b.md)
-TRAFFIC_PER_CALL = {}
+# an ncu capture of the same kernels on this workload's shape, L2 kept
+# between the kernels (`bench.py --case decode --tokens T` under
+# `ncu --cache-control none`; profiles/decode_experts_d35b_T1.md)
+TRAFFIC_PER_CALL = {1: 13_376_256, 8: 103_728_640}
 UNIT = "MoE-layer tokens/s"
 
 
@@ -458,6 +459,78 @@ def run_reference(args, cfg, T):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------- small cases for ncu --
+def kernel_case(name: str, T: int):
+    """A small standalone workload for kernel profiling: a few calls of one
+    kernel family on a bank that fits in a few GB (no pool, no history).
+      decode:  ft_moe_experts_fwd decode on the d35b or flash shape, fresh
+               random experts each call (nothing reused in L2);
+      prefill: permute + ft_moe_experts_fwd prefill, NVFP4 H 4096 I 2048,
+               16 experts, 512 tokens, top-6."""
+    import torch
+
+    import quantized_expert_ffn_router_gb300 as ft
+    import synth
+    from quantized_expert_ffn_router_gb300 import build as ftbuild
+
+    ftbuild.build()
+    ft.load()
+    dev = "cuda"
+    rng = np.random.default_rng(0)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    if name in ("decode", "decode-flash"):
+        cfg = synth.get_config("d35b" if name == "decode" else "flash")
+        E, k = cfg.E, cfg.k
+        _, stride = synth.block_layout(cfg.fmt, cfg.H, cfg.I, cfg.g)
+        bank = torch.empty((2 * E, stride), dtype=torch.uint8, device=dev)
+        synth.bank_blocks_torch(0, range(2 * E), cfg.fmt, cfg.H, cfg.I, cfg.g, bank, ref_K=cfg.ref_K)
+        ts = synth.tensor_scales(cfg.fmt, cfg.H, cfg.I, cfg.L * E)
+        cb = ft.make_bank(cfg.fmt, cfg.H, cfg.I, cfg.g, bank, None if ts is None else torch.from_numpy(ts).to(dev))
+        w = torch.full((T, k), 0.1, device=dev)
+        x = torch.from_numpy(synth.normal_bf16(1, (T, cfg.H)).view(np.int16)).to(dev)
+        out = torch.empty((T, cfg.H), device=dev)
+        ws = torch.zeros(ft.experts_workspace(ft.FT_DECODE, T, k, cfg.H, cfg.I, E), dtype=torch.uint8, device=dev)
+        # evict the bank generation's dirty lines so DRAM counters see only the calls
+        scratch = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        scratch.zero_()
+        scratch.sum()
+        torch.cuda.synchronize()
+        for c in range(3):
+            ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+            slots = torch.from_numpy(ids + (c % 2) * E).to(dev)
+            ft.experts_fwd(cb, None, 0, E, x, T, k, slots, torch.from_numpy(ids).to(dev), w, out, ws,
+                           dev_status=status)
+    elif name == "prefill":
+        H, I, E, k, Tp = 4096, 2048, 16, 6, 512
+        _, stride = synth.block_layout(synth.gen.FMT_NVFP4, H, I, 16)
+        bank = torch.empty((E, stride), dtype=torch.uint8, device=dev)
+        synth.bank_blocks_torch(0, range(E), synth.gen.FMT_NVFP4, H, I, 16, bank)
+        ts = torch.from_numpy(synth.tensor_scales(synth.gen.FMT_NVFP4, H, I, E)).to(dev)
+        cb = ft.make_bank(synth.gen.FMT_NVFP4, H, I, 16, bank, ts)
+        ids = torch.from_numpy(np.stack([rng.choice(E, k, replace=False) for _ in range(Tp)]).astype(np.int32)).to(dev)
+        x = torch.from_numpy(synth.normal_bf16(1, (Tp, H)).view(np.int16)).to(dev)
+        n = Tp * k
+        perm = torch.empty(n, dtype=torch.int32, device=dev)
+        inv = torch.empty((Tp, k), dtype=torch.int32, device=dev)
+        off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        xp = torch.empty((n, H), dtype=torch.int16, device=dev)
+        xs = torch.empty(n, device=dev)
+        pws = torch.empty(ft.permute_workspace(Tp, k, E), dtype=torch.uint8, device=dev)
+        yp = torch.empty((n, H), dtype=torch.int16, device=dev)
+        ews = torch.empty(ft.experts_workspace(ft.FT_PREFILL, Tp, k, H, I, E), dtype=torch.uint8, device=dev)
+        slot = torch.arange(E, dtype=torch.int32, device=dev)
+        ft.permute(ids, E, x, perm, inv, off, xp, pws, dev_status=status, xp_scale=xs)
+        for _ in range(2):
+            ft.experts_fwd(cb, None, 0, E, xp, Tp, k, slot, None, None, yp, ews, mode=ft.FT_PREFILL,
+                           offsets=off, dev_status=status, x_scale=xs)
+    else:
+        raise SystemExit(f"unknown case {name}")
+    torch.cuda.synchronize()
+    if ft.get_status(status) != 0:
+        raise RuntimeError(f"device status {ft.get_status(status)}")
+    print("ok", flush=True)
+
+
 # ---------------------------------------------------------------------- main --
 def main():
     ap = argparse.ArgumentParser()
@@ -469,7 +542,12 @@ def main():
     ap.add_argument("--phi", type=int, default=65536, help="frac_q16 of the q* split")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--extra-batch", type=int, default=8, help="also time this batch (0: off)")
+    ap.add_argument("--case", choices=["decode", "decode-flash", "prefill"],
+                    help="run a small kernel case for a profiler instead of the benchmark")
     args = ap.parse_args()
+    if args.case:
+        kernel_case(args.case, args.tokens)
+        return
     if args.warmup < 3:
         args.warmup = 3
 
