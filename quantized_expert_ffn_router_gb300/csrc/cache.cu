@@ -4,6 +4,7 @@
 //
 // Sources: "FreeToken 딥다이브" (fiv.co.kr), design patterns 2, 3, 5;
 // "FreeToken: 让消费级电脑跑起 284B MoE" (fengjutian.github.io), secs. 4, 6.
+#include "ft_async.cuh"
 #include "ft_common.cuh"
 
 namespace ft {
@@ -131,6 +132,8 @@ __global__ void __launch_bounds__(kResThreads, 1) resolve_kernel(ResolveArgs a) 
   const int tid = threadIdx.x;
   const int nt = blockDim.x;
   const int base = a.layer * E;
+  pdl_wait();               // ids come from the previous kernel (route)
+  pdl_launch_dependents();  // the next call (fetch) may start its launch now
 
   if (n <= 32) {
     __shared__ int s_done;
@@ -394,6 +397,8 @@ __global__ void __launch_bounds__(kFetchThreads) fetch_kernel(
     uint64_t cstride, uint64_t n16, const int32_t* __restrict__ num_fetch,
     const int32_t* __restrict__ ffid, const int32_t* __restrict__ fslot, int32_t max_list,
     int64_t n_pool, int64_t n_cache, int32_t* dev_status) {
+  pdl_wait();               // the fetch list comes from the previous kernel (resolve)
+  pdl_launch_dependents();  // the experts call may start its launch now
   const int nf = min(*num_fetch, max_list);
   const uint64_t per = static_cast<uint64_t>(kFetchThreads) * kFetchVec;
   const uint64_t nchunks = (n16 + per - 1) / per;
@@ -506,7 +511,18 @@ ft_status ft_moe_resolve_slots(const ft_cache_state* st, int32_t layer, const in
   // small calls usually finish in the one-warp path; 256 threads keep the
   // rest cheap to synchronise.  Larger calls get the whole block.
   const int threads = n <= 32 ? 256 : ft::kResThreads;
-  ft::resolve_kernel<<<1, threads, smem, ft::as_stream(stream)>>>(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = ft::as_stream(stream);
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, ft::resolve_kernel, a);
+  if (e != cudaSuccess) return ft::fail(FT_ERR_CUDA, "resolve_slots: %s", cudaGetErrorString(e));
   return ft::launch_check("resolve_slots");
 }
 
@@ -529,10 +545,21 @@ ft_status ft_moe_fetch(const ft_bank* pool, const ft_bank* cache, const int32_t*
   const uint64_t nchunks = (n16 + per - 1) / per;
   const uint64_t items = nchunks * static_cast<uint64_t>(max_list);
   const int grid = static_cast<int>(std::min<uint64_t>(items, static_cast<uint64_t>(ft::num_sms())));
-  ft::fetch_kernel<<<grid, ft::kFetchThreads, 0, ft::as_stream(stream)>>>(
-      static_cast<const uint8_t*>(pool->base), pool->stride,
-      static_cast<uint8_t*>(const_cast<void*>(cache->base)), cache->stride, n16, num_fetch,
-      fetch_fid, fetch_slot, max_list, pool->n_blocks, cache->n_blocks, dev_status);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(ft::kFetchThreads);
+  cfg.stream = ft::as_stream(stream);
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  const uint8_t* src = static_cast<const uint8_t*>(pool->base);
+  uint8_t* dst = static_cast<uint8_t*>(const_cast<void*>(cache->base));
+  const int64_t npool = pool->n_blocks, ncache = cache->n_blocks;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, ft::fetch_kernel, src, pool->stride, dst, cache->stride, n16, num_fetch,
+                                     fetch_fid, fetch_slot, max_list, npool, ncache, dev_status);
+  if (e != cudaSuccess) return ft::fail(FT_ERR_CUDA, "fetch: %s", cudaGetErrorString(e));
   return ft::launch_check("fetch");
 }
 

@@ -188,6 +188,9 @@ __device__ __forceinline__ const uint8_t* pair_block(const DecArgs& a, int p, bo
 // CPL = 32-element chunks per lane (H <= 1024 * CPL), RPW = rows per warp.
 template <int FMT, int CPL, int RPW>
 __global__ void __launch_bounds__(kThreads, 2) pm_gateup_kernel(DecArgs a, int gshift) {
+  // ids and fetched blocks come from earlier kernels: wait for them, and only
+  // then let the down kernel (which reads weights before its own wait) start
+  pdl_wait();
   pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int p = blockIdx.y;
@@ -442,8 +445,17 @@ __global__ void __launch_bounds__(kThreads, 2) pm_down_kernel(DecArgs a, int gsh
 
 template <int FMT, int CPL, int RPW>
 ft_status launch_gateup(const DecArgs& a, int gshift, cudaStream_t s) {
-  const dim3 grid(a.I / (kWarps * RPW), a.T * a.k);
-  pm_gateup_kernel<FMT, CPL, RPW><<<grid, kThreads, 0, s>>>(a, gshift);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.I / (kWarps * RPW), a.T * a.k);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, pm_gateup_kernel<FMT, CPL, RPW>, a, gshift);
+  if (e != cudaSuccess) return fail(FT_ERR_CUDA, "experts decode gate/up: %s", cudaGetErrorString(e));
   return launch_check("experts decode gate/up");
 }
 

@@ -39,6 +39,8 @@ __global__ void __launch_bounds__(256) route_rows_kernel(const uint16_t* __restr
   extern __shared__ float lsm[];  // last CTA: [min(T, 8)][E] logits
   __shared__ float part[8][TMAX];
   __shared__ int s_last;
+  pdl_wait();               // x may come from the previous kernel in the stream
+  pdl_launch_dependents();  // the next call (resolve) may start its launch now
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x;
   const float4* wrow = reinterpret_cast<const float4*>(W + static_cast<size_t>(e) * H);
@@ -297,12 +299,24 @@ ft_status ft_moe_route(const uint16_t* x, int32_t T, int32_t H, const float* w_r
       cudaFuncSetAttribute(ft::route_rows_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
       attr = true;
     }
+    cudaLaunchConfig_t rc = {};
+    rc.gridDim = dim3(E);
+    rc.blockDim = dim3(256);
+    rc.dynamicSmemBytes = smem;
+    rc.stream = s;
+    cudaLaunchAttribute ra[1];
+    ra[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    ra[0].val.programmaticStreamSerializationAllowed = 1;
+    rc.attrs = ra;
+    rc.numAttrs = 1;
+    cudaError_t le;
     if (T <= 1)
-      ft::route_rows_kernel<1><<<E, 256, smem, s>>>(x, T, H, w_router, E, logits, counter, k, renorm, topk_ids, topk_w);
+      le = cudaLaunchKernelEx(&rc, ft::route_rows_kernel<1>, x, T, H, w_router, E, logits, counter, k, renorm, topk_ids, topk_w);
     else if (T <= 4)
-      ft::route_rows_kernel<4><<<E, 256, smem, s>>>(x, T, H, w_router, E, logits, counter, k, renorm, topk_ids, topk_w);
+      le = cudaLaunchKernelEx(&rc, ft::route_rows_kernel<4>, x, T, H, w_router, E, logits, counter, k, renorm, topk_ids, topk_w);
     else
-      ft::route_rows_kernel<16><<<E, 256, smem, s>>>(x, T, H, w_router, E, logits, counter, k, renorm, topk_ids, topk_w);
+      le = cudaLaunchKernelEx(&rc, ft::route_rows_kernel<16>, x, T, H, w_router, E, logits, counter, k, renorm, topk_ids, topk_w);
+    if (le != cudaSuccess) return ft::fail(FT_ERR_CUDA, "route: %s", cudaGetErrorString(le));
     return ft::launch_check("route");
   } else {
     FT_REQUIRE(H % ft::kTK == 0, "route: H %d must be a multiple of 32 for T > 16", H);
