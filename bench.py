@@ -470,6 +470,88 @@ def run_reference(args, cfg, T):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------ prefill -----
+def prefill_bench(T: int, steps: int, warmup: int, device, log=print, state=None):
+    """One prefill MoE layer of the prefill config (NVFP4, H 4096, I 2048,
+    256 experts, top-6): route -> permute (f16 gather) -> grouped SwiGLU
+    experts on tcgen05 -> combine, for T prompt tokens, the whole layer's
+    experts resident in the cache bank.  Returns the layer time, the grouped
+    GEMM (experts call) time and its TFLOP/s; all inputs resident in HBM."""
+    import torch
+
+    import quantized_expert_ffn_router_gb300 as ft
+    import synth
+
+    cfg = synth.get_config("prefill")
+    H, I, E, k = cfg.H, cfg.I, cfg.E, cfg.k
+    if state is None:
+        _, stride = synth.block_layout(cfg.fmt, H, I, cfg.g)
+        bank = torch.empty((E, stride), dtype=torch.uint8, device=device)
+        for e0 in range(0, E, 32):
+            synth.bank_blocks_torch(cfg.seed, range(e0, min(E, e0 + 32)), cfg.fmt, H, I, cfg.g, bank[e0:e0 + 32])
+        ts = torch.from_numpy(synth.tensor_scales(cfg.fmt, H, I, E)).to(device)
+        W = torch.from_numpy(synth.router_weights(cfg.seed, 0, E, H, cfg.router_std)).to(device)
+        state = dict(bank=bank, ts=ts, W=W, cb=ft.make_bank(cfg.fmt, H, I, cfg.g, bank, ts),
+                     slot=torch.arange(E, dtype=torch.int32, device=device))
+    n = T * k
+    x = torch.from_numpy(synth.normal_bf16(synth.stream_key(cfg.seed, "prefill-bench-x", T), (T, H))
+                         .view(np.int16)).to(device)
+    ids = torch.empty((T, k), dtype=torch.int32, device=device)
+    w = torch.empty((T, k), dtype=torch.float32, device=device)
+    rws = torch.zeros(ft.route_workspace(T, E), dtype=torch.uint8, device=device)
+    perm = torch.empty(n, dtype=torch.int32, device=device)
+    inv = torch.empty((T, k), dtype=torch.int32, device=device)
+    off = torch.empty(E + 1, dtype=torch.int32, device=device)
+    xp = torch.empty((n, H), dtype=torch.int16, device=device)
+    xs = torch.empty(n, dtype=torch.float32, device=device)
+    pws = torch.empty(ft.permute_workspace(T, k, E), dtype=torch.uint8, device=device)
+    yp = torch.empty((n, H), dtype=torch.int16, device=device)
+    ews = torch.empty(ft.experts_workspace(ft.FT_PREFILL, T, k, H, I, E), dtype=torch.uint8, device=device)
+    out = torch.empty((T, H), dtype=torch.int16, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+
+    def layer(timed):
+        if timed:
+            ev[0].record()
+        ft.route(x, state["W"], k, ids, w, rws)
+        ft.permute(ids, E, x, perm, inv, off, xp, pws, dev_status=status, xp_scale=xs)
+        if timed:
+            ev[1].record()
+        ft.experts_fwd(state["cb"], None, 0, E, xp, T, k, state["slot"], None, None, yp, ews,
+                       mode=ft.FT_PREFILL, offsets=off, dev_status=status, x_scale=xs)
+        if timed:
+            ev[2].record()
+        ft.combine(yp, inv, w, out)
+
+    for _ in range(warmup):
+        layer(False)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    gemm_ms = []
+    e0.record()
+    for _ in range(steps):
+        layer(True)
+    e1.record()
+    torch.cuda.synchronize()
+    # the experts interval of each step (events also sit on the stream)
+    layer_ms = e0.elapsed_time(e1) / steps
+    for _ in range(steps):
+        layer(True)
+        torch.cuda.synchronize()
+        gemm_ms.append(ev[1].elapsed_time(ev[2]))
+    if ft.get_status(status) != 0:
+        raise RuntimeError(f"device status {ft.get_status(status)} in prefill")
+    flops = 6.0 * H * I * T * k
+    gm = statistics.median(gemm_ms)
+    res = {"T": T, "layer_ms": layer_ms, "layer_tokens_per_s": T / (layer_ms * 1e-3),
+           "grouped_gemm_ms": gm, "grouped_gemm_tflops": flops / (gm * 1e-3) / 1e12,
+           "weight_bytes": int(state["bank"].numel()), "flops": flops}
+    log(f"prefill T={T}: layer {layer_ms:.3f} ms, grouped GEMM {gm:.3f} ms = {res['grouped_gemm_tflops']:.0f} TFLOP/s")
+    return res, state
+
+
 # ----------------------------------------------------- small cases for ncu --
 def kernel_case(name: str, T: int):
     """A small standalone workload for kernel profiling: a few calls of one
@@ -553,6 +635,7 @@ def main():
     ap.add_argument("--phi", type=int, default=65536, help="frac_q16 of the q* split")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--extra-batch", type=int, default=8, help="also time this batch (0: off)")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill layer measurement")
     ap.add_argument("--case", choices=["decode", "decode-flash", "prefill"],
                     help="run a small kernel case for a profiler instead of the benchmark")
     args = ap.parse_args()
@@ -619,6 +702,16 @@ def main():
             raise RuntimeError(f"device status {st} during the benchmark")
         log(f"T={T}: {value:.1f} {UNIT}, {secs_max / args.steps * 1e3:.3f} ms/step, kernels {kt}")
 
+    prefill = None
+    if not args.no_prefill:
+        del wl
+        torch.cuda.empty_cache()
+        pst = None
+        prefill = {}
+        for Tp in synth.get_config("prefill").tokens:
+            res, pst = prefill_bench(Tp, max(3, min(args.steps, 20)), args.warmup, device, log, pst)
+            prefill[str(Tp)] = res
+        del pst
     if rank != 0:
         return
     peaks, peak_kind = measured_peaks()
@@ -671,6 +764,13 @@ def main():
             "expert_bytes_per_step": r["ebytes"],
             "fetched_experts_per_step": r["nfetch"],
             "host_path_pairs_per_step": r["host_pairs"],
+            "prefill": None if prefill is None else {
+                "workload": "one prefill MoE layer: NVFP4, H 4096, I 2048, 256 experts, top-6, all experts "
+                            "resident; route -> permute -> grouped SwiGLU on tcgen05 -> combine",
+                "tensor_peak_tflops": peaks["bf16_tflops"],
+                "tensor_peak_kind": f"{peak_kind} bf16 dense (f16 runs at the bf16 rate)",
+                "by_tokens": {t: dict(v, tensor_frac=v["grouped_gemm_tflops"] / peaks["bf16_tflops"])
+                              for t, v in prefill.items()}},
             "other_batches": {str(T): {"value": v["value"], "ms_per_step": v["secs"] / args.steps * 1e3,
                                        "per_op_us_per_step": v["kt"], "expert_bytes_per_step": v["ebytes"],
                                        "experts_us_per_call": v["exp_us"],
