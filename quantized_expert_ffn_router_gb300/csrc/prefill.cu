@@ -23,12 +23,16 @@
 //      per row (x_scale undoes it), and for down the f16 h written by the
 //      gate/up epilogue with a fixed 2^-4 prescale.
 //
-// Roles (192 threads): warp 0 lane 0 issues TMA (raw codes with the 128-byte
-// swizzle so converter threads read them conflict-free, E4M3 scales, and the
-// B tiles), warp 1 lane 0 issues the MMAs, warps 2..5 dequantise one weight
-// row per thread into the 128-byte-swizzled K-major A tile and afterwards run
-// the epilogue (tcgen05.ld, 32 TMEM lanes per warp).  Stages are handed over
-// with mbarriers; every wait is bounded.
+// Roles (352 threads).  Warp 0 lane 0 streams the weights by TMA: E2M1 codes
+// in 128-byte-wide boxes (four k-steps, 16 KB per matrix, 128-byte swizzle)
+// and E4M3 scales (eight k-steps per stage).  Warp 2 lane 0 streams the B
+// tiles (tokens), with as many stages as the expert's token count leaves room
+// for, so that neither stream waits on the other.  Warp 1 lane 0 issues the
+// MMAs.  Warps 3..10 (two per SM sub-partition) dequantise half a weight row
+// per thread per k-step into the 128-byte-swizzled K-major A tile, and
+// afterwards run the epilogue (tcgen05.ld; the two warps that share a TMEM
+// lane quarter take alternate 32-token chunks).  Stages are handed over with
+// mbarriers; every wait is bounded.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -39,28 +43,40 @@ namespace ft {
 namespace {
 
 constexpr int kBM = 128;        // weight rows per tile (MMA M)
-constexpr int kBK = 64;         // K per k-step: one 128-byte row of f16
-constexpr int kSuper = 256;     // K per raw stage: 128 code bytes per row
+constexpr int kBK = 64;         // K per k-step: one 128-byte row of f16 (four MMAs of K = 16)
+constexpr int kRawSteps = 2;    // k-steps per code stage: 64 code bytes per row
+constexpr int kScSteps = 4;     // k-steps per scale stage: 16 scale bytes per row
+constexpr int kSuper = kScSteps * kBK;  // K must be a multiple of this
 constexpr int kNMax = 256;      // tokens per pass (MMA N)
 constexpr int kBRows = 64;      // rows per B TMA box
-constexpr int kStages = 2;      // raw, A and B ring depth
-constexpr int kPfThreads = 192;
+constexpr int kBBytes = 64 * 1024;  // the B (tokens) ring: 2 stages of 256 rows .. 8 of 64
+constexpr int kBMaxStages = 8;
+constexpr int kConvWarps = 8;   // two per SM sub-partition
+constexpr int kPfThreads = 128 + 32 * kConvWarps;  // + TMA x2, MMA issuer x2
 constexpr float kHScale = 0.0625f;  // h is stored as f16(h * 2^-4)
 
-constexpr int kATile = kBM * kBK * 2;            // 16 KB per matrix per k-step
-constexpr int kBTile = kNMax * kBK * 2;          // 32 KB
-constexpr int kRawCodes = kBM * (kSuper / 2);    // 16 KB per matrix per raw stage
-constexpr int kRawScales = kBM * (kSuper / 16);  // 2 KB
+constexpr int kATile = kBM * kBK * 2;                 // 16 KB per matrix per k-step
+constexpr int kBBox = kBRows * kBK * 2;               // 8 KB per 64-row B box
+constexpr int kRawTile = kBM * kRawSteps * kBK / 2;   // 8 KB per matrix per code stage
+constexpr int kScTile = kBM * kScSteps * kBK / 16;    // 2 KB per matrix per scale stage
 
+// Shared memory per CTA (216 KB gate/up, 212 KB down).  Weight codes arrive in
+// 64-byte-wide boxes: one TMA row request per 32 B reached about 4.3 TB/s on
+// GB300, 64 B about 6.9 TB/s.  The dequantised A ring is three (gate/up) or
+// six (down) k-steps deep, so that the MMAs of earlier k-steps and the
+// conversion of later ones overlap.
 template <int NMAT>
 struct PfSmem {
+  static constexpr int kAStages = NMAT == 2 ? 3 : 6;
+  static constexpr int kRawStages = NMAT == 2 ? 3 : 6;
+  static constexpr int kScStages = 2;
   static constexpr int a_off = 0;
-  static constexpr int b_off = a_off + kStages * NMAT * kATile;
-  static constexpr int raw_off = b_off + kStages * kBTile;
-  static constexpr int raw_codes = 0;                          // within a raw stage
-  static constexpr int raw_scales = NMAT * kRawCodes;
-  static constexpr int raw_stage = NMAT * (kRawCodes + kRawScales);
-  static constexpr int total = raw_off + kStages * raw_stage;
+  static constexpr int b_off = a_off + kAStages * NMAT * kATile;
+  static constexpr int raw_off = b_off + kBBytes;
+  static constexpr int raw_stage = NMAT * kRawTile;
+  static constexpr int sc_off = raw_off + kRawStages * raw_stage;
+  static constexpr int sc_stage = NMAT * kScTile;
+  static constexpr int total = sc_off + kScStages * sc_stage;
 };
 
 struct PfArgs {
@@ -137,19 +153,29 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
-  uint32_t r[16];
+#define FT_R8(b) "=r"(r[b]), "=r"(r[b + 1]), "=r"(r[b + 2]), "=r"(r[b + 3]), "=r"(r[b + 4]), "=r"(r[b + 5]), "=r"(r[b + 6]), "=r"(r[b + 7])
+
+// 2 x 32 consecutive fp32 TMEM columns of this warp's 32 lanes, both loads in
+// flight before one wait.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float va[32], float vb[32]) {
+  uint32_t r[64];
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-      "%12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, "
+      "%44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, "
+      "[%65];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : FT_R8(0), FT_R8(8), FT_R8(16), FT_R8(24), FT_R8(32), FT_R8(40), FT_R8(48), FT_R8(56)
+      : "r"(ta), "r"(tb)
+      : "memory");
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 32; ++i) {
+    va[i] = __uint_as_float(r[i]);
+    vb[i] = __uint_as_float(r[32 + i]);
+  }
 }
+#undef FT_R8
 
 // E2M1 codes of one 32-bit word (8 codes) times a broadcast f16x2 scale.
 __device__ __forceinline__ uint4 dequant8(uint32_t w, uint32_t s2) {
@@ -167,17 +193,12 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, uint32_t s2) {
   return o;
 }
 
-// Four E4M3 scale bytes -> four broadcast f16x2 values {s_i, s_i}.
-__device__ __forceinline__ void scales4(uint32_t four, uint32_t s2[4]) {
-  uint32_t lo, hi;
-  const unsigned short b01 = static_cast<unsigned short>(four & 0xffffu);
-  const unsigned short b23 = static_cast<unsigned short>(four >> 16);
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(lo) : "h"(b01));
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hi) : "h"(b23));
-  s2[0] = __byte_perm(lo, 0, 0x1010);
-  s2[1] = __byte_perm(lo, 0, 0x3232);
-  s2[2] = __byte_perm(hi, 0, 0x1010);
-  s2[3] = __byte_perm(hi, 0, 0x3232);
+// Two E4M3 scale bytes -> {s0, s0} and {s1, s1} as f16x2.
+__device__ __forceinline__ void scales2(unsigned short two, uint32_t s2[2]) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(two));
+  s2[0] = __byte_perm(h, 0, 0x1010);
+  s2[1] = __byte_perm(h, 0, 0x3232);
 }
 
 // ---------------------------------------------------------------- kernel ---
@@ -190,11 +211,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
                                                            const __grid_constant__ CUtensorMap bmap,
                                                            PfArgs a) {
   using L = PfSmem<NMAT>;
+  constexpr int RS = L::kRawStages, SS = L::kScStages, AS = L::kAStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t raw_full[kStages], raw_empty[kStages];
-  __shared__ __align__(8) uint64_t a_full[kStages], a_empty[kStages];
-  __shared__ __align__(8) uint64_t b_full[kStages], b_empty[kStages];
+  __shared__ __align__(8) uint64_t raw_full[RS], raw_empty[RS];
+  __shared__ __align__(8) uint64_t sc_full[SS], sc_empty[SS];
+  __shared__ __align__(8) uint64_t a_full[AS], a_empty[AS];
+  __shared__ __align__(8) uint64_t b_full[kBMaxStages], b_empty[kBMaxStages];
   __shared__ __align__(8) uint64_t acc_full, acc_empty;
   __shared__ uint32_t s_tmem;
 
@@ -209,21 +232,36 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
     return;
   }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ksteps = a.K / kBK, supers = a.K / kSuper;
+  const int ksteps = a.K / kBK;
+  const int rps = ksteps / kRawSteps;                  // code stages per pass
+  const int sps = ksteps / kScSteps;                   // scale stages per pass
   const int n_pass = (n_e + kNMax - 1) / kNMax;
-  constexpr uint32_t kCols = NMAT == 2 ? 512 : 256;
+  constexpr uint32_t kCols = 512;  // two accumulators of up to 256 columns
+  constexpr int kIss = NMAT == 2 ? 2 : 1;  // MMA issuers that read each k-step's A and B
+  // the B ring: stages sized for this expert's widest pass
+  const int nbox_max = (min(n_e, kNMax) + kBRows - 1) / kBRows;
+  const int b_stage = nbox_max * kBBox;
+  const int NB = min(kBMaxStages, kBBytes / b_stage);
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < RS; ++s) {
       mbar_init(&raw_full[s], 1);
-      mbar_init(&raw_empty[s], 4);
-      mbar_init(&a_full[s], 4);
-      mbar_init(&a_empty[s], 1);
-      mbar_init(&b_full[s], 1);
-      mbar_init(&b_empty[s], 1);
+      mbar_init(&raw_empty[s], kConvWarps);
     }
-    mbar_init(&acc_full, 1);
-    mbar_init(&acc_empty, 4);
+    for (int s = 0; s < SS; ++s) {
+      mbar_init(&sc_full[s], 1);
+      mbar_init(&sc_empty[s], kConvWarps);
+    }
+    for (int s = 0; s < AS; ++s) {
+      mbar_init(&a_full[s], kConvWarps);
+      mbar_init(&a_empty[s], kIss);
+    }
+    for (int s = 0; s < NB; ++s) {
+      mbar_init(&b_full[s], 1);
+      mbar_init(&b_empty[s], kIss);
+    }
+    mbar_init(&acc_full, 2);
+    mbar_init(&acc_empty, kConvWarps);
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -238,41 +276,67 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
   const uint32_t tmem = s_tmem;
 
   if (warp == 0) {
-    // ------------------------------------------------------------- TMA ---
+    // -------------------------------------------------- TMA: weights ---
     if (lane == 0) {
       const CUtensorMap* cm[2] = {&c0map, &c1map};
       const CUtensorMap* sm[2] = {&s0map, &s1map};
       for (int pass = 0; pass < n_pass; ++pass) {
+        for (int kk = 0; kk < ksteps; kk += kRawSteps) {
+          if (kk % kScSteps == 0) {
+            const int su = pass * sps + kk / kScSteps, sst = su % SS;
+            if (su >= SS && !mbar_wait(&sc_empty[sst], ((su / SS) - 1) & 1, a.dev_status)) goto done_w;
+            uint8_t* sc = smem + L::sc_off + sst * L::sc_stage;
+            mbar_arrive_expect_tx(&sc_full[sst], NMAT * kScTile);
+            for (int m = 0; m < NMAT; ++m)
+              tma_load_3d(sc + m * kScTile, sm[m], (kk / kScSteps) * 16, mt * kBM, slot, &sc_full[sst]);
+          }
+          const int v = pass * rps + kk / kRawSteps, rst = v % RS;
+          if (v >= RS && !mbar_wait(&raw_empty[rst], ((v / RS) - 1) & 1, a.dev_status)) goto done_w;
+          uint8_t* raw = smem + L::raw_off + rst * L::raw_stage;
+          mbar_arrive_expect_tx(&raw_full[rst], NMAT * kRawTile);
+          for (int m = 0; m < NMAT; ++m)
+            tma_load_3d(raw + m * kRawTile, cm[m], (kk / kRawSteps) * 64, mt * kBM, slot, &raw_full[rst]);
+        }
+      }
+    done_w:;
+    }
+  } else if (warp == 2) {
+    // --------------------------------------------------- TMA: tokens ---
+    if (lane == 0) {
+      // ring position kept incrementally: NB is not a compile-time constant
+      int bst = 0;
+      uint32_t bph = 0;
+      bool wrapped = false;
+      for (int pass = 0; pass < n_pass; ++pass) {
         const int n_valid = min(kNMax, n_e - pass * kNMax);
         const int nbox = (n_valid + kBRows - 1) / kBRows;
-        for (int s = 0; s < supers; ++s) {
-          const int ru = pass * supers + s, rst = ru % kStages;
-          if (ru >= kStages && !mbar_wait(&raw_empty[rst], ((ru / kStages) - 1) & 1, a.dev_status)) goto done_tma;
-          uint8_t* raw = smem + L::raw_off + rst * L::raw_stage;
-          mbar_arrive_expect_tx(&raw_full[rst], NMAT * (kRawCodes + kRawScales));
-          for (int m = 0; m < NMAT; ++m) {
-            tma_load_3d(raw + L::raw_codes + m * kRawCodes, cm[m], s * (kSuper / 2), mt * kBM, slot, &raw_full[rst]);
-            tma_load_3d(raw + L::raw_scales + m * kRawScales, sm[m], s * (kSuper / 16), mt * kBM, slot,
-                        &raw_full[rst]);
-          }
-          for (int j = 0; j < kSuper / kBK; ++j) {
-            const int kk = s * (kSuper / kBK) + j;
-            const int bu = pass * ksteps + kk, bst = bu % kStages;
-            if (bu >= kStages && !mbar_wait(&b_empty[bst], ((bu / kStages) - 1) & 1, a.dev_status)) goto done_tma;
-            uint8_t* bt = smem + L::b_off + bst * kBTile;
-            mbar_arrive_expect_tx(&b_full[bst], nbox * kBRows * kBK * 2);
-            for (int bx = 0; bx < nbox; ++bx)
-              tma_load_2d(bt + bx * kBRows * kBK * 2, &bmap, kk * kBK, row_lo + pass * kNMax + bx * kBRows,
-                          &b_full[bst]);
+        for (int kk = 0; kk < ksteps; ++kk) {
+          if (wrapped && !mbar_wait(&b_empty[bst], bph ^ 1u, a.dev_status)) goto done_b;
+          uint8_t* bt = smem + L::b_off + bst * b_stage;
+          mbar_arrive_expect_tx(&b_full[bst], nbox * kBBox);
+          for (int bx = 0; bx < nbox; ++bx)
+            tma_load_2d(bt + bx * kBBox, &bmap, kk * kBK, row_lo + pass * kNMax + bx * kBRows, &b_full[bst]);
+          if (++bst == NB) {
+            bst = 0;
+            bph ^= 1u;
+            wrapped = true;
           }
         }
       }
-    done_tma:;
+    done_b:;
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 3 + kConvWarps) {
     // ------------------------------------------------------------- MMA ---
+    // Two issuing threads: one thread issues a tcgen05.mma only every ~94
+    // cycles, whatever N is, so small token counts need two issuers to keep
+    // the tensor pipe busy.  gate/up: issuer i owns matrix i.  down: issuer i
+    // owns the k-steps kk % 2 == i, into accumulator i (summed in the
+    // epilogue).
+    const int iss = warp == 1 ? 0 : 1;
     if (lane == 0) {
       bool ok = true;
+      int ast = 0, bst = 0;
+      uint32_t aph = 0, bph = 0;
       for (int pass = 0; pass < n_pass && ok; ++pass) {
         const int n_valid = min(kNMax, n_e - pass * kNMax);
         const int n_mma = (n_valid + 15) & ~15;
@@ -282,32 +346,44 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
           tc_fence_after();
         }
         for (int kk = 0; kk < ksteps; ++kk) {
-          const int u = pass * ksteps + kk, st = u % kStages;
-          if (!mbar_wait(&a_full[st], (u / kStages) & 1, a.dev_status) ||
-              !mbar_wait(&b_full[st], (u / kStages) & 1, a.dev_status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint8_t* at = smem + L::a_off + st * NMAT * kATile;
-          const uint64_t bdesc = sw128_desc(smem + L::b_off + st * kBTile);
+          if (NMAT == 2 || (kk & 1) == iss) {
+            if (!mbar_wait(&a_full[ast], aph, a.dev_status) || !mbar_wait(&b_full[bst], bph, a.dev_status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint8_t* at = smem + L::a_off + ast * NMAT * kATile + (NMAT == 2 ? iss * kATile : 0);
+            const uint64_t adesc = sw128_desc(at);
+            const uint64_t bdesc = sw128_desc(smem + L::b_off + bst * b_stage);
+            const uint32_t first = NMAT == 2 ? (kk == 0) : (kk == iss);
 #pragma unroll
-          for (int j = 0; j < kBK / 16; ++j) {
-            const uint32_t acc = (kk > 0 || j > 0) ? 1u : 0u;
-#pragma unroll
-            for (int m = 0; m < NMAT; ++m)
-              mma_f16(tmem + m * 256, sw128_desc(at + m * kATile) + 2 * j, bdesc + 2 * j, idesc, acc);
+            for (int j = 0; j < kBK / 16; ++j)
+              mma_f16(tmem + iss * 256, adesc + 2 * j, bdesc + 2 * j, idesc, (first && j == 0) ? 0u : 1u);
+            mma_commit(&a_empty[ast]);
+            mma_commit(&b_empty[bst]);
           }
-          mma_commit(&a_empty[st]);
-          mma_commit(&b_empty[st]);
+          if (++ast == AS) {
+            ast = 0;
+            aph ^= 1u;
+          }
+          if (++bst == NB) {
+            bst = 0;
+            bph ^= 1u;
+          }
         }
         if (ok) mma_commit(&acc_full);
       }
     }
   } else {
     // --------------------------------------- convert, then the epilogue ---
-    const int r = tid - 64;  // weight row within the tile (0..127)
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // Thread (r, hf) converts K half hf of weight row r per k-step.  Lanes
+    // 0-7 and 16-23 take half 0, lanes 8-15 and 24-31 half 1, so the eight
+    // lanes of each shared-memory phase touch eight consecutive rows: with the
+    // 64-byte swizzle of the code tiles and the 128-byte swizzle of the A
+    // tiles their 16-byte chunks fall in distinct banks.  Each stage's codes
+    // and scales are read into registers at once and the stage released.
+    const int wc = warp - 3;
+    const int r = wc * 16 + (lane & 7) + ((lane >> 4) << 3), hf = (lane >> 3) & 1;
     float ts[2] = {1.f, 1.f};
     {
       const int64_t fid = static_cast<int64_t>(a.layer) * a.E + e;
@@ -320,71 +396,104 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
     }
     bool ok = true;
     for (int pass = 0; pass < n_pass && ok; ++pass) {
-      for (int s = 0; s < supers && ok; ++s) {
-        const int ru = pass * supers + s, rst = ru % kStages;
-        if (!mbar_wait(&raw_full[rst], (ru / kStages) & 1, a.dev_status)) {
+      for (int k4 = 0; k4 < ksteps; k4 += kScSteps) {
+        const int su = pass * sps + k4 / kScSteps, sst = su % SS;
+        if (!mbar_wait(&sc_full[sst], (su / SS) & 1, a.dev_status)) {
           ok = false;
           break;
         }
-        const uint8_t* raw = smem + L::raw_off + rst * L::raw_stage;
         uint4 sc[NMAT];
 #pragma unroll
         for (int m = 0; m < NMAT; ++m)
-          sc[m] = *reinterpret_cast<const uint4*>(raw + L::raw_scales + m * kRawScales + r * 16);
-        for (int j = 0; j < kSuper / kBK; ++j) {
-          const int kk = s * (kSuper / kBK) + j;
-          const int u = pass * ksteps + kk, ast = u % kStages;
-          if (u >= kStages && !mbar_wait(&a_empty[ast], ((u / kStages) - 1) & 1, a.dev_status)) {
+          sc[m] = *reinterpret_cast<const uint4*>(smem + L::sc_off + sst * L::sc_stage + m * kScTile + r * 16);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sc_empty[sst]);
+#pragma unroll
+        for (int h2 = 0; h2 < kScSteps / kRawSteps; ++h2) {
+          const int v = pass * rps + k4 / kRawSteps + h2, rst = v % RS;
+          if (!mbar_wait(&raw_full[rst], (v / RS) & 1, a.dev_status)) {
             ok = false;
             break;
           }
-          uint8_t* at = smem + L::a_off + ast * NMAT * kATile;
+          uint4 cw[NMAT][kRawSteps];
+          const uint8_t* raw = smem + L::raw_off + rst * L::raw_stage + r * 64;
 #pragma unroll
-          for (int m = 0; m < NMAT; ++m) {
-            const uint32_t sw = (j == 0) ? sc[m].x : (j == 1) ? sc[m].y : (j == 2) ? sc[m].z : sc[m].w;
-            uint32_t s2[4];
-            scales4(sw, s2);
-            const uint8_t* crow = raw + L::raw_codes + m * kRawCodes + r * 128;
-            // the 32 code bytes of this k-step are logical 16-byte chunks 2j, 2j+1
-            const uint4 c0 = *reinterpret_cast<const uint4*>(crow + (((2 * j) ^ (r & 7)) << 4));
-            const uint4 c1 = *reinterpret_cast<const uint4*>(crow + (((2 * j + 1) ^ (r & 7)) << 4));
-            const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-            uint8_t* arow = at + m * kATile + r * 128;
+          for (int m = 0; m < NMAT; ++m)
 #pragma unroll
-            for (int w = 0; w < 8; ++w)
-              *reinterpret_cast<uint4*>(arow + ((w ^ (r & 7)) << 4)) = dequant8(words[w], s2[w >> 1]);
-          }
-          fence_proxy_async_smem();
+            for (int jj = 0; jj < kRawSteps; ++jj)
+              cw[m][jj] = *reinterpret_cast<const uint4*>(raw + m * kRawTile + (((2 * jj + hf) ^ ((r >> 1) & 3)) << 4));
           __syncwarp();
-          if (lane == 0) mbar_arrive(&a_full[ast]);
+          if (lane == 0) mbar_arrive(&raw_empty[rst]);
+#pragma unroll
+          for (int jj = 0; jj < kRawSteps; ++jj) {
+            const int j4 = h2 * kRawSteps + jj;  // k-step within the scale stage
+            const int u = pass * ksteps + k4 + j4, ast = u % AS;
+            if (u >= AS && !mbar_wait(&a_empty[ast], ((u / AS) - 1) & 1, a.dev_status)) {
+              ok = false;
+              break;
+            }
+            uint8_t* at = smem + L::a_off + ast * NMAT * kATile + r * 128;
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m) {
+              const uint32_t sw = j4 == 0 ? sc[m].x : j4 == 1 ? sc[m].y : j4 == 2 ? sc[m].z : sc[m].w;
+              uint32_t s2[2];
+              scales2(static_cast<unsigned short>(hf ? sw >> 16 : sw & 0xffffu), s2);
+              const uint32_t words[4] = {cw[m][jj].x, cw[m][jj].y, cw[m][jj].z, cw[m][jj].w};
+#pragma unroll
+              for (int w = 0; w < 4; ++w)
+                *reinterpret_cast<uint4*>(at + m * kATile + (((4 * hf + w) ^ (r & 7)) << 4)) =
+                    dequant8(words[w], s2[w >> 1]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&a_full[ast]);
+          }
+          if (!ok) break;
         }
-        __syncwarp();
-        if (ok && lane == 0) mbar_arrive(&raw_empty[rst]);
+        if (!ok) break;
       }
       if (!ok) break;
-      // epilogue of this pass
+      // epilogue of this pass: warp w reads TMEM lanes 32 (w % 4) .. + 31 and
+      // every other 32-token chunk (the two warps of a lane quarter alternate)
       if (!mbar_wait(&acc_full, pass & 1, a.dev_status)) break;
       tc_fence_after();
+      const int q = warp & 3, half = (warp - 3) >> 2;
       const int n_valid = min(kNMax, n_e - pass * kNMax);
       const int row = mt * kBM + q * 32 + lane;  // output column of Hp / Yp
-      for (int c0 = 0; c0 < n_valid; c0 += 16) {
-        float v0[16], v1[16];
-        tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c0, v0);
-        if (NMAT == 2) tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + 256 + c0, v1);
+      const size_t m0 = static_cast<size_t>(row_lo) + pass * kNMax;
+      const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16);
+      for (int c0 = half * 32; c0 < n_valid; c0 += 64) {
+        float v0[32], v1[32];
+        tmem_ld32x2(tq + c0, tq + 256 + c0, v0, v1);
+        const float xs_l =
+            (NMAT == 2 && c0 + lane < n_valid) ? __ldg(a.x_scale + m0 + c0 + lane) : 0.f;
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-          const int col = c0 + jj;
-          if (col >= n_valid) break;
-          const int m = row_lo + pass * kNMax + col;
-          if (NMAT == 2) {
-            const float xs = __ldg(a.x_scale + m);
-            const float gv = v0[jj] * ts[0] * xs, uv = v1[jj] * ts[1] * xs;
-            const float hv = gv / (1.f + expf(-gv)) * uv * kHScale;
-            if (!(fabsf(hv) <= 65504.f)) record_status(a.dev_status, FT_ERR_RANGE);
-            a.out[static_cast<size_t>(m) * a.M + row] = __half_as_ushort(__float2half_rn(hv));
-          } else {
-            a.out[static_cast<size_t>(m) * a.M + row] = f32_to_bf16(v0[jj] * ts[0] * (1.f / kHScale));
+        for (int jj = 0; jj < 32; jj += 2) {
+          float o[2];
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (NMAT == 2) {
+              const float xs = __shfl_sync(0xffffffffu, xs_l, jj + t);
+              const float gv = v0[jj + t] * ts[0] * xs, uv = v1[jj + t] * ts[1] * xs;
+              o[t] = __fdividef(gv, 1.f + __expf(fminf(-gv, 80.f))) * uv * kHScale;
+              if (!(fabsf(o[t]) <= 65504.f) && c0 + jj + t < n_valid) record_status(a.dev_status, FT_ERR_RANGE);
+            } else {
+              o[t] = (v0[jj + t] + v1[jj + t]) * ts[0] * (1.f / kHScale);
+            }
           }
+          // lane pairs swap halves so each lane stores two adjacent outputs of
+          // one token (even lane: token jj, odd lane: token jj + 1)
+          const float mine = (lane & 1) ? o[0] : o[1];
+          const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+          const int col = c0 + jj + (lane & 1);
+          const float lo = (lane & 1) ? other : o[0], hi = (lane & 1) ? o[1] : other;
+          uint32_t pk;
+          if (NMAT == 2)
+            pk = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(lo))) |
+                 (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(hi))) << 16);
+          else
+            pk = static_cast<uint32_t>(f32_to_bf16(lo)) | (static_cast<uint32_t>(f32_to_bf16(hi)) << 16);
+          if (col < n_valid) *reinterpret_cast<uint32_t*>(a.out + (m0 + col) * a.M + (row & ~1)) = pk;
         }
       }
       tc_fence_before();
@@ -421,14 +530,14 @@ EncodeFn encode_fn() {
 // A [n_blocks][rows][inner] byte tensor (codes or scales of one matrix of every
 // block in a bank), box {box_inner, 128 rows, 1 block}.
 bool map_bank(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t blocks,
-              uint64_t block_stride, uint32_t box_inner, bool swizzle) {
+              uint64_t block_stride, uint32_t box_inner, CUtensorMapSwizzle swizzle) {
   const cuuint64_t dims[3] = {inner, rows, blocks};
   const cuuint64_t strides[2] = {inner, block_stride};
   const cuuint32_t box[3] = {box_inner, static_cast<cuuint32_t>(kBM), 1};
   const cuuint32_t es[3] = {1, 1, 1};
   return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     swizzle,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -474,13 +583,13 @@ ft_status experts_prefill(const ft_bank* cache, const ft_bank* pool, int32_t lay
   const int n_rows = static_cast<int>(n_rows64);
   uint16_t* hp = static_cast<uint16_t*>(ws);
   CUtensorMap mg, mu, mgs, mus, mx, md, mds, mh;
-  bool ok = map_bank(&mg, base + L.off[0], H / 2, I, nb, st, kSuper / 2, true) &&
-            map_bank(&mu, base + L.off[1], H / 2, I, nb, st, kSuper / 2, true) &&
-            map_bank(&mgs, base + L.off[3], H / 16, I, nb, st, kSuper / 16, false) &&
-            map_bank(&mus, base + L.off[4], H / 16, I, nb, st, kSuper / 16, false) &&
+  bool ok = map_bank(&mg, base + L.off[0], H / 2, I, nb, st, kRawSteps * kBK / 2, CU_TENSOR_MAP_SWIZZLE_64B) &&
+            map_bank(&mu, base + L.off[1], H / 2, I, nb, st, kRawSteps * kBK / 2, CU_TENSOR_MAP_SWIZZLE_64B) &&
+            map_bank(&mgs, base + L.off[3], H / 16, I, nb, st, 16, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+            map_bank(&mus, base + L.off[4], H / 16, I, nb, st, 16, CU_TENSOR_MAP_SWIZZLE_NONE) &&
             map_acts(&mx, xp, H, n_rows) &&
-            map_bank(&md, base + L.off[2], I / 2, H, nb, st, kSuper / 2, true) &&
-            map_bank(&mds, base + L.off[5], I / 16, H, nb, st, kSuper / 16, false) &&
+            map_bank(&md, base + L.off[2], I / 2, H, nb, st, kRawSteps * kBK / 2, CU_TENSOR_MAP_SWIZZLE_64B) &&
+            map_bank(&mds, base + L.off[5], I / 16, H, nb, st, 16, CU_TENSOR_MAP_SWIZZLE_NONE) &&
             map_acts(&mh, hp, I, n_rows);
   if (!ok) return fail(FT_ERR_INVALID, "experts prefill: tensor map encoding rejected the bank or batch");
   static bool attr = false;
