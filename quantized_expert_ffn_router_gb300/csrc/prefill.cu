@@ -49,7 +49,8 @@ constexpr int kScSteps = 4;     // k-steps per scale stage: 16 scale bytes per r
 constexpr int kSuper = kScSteps * kBK;  // K must be a multiple of this
 constexpr int kNMax = 256;      // tokens per pass (MMA N)
 constexpr int kBRows = 64;      // rows per B TMA box
-constexpr int kBBytes = 64 * 1024;  // the B (tokens) ring: 2 stages of 256 rows .. 8 of 64
+constexpr int kBBytes = 64 * 1024;     // the B (tokens) ring for <= 128 tokens: 4 .. 8 stages
+constexpr int kBBytesBig = 96 * 1024;  // ... for more: 3 stages of 256 rows, 4 of 192
 constexpr int kBMaxStages = 8;
 constexpr int kConvWarps = 8;   // two per SM sub-partition
 constexpr int kPfThreads = 128 + 32 * kConvWarps;  // + TMA x2, MMA issuer x2
@@ -63,20 +64,22 @@ constexpr int kScTile = kBM * kScSteps * kBK / 16;    // 2 KB per matrix per sca
 // Shared memory per CTA (216 KB gate/up, 212 KB down).  Weight codes arrive in
 // 64-byte-wide boxes: one TMA row request per 32 B reached about 4.3 TB/s on
 // GB300, 64 B about 6.9 TB/s.  The dequantised A ring is three (gate/up) or
-// six (down) k-steps deep, so that the MMAs of earlier k-steps and the
-// conversion of later ones overlap.
+// six (down) k-steps deep so that the MMAs of earlier k-steps and the
+// conversion of later ones overlap; for experts with more than 128 tokens a
+// B stage is larger and arrives from L2 with a microsecond of latency, so one
+// A stage (two for down) goes to the B ring instead.  Offsets are computed at
+// run time from the layout chosen.
 template <int NMAT>
 struct PfSmem {
   static constexpr int kAStages = NMAT == 2 ? 3 : 6;
+  static constexpr int kAStagesBig = NMAT == 2 ? 2 : 4;
   static constexpr int kRawStages = NMAT == 2 ? 3 : 6;
   static constexpr int kScStages = 2;
-  static constexpr int a_off = 0;
-  static constexpr int b_off = a_off + kAStages * NMAT * kATile;
-  static constexpr int raw_off = b_off + kBBytes;
   static constexpr int raw_stage = NMAT * kRawTile;
-  static constexpr int sc_off = raw_off + kRawStages * raw_stage;
   static constexpr int sc_stage = NMAT * kScTile;
-  static constexpr int total = sc_off + kScStages * sc_stage;
+  static constexpr int tail = kRawStages * raw_stage + kScStages * sc_stage;  // raw + scale rings
+  static constexpr int total = kAStages * NMAT * kATile + kBBytes + tail;
+  static_assert(kAStagesBig * NMAT * kATile + kBBytesBig + tail <= total, "big-N layout must fit");
 };
 
 struct PfArgs {
@@ -211,12 +214,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
                                                            const __grid_constant__ CUtensorMap bmap,
                                                            PfArgs a) {
   using L = PfSmem<NMAT>;
-  constexpr int RS = L::kRawStages, SS = L::kScStages, AS = L::kAStages;
+  constexpr int RS = L::kRawStages, SS = L::kScStages, AS_MAX = L::kAStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t raw_full[RS], raw_empty[RS];
   __shared__ __align__(8) uint64_t sc_full[SS], sc_empty[SS];
-  __shared__ __align__(8) uint64_t a_full[AS], a_empty[AS];
+  __shared__ __align__(8) uint64_t a_full[AS_MAX], a_empty[AS_MAX];
   __shared__ __align__(8) uint64_t b_full[kBMaxStages], b_empty[kBMaxStages];
   __shared__ __align__(8) uint64_t acc_full, acc_empty;
   __shared__ uint32_t s_tmem;
@@ -238,10 +241,18 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
   const int n_pass = (n_e + kNMax - 1) / kNMax;
   constexpr uint32_t kCols = 512;  // two accumulators of up to 256 columns
   constexpr int kIss = NMAT == 2 ? 2 : 1;  // MMA issuers that read each k-step's A and B
-  // the B ring: stages sized for this expert's widest pass
+  // the B ring: stages sized for this expert's widest pass; more than two
+  // boxes (128 tokens) take the big-N layout
   const int nbox_max = (min(n_e, kNMax) + kBRows - 1) / kBRows;
   const int b_stage = nbox_max * kBBox;
-  const int NB = min(kBMaxStages, kBBytes / b_stage);
+  const bool big = nbox_max > 2;
+  const int AS = big ? L::kAStagesBig : L::kAStages;
+  const int b_bytes = big ? kBBytesBig : kBBytes;
+  const int NB = min(kBMaxStages, b_bytes / b_stage);
+  uint8_t* const a_base = smem;
+  uint8_t* const b_base = a_base + AS * NMAT * kATile;
+  uint8_t* const raw_base = b_base + b_bytes;
+  uint8_t* const sc_base = raw_base + RS * L::raw_stage;
 
   if (tid == 0) {
     for (int s = 0; s < RS; ++s) {
@@ -285,14 +296,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
           if (kk % kScSteps == 0) {
             const int su = pass * sps + kk / kScSteps, sst = su % SS;
             if (su >= SS && !mbar_wait(&sc_empty[sst], ((su / SS) - 1) & 1, a.dev_status)) goto done_w;
-            uint8_t* sc = smem + L::sc_off + sst * L::sc_stage;
+            uint8_t* sc = sc_base + sst * L::sc_stage;
             mbar_arrive_expect_tx(&sc_full[sst], NMAT * kScTile);
             for (int m = 0; m < NMAT; ++m)
               tma_load_3d(sc + m * kScTile, sm[m], (kk / kScSteps) * 16, mt * kBM, slot, &sc_full[sst]);
           }
           const int v = pass * rps + kk / kRawSteps, rst = v % RS;
           if (v >= RS && !mbar_wait(&raw_empty[rst], ((v / RS) - 1) & 1, a.dev_status)) goto done_w;
-          uint8_t* raw = smem + L::raw_off + rst * L::raw_stage;
+          uint8_t* raw = raw_base + rst * L::raw_stage;
           mbar_arrive_expect_tx(&raw_full[rst], NMAT * kRawTile);
           for (int m = 0; m < NMAT; ++m)
             tma_load_3d(raw + m * kRawTile, cm[m], (kk / kRawSteps) * 64, mt * kBM, slot, &raw_full[rst]);
@@ -312,7 +323,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
         const int nbox = (n_valid + kBRows - 1) / kBRows;
         for (int kk = 0; kk < ksteps; ++kk) {
           if (wrapped && !mbar_wait(&b_empty[bst], bph ^ 1u, a.dev_status)) goto done_b;
-          uint8_t* bt = smem + L::b_off + bst * b_stage;
+          uint8_t* bt = b_base + bst * b_stage;
           mbar_arrive_expect_tx(&b_full[bst], nbox * kBBox);
           for (int bx = 0; bx < nbox; ++bx)
             tma_load_2d(bt + bx * kBBox, &bmap, kk * kBK, row_lo + pass * kNMax + bx * kBRows, &b_full[bst]);
@@ -352,9 +363,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
               break;
             }
             tc_fence_after();
-            const uint8_t* at = smem + L::a_off + ast * NMAT * kATile + (NMAT == 2 ? iss * kATile : 0);
+            const uint8_t* at = a_base + ast * NMAT * kATile + (NMAT == 2 ? iss * kATile : 0);
             const uint64_t adesc = sw128_desc(at);
-            const uint64_t bdesc = sw128_desc(smem + L::b_off + bst * b_stage);
+            const uint64_t bdesc = sw128_desc(b_base + bst * b_stage);
             const uint32_t first = NMAT == 2 ? (kk == 0) : (kk == iss);
 #pragma unroll
             for (int j = 0; j < kBK / 16; ++j)
@@ -395,6 +406,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
       }
     }
     bool ok = true;
+    int ast = 0, u = 0;
+    uint32_t aph = 0;
     for (int pass = 0; pass < n_pass && ok; ++pass) {
       for (int k4 = 0; k4 < ksteps; k4 += kScSteps) {
         const int su = pass * sps + k4 / kScSteps, sst = su % SS;
@@ -405,7 +418,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
         uint4 sc[NMAT];
 #pragma unroll
         for (int m = 0; m < NMAT; ++m)
-          sc[m] = *reinterpret_cast<const uint4*>(smem + L::sc_off + sst * L::sc_stage + m * kScTile + r * 16);
+          sc[m] = *reinterpret_cast<const uint4*>(sc_base + sst * L::sc_stage + m * kScTile + r * 16);
         __syncwarp();
         if (lane == 0) mbar_arrive(&sc_empty[sst]);
 #pragma unroll
@@ -416,7 +429,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
             break;
           }
           uint4 cw[NMAT][kRawSteps];
-          const uint8_t* raw = smem + L::raw_off + rst * L::raw_stage + r * 64;
+          const uint8_t* raw = raw_base + rst * L::raw_stage + r * 64;
 #pragma unroll
           for (int m = 0; m < NMAT; ++m)
 #pragma unroll
@@ -427,12 +440,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
 #pragma unroll
           for (int jj = 0; jj < kRawSteps; ++jj) {
             const int j4 = h2 * kRawSteps + jj;  // k-step within the scale stage
-            const int u = pass * ksteps + k4 + j4, ast = u % AS;
-            if (u >= AS && !mbar_wait(&a_empty[ast], ((u / AS) - 1) & 1, a.dev_status)) {
+            if (u >= AS && !mbar_wait(&a_empty[ast], aph ^ 1u, a.dev_status)) {
               ok = false;
               break;
             }
-            uint8_t* at = smem + L::a_off + ast * NMAT * kATile + r * 128;
+            uint8_t* at = a_base + ast * NMAT * kATile + r * 128;
 #pragma unroll
             for (int m = 0; m < NMAT; ++m) {
               const uint32_t sw = j4 == 0 ? sc[m].x : j4 == 1 ? sc[m].y : j4 == 2 ? sc[m].z : sc[m].w;
@@ -447,6 +459,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&a_full[ast]);
+            ++u;
+            if (++ast == AS) {
+              ast = 0;
+              aph ^= 1u;
+            }
           }
           if (!ok) break;
         }
