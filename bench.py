@@ -559,7 +559,7 @@ def kernel_case(name: str, T: int):
       decode:  ft_moe_experts_fwd decode on the d35b or flash shape, fresh
                random experts each call (nothing reused in L2);
       prefill: permute + ft_moe_experts_fwd prefill, NVFP4 H 4096 I 2048,
-               16 experts, 512 tokens, top-6."""
+               16 experts, top-6, 512 tokens (or --tokens >= 16)."""
     import torch
 
     import quantized_expert_ffn_router_gb300 as ft
@@ -594,7 +594,10 @@ def kernel_case(name: str, T: int):
             ft.experts_fwd(cb, None, 0, E, x, T, k, slots, torch.from_numpy(ids).to(dev), w, out, ws,
                            dev_status=status)
     elif name == "prefill":
-        H, I, E, k, Tp = 4096, 2048, 16, 6, 512
+        # --tokens 128: ~48 rows per expert (the 2048-token layer's regime);
+        # 512 (the default): ~192 rows per expert (the 8192-token layer's)
+        H, I, E, k = 4096, 2048, 16, 6
+        Tp = T if T >= 16 else 512
         _, stride = synth.block_layout(synth.gen.FMT_NVFP4, H, I, 16)
         bank = torch.empty((E, stride), dtype=torch.uint8, device=dev)
         synth.bank_blocks_torch(0, range(E), synth.gen.FMT_NVFP4, H, I, 16, bank)
