@@ -23,16 +23,19 @@
 //      per row (x_scale undoes it), and for down the f16 h written by the
 //      gate/up epilogue with a fixed 2^-4 prescale.
 //
-// Roles (352 threads).  Warp 0 lane 0 streams the weights by TMA: E2M1 codes
-// in 128-byte-wide boxes (four k-steps, 16 KB per matrix, 128-byte swizzle)
-// and E4M3 scales (eight k-steps per stage).  Warp 2 lane 0 streams the B
-// tiles (tokens), with as many stages as the expert's token count leaves room
-// for, so that neither stream waits on the other.  Warp 1 lane 0 issues the
-// MMAs.  Warps 3..10 (two per SM sub-partition) dequantise half a weight row
-// per thread per k-step into the 128-byte-swizzled K-major A tile, and
-// afterwards run the epilogue (tcgen05.ld; the two warps that share a TMEM
-// lane quarter take alternate 32-token chunks).  Stages are handed over with
-// mbarriers; every wait is bounded.
+// Roles (640 threads).  Warp 0 lane 0 streams the weights by TMA: E2M1 codes
+// in 64-byte-wide boxes (two k-steps, 64-byte swizzle) and E4M3 scales (four
+// k-steps per stage).  Warp 2 lane 0 streams the B tiles (tokens), with as
+// many stages as the expert's token count leaves room for, so that neither
+// stream waits on the other.  Warps 1 and 3 (lane 0) issue the MMAs: one
+// thread issues a tcgen05.mma only every ~94 cycles whatever N is, so two
+// issuers share the work (gate / up; for down, even / odd k-steps into two
+// accumulators).  Warps 4..19, two groups of eight, dequantise into the
+// 128-byte-swizzled K-major A tiles (gate / up, or even / odd k-steps), half
+// a weight row per thread per k-step, and afterwards run the epilogue
+// (tcgen05.ld; the four warps of a TMEM lane quarter take every fourth
+// 16-token chunk).  Stages are handed over with mbarriers; every wait is
+// bounded.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -52,7 +55,7 @@ constexpr int kBRows = 64;      // rows per B TMA box
 constexpr int kBBytes = 64 * 1024;     // the B (tokens) ring for <= 128 tokens: 4 .. 8 stages
 constexpr int kBBytesBig = 96 * 1024;  // ... for more: 3 stages of 256 rows, 4 of 192
 constexpr int kBMaxStages = 8;
-constexpr int kConvWarps = 8;   // two per SM sub-partition
+constexpr int kConvWarps = 16;  // four per SM sub-partition, in two groups of eight
 constexpr int kPfThreads = 128 + 32 * kConvWarps;  // + TMA x2, MMA issuer x2
 constexpr float kHScale = 0.0625f;  // h is stored as f16(h * 2^-4)
 
@@ -158,24 +161,23 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 
 #define FT_R8(b) "=r"(r[b]), "=r"(r[b + 1]), "=r"(r[b + 2]), "=r"(r[b + 3]), "=r"(r[b + 4]), "=r"(r[b + 5]), "=r"(r[b + 6]), "=r"(r[b + 7])
 
-// 2 x 32 consecutive fp32 TMEM columns of this warp's 32 lanes, both loads in
+// 2 x 16 consecutive fp32 TMEM columns of this warp's 32 lanes, both loads in
 // flight before one wait.
-__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float va[32], float vb[32]) {
-  uint32_t r[64];
+__device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float va[16], float vb[16]) {
+  uint32_t r[32];
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-      "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, "
-      "%44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, "
-      "[%65];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15}, [%32];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%33];\n"
       "tcgen05.wait::ld.sync.aligned;"
-      : FT_R8(0), FT_R8(8), FT_R8(16), FT_R8(24), FT_R8(32), FT_R8(40), FT_R8(48), FT_R8(56)
+      : FT_R8(0), FT_R8(8), FT_R8(16), FT_R8(24)
       : "r"(ta), "r"(tb)
       : "memory");
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
+  for (int i = 0; i < 16; ++i) {
     va[i] = __uint_as_float(r[i]);
-    vb[i] = __uint_as_float(r[32 + i]);
+    vb[i] = __uint_as_float(r[16 + i]);
   }
 }
 #undef FT_R8
@@ -264,7 +266,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
       mbar_init(&sc_empty[s], kConvWarps);
     }
     for (int s = 0; s < AS; ++s) {
-      mbar_init(&a_full[s], kConvWarps);
+      mbar_init(&a_full[s], NMAT == 2 ? kConvWarps : kConvWarps / 2);
       mbar_init(&a_empty[s], kIss);
     }
     for (int s = 0; s < NB; ++s) {
@@ -336,7 +338,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
       }
     done_b:;
     }
-  } else if (warp == 1 || warp == 3 + kConvWarps) {
+  } else if (warp == 1 || warp == 3) {
     // ------------------------------------------------------------- MMA ---
     // Two issuing threads: one thread issues a tcgen05.mma only every ~94
     // cycles, whatever N is, so small token counts need two issuers to keep
@@ -387,24 +389,18 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
     }
   } else {
     // --------------------------------------- convert, then the epilogue ---
-    // Thread (r, hf) converts K half hf of weight row r per k-step.  Lanes
-    // 0-7 and 16-23 take half 0, lanes 8-15 and 24-31 half 1, so the eight
-    // lanes of each shared-memory phase touch eight consecutive rows: with the
-    // 64-byte swizzle of the code tiles and the 128-byte swizzle of the A
-    // tiles their 16-byte chunks fall in distinct banks.  Each stage's codes
-    // and scales are read into registers at once and the stage released.
-    const int wc = warp - 3;
+    // Two groups of eight warps.  gate/up: group g converts matrix g of every
+    // k-step; down: group g converts the k-steps kk % 2 == g (the ones MMA
+    // issuer g consumes).  In a group, thread (r, hf) converts K half hf of
+    // weight row r: lanes 0-7 and 16-23 take half 0, lanes 8-15 and 24-31
+    // half 1, so the eight lanes of each shared-memory phase touch eight
+    // consecutive rows and, with the 64-byte swizzle of the code tiles and
+    // the 128-byte swizzle of the A tiles, distinct banks.  Each stage's codes
+    // and scales go to registers at once and the stage is released.
+    const int cwarp = warp - 4;
+    const int grp = cwarp >> 3, wc = cwarp & 7;
+    const int m = NMAT == 2 ? grp : 0;  // matrix this group converts
     const int r = wc * 16 + (lane & 7) + ((lane >> 4) << 3), hf = (lane >> 3) & 1;
-    float ts[2] = {1.f, 1.f};
-    {
-      const int64_t fid = static_cast<int64_t>(a.layer) * a.E + e;
-      if (NMAT == 2) {
-        ts[0] = __ldg(a.tscale + 3 * fid + 0);
-        ts[1] = __ldg(a.tscale + 3 * fid + 1);
-      } else {
-        ts[0] = __ldg(a.tscale + 3 * fid + 2);
-      }
-    }
     bool ok = true;
     int ast = 0, u = 0;
     uint32_t aph = 0;
@@ -415,10 +411,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
           ok = false;
           break;
         }
-        uint4 sc[NMAT];
-#pragma unroll
-        for (int m = 0; m < NMAT; ++m)
-          sc[m] = *reinterpret_cast<const uint4*>(sc_base + sst * L::sc_stage + m * kScTile + r * 16);
+        const uint4 sc = *reinterpret_cast<const uint4*>(sc_base + sst * L::sc_stage + m * kScTile + r * 16);
         __syncwarp();
         if (lane == 0) mbar_arrive(&sc_empty[sst]);
 #pragma unroll
@@ -428,37 +421,35 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
             ok = false;
             break;
           }
-          uint4 cw[NMAT][kRawSteps];
-          const uint8_t* raw = raw_base + rst * L::raw_stage + r * 64;
+          uint4 cw[kRawSteps];
+          const uint8_t* raw = raw_base + rst * L::raw_stage + m * kRawTile + r * 64;
 #pragma unroll
-          for (int m = 0; m < NMAT; ++m)
-#pragma unroll
-            for (int jj = 0; jj < kRawSteps; ++jj)
-              cw[m][jj] = *reinterpret_cast<const uint4*>(raw + m * kRawTile + (((2 * jj + hf) ^ ((r >> 1) & 3)) << 4));
+          for (int jj = 0; jj < kRawSteps; ++jj)
+            if (NMAT == 2 || jj == grp)
+              cw[jj] = *reinterpret_cast<const uint4*>(raw + (((2 * jj + hf) ^ ((r >> 1) & 3)) << 4));
           __syncwarp();
           if (lane == 0) mbar_arrive(&raw_empty[rst]);
 #pragma unroll
           for (int jj = 0; jj < kRawSteps; ++jj) {
-            const int j4 = h2 * kRawSteps + jj;  // k-step within the scale stage
-            if (u >= AS && !mbar_wait(&a_empty[ast], aph ^ 1u, a.dev_status)) {
-              ok = false;
-              break;
-            }
-            uint8_t* at = a_base + ast * NMAT * kATile + r * 128;
-#pragma unroll
-            for (int m = 0; m < NMAT; ++m) {
-              const uint32_t sw = j4 == 0 ? sc[m].x : j4 == 1 ? sc[m].y : j4 == 2 ? sc[m].z : sc[m].w;
+            // k4 and 2 * h2 are even, so this k-step's parity is jj's
+            if (NMAT == 2 || jj == grp) {
+              const int j4 = h2 * kRawSteps + jj;  // k-step within the scale stage
+              if (u >= AS && !mbar_wait(&a_empty[ast], aph ^ 1u, a.dev_status)) {
+                ok = false;
+                break;
+              }
+              uint8_t* at = a_base + ast * NMAT * kATile + m * kATile + r * 128;
+              const uint32_t sw = j4 == 0 ? sc.x : j4 == 1 ? sc.y : j4 == 2 ? sc.z : sc.w;
               uint32_t s2[2];
               scales2(static_cast<unsigned short>(hf ? sw >> 16 : sw & 0xffffu), s2);
-              const uint32_t words[4] = {cw[m][jj].x, cw[m][jj].y, cw[m][jj].z, cw[m][jj].w};
+              const uint32_t words[4] = {cw[jj].x, cw[jj].y, cw[jj].z, cw[jj].w};
 #pragma unroll
               for (int w = 0; w < 4; ++w)
-                *reinterpret_cast<uint4*>(at + m * kATile + (((4 * hf + w) ^ (r & 7)) << 4)) =
-                    dequant8(words[w], s2[w >> 1]);
+                *reinterpret_cast<uint4*>(at + (((4 * hf + w) ^ (r & 7)) << 4)) = dequant8(words[w], s2[w >> 1]);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&a_full[ast]);
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&a_full[ast]);
             ++u;
             if (++ast == AS) {
               ast = 0;
@@ -470,22 +461,28 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
         if (!ok) break;
       }
       if (!ok) break;
-      // epilogue of this pass: warp w reads TMEM lanes 32 (w % 4) .. + 31 and
-      // every other 32-token chunk (the two warps of a lane quarter alternate)
+      // epilogue of this pass: warp w reads TMEM lanes 32 (w % 4) .. + 31; the
+      // four warps of a lane quarter take every fourth 16-token chunk
       if (!mbar_wait(&acc_full, pass & 1, a.dev_status)) break;
       tc_fence_after();
-      const int q = warp & 3, half = (warp - 3) >> 2;
+      float ts[2];
+      {
+        const int64_t fid = static_cast<int64_t>(a.layer) * a.E + e;
+        ts[0] = __ldg(a.tscale + 3 * fid + (NMAT == 2 ? 0 : 2));
+        ts[1] = NMAT == 2 ? __ldg(a.tscale + 3 * fid + 1) : 0.f;
+      }
+      const int q = warp & 3, part = cwarp >> 2;
       const int n_valid = min(kNMax, n_e - pass * kNMax);
       const int row = mt * kBM + q * 32 + lane;  // output column of Hp / Yp
       const size_t m0 = static_cast<size_t>(row_lo) + pass * kNMax;
       const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16);
-      for (int c0 = half * 32; c0 < n_valid; c0 += 64) {
-        float v0[32], v1[32];
-        tmem_ld32x2(tq + c0, tq + 256 + c0, v0, v1);
+      for (int c0 = part * 16; c0 < n_valid; c0 += 64) {
+        float v0[16], v1[16];
+        tmem_ld16x2(tq + c0, tq + 256 + c0, v0, v1);
         const float xs_l =
-            (NMAT == 2 && c0 + lane < n_valid) ? __ldg(a.x_scale + m0 + c0 + lane) : 0.f;
+            (NMAT == 2 && c0 + (lane & 15) < n_valid) ? __ldg(a.x_scale + m0 + c0 + (lane & 15)) : 0.f;
 #pragma unroll
-        for (int jj = 0; jj < 32; jj += 2) {
+        for (int jj = 0; jj < 16; jj += 2) {
           float o[2];
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
