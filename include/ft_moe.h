@@ -73,7 +73,8 @@ enum {
   FT_ERR_CUDA = 3,
   FT_ERR_TIMEOUT = 4,   /* device: a bounded wait ran out */
   FT_ERR_BAD_ID = 5,    /* device: an expert id outside [0, E) */
-  FT_ERR_RANGE = 6      /* device: an intermediate left the f16 range (|h| > 2^20) */
+  FT_ERR_RANGE = 6,     /* device: an intermediate left the f16 range (|h| > 2^20) */
+  FT_ERR_REJECTED = 7   /* host: a cache rebuild that does not fit; nothing was changed */
 };
 
 /* Expert weight formats. */
@@ -213,6 +214,34 @@ FT_API ft_status ft_moe_fetch(const ft_bank* pool_host, const ft_bank* cache_hos
                        const int32_t* num_fetch, const int32_t* fetch_fid,
                        const int32_t* fetch_slot, int32_t max_list, int32_t* dev_status,
                        void* stream);
+
+/*
+ * ft_moe_cache_rebuild -- rebuild the slot cache at a new size (FreeToken
+ * paper post, sec. 7 item 1: the GPU expert cache is re-partitioned at a
+ * safe point for a new memory budget without reloading the host pool, which
+ * stays the source of truth; deep-dive design pattern 7: everything is
+ * validated before anything is destroyed, and a rebuild that does not fit is
+ * refused).
+ * Checks, on the host and before anything is enqueued: new_state has the
+ * same L and E as old_state; new_cache the same format and shape as
+ * old_cache and room for new_state->S blocks; new_state->S * new_cache->stride
+ * plus 12 bytes per new slot (slot_owner, usage) fits in budget_bytes; and
+ * the new bank and state arrays do not overlap the old ones.  Any failure
+ * returns FT_ERR_REJECTED (FT_ERR_INVALID for a malformed call: NULL
+ * pointers, negative sizes) and changes nothing.
+ * Otherwise, on the stream: the resident experts of the old cache (slots
+ * whose owner is >= 0) are ranked by usage, larger first, the lower slot
+ * first among equals; the first min(residents, new S) move, in that order,
+ * to new slots 0.. (block bytes copied old_cache -> new_cache, slot_owner and
+ * usage carried over, map pointing at the new slots); every other new slot is
+ * empty and every other flat id maps to -1; recency and step are copied.
+ * The old state and bank are only read: the caller switches to the new ones
+ * and frees the old after the stream has passed this call.  An old owner
+ * outside [0, L*E) is skipped and records FT_ERR_BAD_ID.
+ */
+FT_API ft_status ft_moe_cache_rebuild(const ft_cache_state* old_state_host, const ft_bank* old_cache_host,
+                                      const ft_cache_state* new_state_host, const ft_bank* new_cache_host,
+                                      uint64_t budget_bytes, int32_t* dev_status, void* stream);
 
 /*
  * ft_moe_experts_fwd -- quantized SwiGLU experts y = down(silu(gate.x) * up.x)

@@ -87,6 +87,9 @@ def lib():
             L.orc_resolve_many.argtypes = ([c.c_int] * 3 + [c.c_void_p] * 5 + [c.c_int, c.c_void_p,
                                            c.c_int, c.c_int, c.c_int32, c.c_int] + [c.c_void_p] * 4
                                            + [c.c_int])
+            L.orc_cache_rebuild.restype = c.c_int
+            L.orc_cache_rebuild.argtypes = [c.c_int, c.c_int, c.c_int, c.c_void_p, c.c_void_p, c.c_int,
+                                            c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p]
             L.orc_route.restype = None
             L.orc_route.argtypes = [c.c_void_p, c.c_int, c.c_int, c.c_void_p, c.c_int,
                                     c.c_int, c.c_int, c.c_void_p, c.c_void_p, c.c_void_p]
@@ -261,6 +264,21 @@ def resolve_many(st: CacheState, layer: int, ids: np.ndarray, phi: int, max_list
 
 
 # ------------------------------------------------------------------ permute
+def cache_rebuild(st: CacheState, S_new: int):
+    """The slot cache rebuilt at S_new slots (see orc_cache_rebuild): returns
+    (new CacheState, src_of_new [S_new] = old slot moved to each new slot or -1)."""
+    new = CacheState(st.L, st.E, S_new)
+    src = np.full(S_new, -1, np.int32)
+    rc = lib().orc_cache_rebuild(st.L, st.E, st.S, _ptr(_c(st.slot_owner, np.int32)),
+                                 _ptr(_c(st.usage, np.int64)), S_new, _ptr(new.slot_owner), _ptr(new.map),
+                                 _ptr(new.usage), _ptr(src))
+    if rc != 0:
+        raise ValueError("orc_cache_rebuild: an owner is outside [0, L*E)")
+    new.recency[:] = st.recency
+    new.step[:] = st.step
+    return new, src
+
+
 def permute(ids: np.ndarray, E: int):
     ids = _c(ids, np.int32)
     T, k = ids.shape

@@ -405,6 +405,50 @@ int orc_resolve_many(int L, int E, int S, int32_t* slot_owner, int32_t* map, int
   return 0;
 }
 
+// -------------------------------------------------------------- rebuild ----
+// [FT-ZH] sec. 7 item 1 and [FT-KR] design pattern 7: the slot cache is rebuilt
+// at a new size at a safe point, after its new geometry has been checked; the
+// host pool stays the source of truth, so only performance depends on what
+// the rebuilt cache holds.  The pages do not say which experts survive; the
+// reading taken here keeps the most recently used ones, the order the cache
+// already evicts in: every resident slot (owner >= 0) is ranked by usage,
+// larger first, the lower slot first among equal usage; the first
+// min(residents, S_new) of that ranking move, in order, to slots 0.., the
+// other new slots are empty, every other flat id maps to -1, and recency and
+// the step carry over unchanged.  src_of_new[d] is the old slot moved to new
+// slot d, or -1.  Returns -1 on an owner outside [0, L*E), else 0.
+// Parity: pinned by invariants and by brute force on small states.
+int orc_cache_rebuild(int L, int E, int S_old, const int32_t* owner_old, const int64_t* usage_old,
+                      int S_new, int32_t* owner_new, int32_t* map_new, int64_t* usage_new,
+                      int32_t* src_of_new) {
+  const int64_t n_fid = static_cast<int64_t>(L) * E;
+  std::vector<int> resident;
+  for (int s = 0; s < S_old; ++s) {
+    if (owner_old[s] < 0) continue;
+    if (owner_old[s] >= n_fid) return -1;
+    resident.push_back(s);
+  }
+  std::stable_sort(resident.begin(), resident.end(), [&](int a, int b) {
+    if (usage_old[a] != usage_old[b]) return usage_old[a] > usage_old[b];
+    return a < b;
+  });
+  for (int64_t f = 0; f < n_fid; ++f) map_new[f] = -1;
+  for (int d = 0; d < S_new; ++d) {
+    owner_new[d] = -1;
+    usage_new[d] = -1;
+    src_of_new[d] = -1;
+  }
+  const int keep = std::min(static_cast<int>(resident.size()), S_new);
+  for (int d = 0; d < keep; ++d) {
+    const int s = resident[d];
+    owner_new[d] = owner_old[s];
+    usage_new[d] = usage_old[s];
+    map_new[owner_old[s]] = d;
+    src_of_new[d] = s;
+  }
+  return 0;
+}
+
 // -------------------------------------------------------------- permute ----
 // Stable sort of the T*k (token, rank) pairs by expert: expert ascending, then
 // token, then rank.  perm[pos] = pair index t*k+j, inv[t*k+j] = pos,

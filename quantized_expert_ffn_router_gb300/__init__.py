@@ -15,7 +15,8 @@ import os
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libft_moe.so")
 
-FT_OK, FT_ERR_INVALID, FT_ERR_UNSUPPORTED, FT_ERR_CUDA, FT_ERR_TIMEOUT, FT_ERR_BAD_ID, FT_ERR_RANGE = range(7)
+(FT_OK, FT_ERR_INVALID, FT_ERR_UNSUPPORTED, FT_ERR_CUDA, FT_ERR_TIMEOUT, FT_ERR_BAD_ID, FT_ERR_RANGE,
+ FT_ERR_REJECTED) = range(8)
 FT_INT4, FT_NVFP4 = 0, 1
 FT_DECODE, FT_PREFILL = 0, 1
 FT_OUT_F32, FT_OUT_BF16 = 0, 1
@@ -54,6 +55,7 @@ _SIGS = {
     "ft_moe_split_q16": (_I32, [_V, _I32, _I32, _V, _V]),
     "ft_moe_resolve_slots": (_I32, [_V, _I32, _V, _I32, _I32, _I32, _V, _V, _V, _V, _I32, _V, _V]),
     "ft_moe_fetch": (_I32, [_V, _V, _V, _V, _V, _I32, _V, _V]),
+    "ft_moe_cache_rebuild": (_I32, [_V, _V, _V, _V, _U64, _V, _V]),
     "ft_moe_experts_workspace": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
     "ft_moe_experts_fwd": (_I32, [_V, _V, _I32, _I32, _V, _V, _I32, _V, _V, _V, _I32, _I32, _V, _V,
                                   _I32, _V, _SZ, _V, _V]),
@@ -91,6 +93,8 @@ def _ptr(t):
 
 
 def _stream(stream=None):
+    if isinstance(stream, int):  # a raw cudaStream_t handle (0: the legacy default stream)
+        return ctypes.c_void_p(stream)
     import torch
 
     s = stream if stream is not None else torch.cuda.current_stream()
@@ -180,6 +184,18 @@ def fetch(pool: FtBank, cache: FtBank, num_fetch, fetch_fid, fetch_slot, dev_sta
     _check(load().ft_moe_fetch(ctypes.byref(pool), ctypes.byref(cache), _ptr(num_fetch),
                                _ptr(fetch_fid), _ptr(fetch_slot), fetch_fid.numel(),
                                _ptr(dev_status), _stream(stream)))
+
+
+def cache_rebuild(old_state, old_cache: FtBank, new_state, new_cache: FtBank, budget_bytes: int,
+                  dev_status=None, stream=None):
+    """Rebuild the slot cache into new_state / new_cache (see ft_moe_cache_rebuild).
+    The states are DeviceCacheState objects or FtCacheState structs.  Raises
+    FtError with status FT_ERR_REJECTED when the rebuild does not fit."""
+    so = old_state.struct() if hasattr(old_state, "struct") else old_state
+    sn = new_state.struct() if hasattr(new_state, "struct") else new_state
+    _check(load().ft_moe_cache_rebuild(ctypes.byref(so), ctypes.byref(old_cache), ctypes.byref(sn),
+                                       ctypes.byref(new_cache), int(budget_bytes), _ptr(dev_status),
+                                       _stream(stream)))
 
 
 def experts_workspace(mode: int, T: int, k: int, H: int, I: int, E: int) -> int:

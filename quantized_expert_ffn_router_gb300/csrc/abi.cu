@@ -98,6 +98,7 @@ const char* ft_status_string(ft_status s) {
     case FT_ERR_TIMEOUT: return "device wait timed out";
     case FT_ERR_BAD_ID: return "expert id out of range";
     case FT_ERR_RANGE: return "intermediate outside the f16 range";
+    case FT_ERR_REJECTED: return "cache rebuild rejected";
     default: return "unknown status";
   }
 }

@@ -93,6 +93,43 @@ def test_host_validation_without_gpu(ft):
     assert ft.load().ft_status_string(ft.FT_ERR_BAD_ID).decode() == "expert id out of range"
 
 
+def test_cache_rebuild_refusals_without_gpu(ft):
+    """Every refusal is decided on the host, before anything is enqueued."""
+    lib = ft.load()
+    V = ctypes.c_void_p
+    stride = 55296  # tiny int4 block
+    old_bank = ft.FtBank(0, 256, 128, 32, V(1 << 20), stride, 8, None)
+    new_bank = ft.FtBank(0, 256, 128, 32, V(1 << 30), stride, 8, None)
+
+    def state(L, E, S, base):
+        return ft.FtCacheState(L, E, S, V(base), V(base + 0x1000), V(base + 0x2000), V(base + 0x3000),
+                               V(base + 0x4000))
+
+    old = state(2, 16, 8, 1 << 24)
+    big = 1 << 40
+
+    def rebuild(new, nb=new_bank, budget=big, ob=old_bank):
+        return lib.ft_moe_cache_rebuild(ctypes.byref(old), ctypes.byref(ob), ctypes.byref(new), ctypes.byref(nb),
+                                        budget, None, None)
+
+    assert rebuild(state(2, 32, 4, 1 << 28)) == ft.FT_ERR_REJECTED  # another model's E
+    assert rebuild(state(3, 16, 4, 1 << 28)) == ft.FT_ERR_REJECTED  # another L
+    other = ft.FtBank(0, 256, 128, 64, V(1 << 30), 53248, 8, None)
+    assert ft.block_bytes(0, 256, 128, 64)[0] <= 53248
+    assert rebuild(state(2, 16, 4, 1 << 28), nb=other) == ft.FT_ERR_REJECTED  # another group size
+    assert rebuild(state(2, 16, 9, 1 << 28)) == ft.FT_ERR_REJECTED  # 9 slots, 8 blocks in the bank
+    assert rebuild(state(2, 16, 4, 1 << 28), budget=4 * stride) == ft.FT_ERR_REJECTED  # state bytes too
+    assert rebuild(state(2, 16, 4, 1 << 28), nb=old_bank) == ft.FT_ERR_REJECTED  # the old bank itself
+    assert rebuild(state(2, 16, 4, (1 << 24) + 0x2000)) == ft.FT_ERR_REJECTED  # aliases the old arrays
+    assert rebuild(state(2, 16, 4, 1 << 28), budget=4 * stride) == ft.FT_ERR_REJECTED
+    assert "budget" in lib.ft_last_error().decode()
+    # malformed calls are invalid, not refused
+    assert rebuild(state(2, 16, -1, 1 << 28)) == ft.FT_ERR_INVALID
+    assert lib.ft_moe_cache_rebuild(None, ctypes.byref(old_bank), None, ctypes.byref(new_bank), big, None,
+                                    None) == ft.FT_ERR_INVALID
+    assert lib.ft_status_string(ft.FT_ERR_REJECTED).decode() == "cache rebuild rejected"
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     import quantized_expert_ffn_router_gb300 as ftmod
 

@@ -199,3 +199,71 @@ def test_resolve_rejects_bad_ids_untouched():
     with pytest.raises(ValueError):
         oracle.resolve(st, 0, np.array([[0, 1]], np.int32), 65537)
     assert np.array_equal(st.usage, before.usage) and int(st.step[0]) == 0
+
+
+# ------------------------------------------------------------ cache rebuild
+def _random_state(rng, L, E, S, steps, phi=65536):
+    st = oracle.CacheState(L, E, S)
+    for _ in range(steps):
+        layer = int(rng.integers(0, L))
+        T, k = int(rng.integers(1, 4)), int(rng.integers(1, min(E, 4) + 1))
+        ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+        oracle.resolve(st, layer, ids, phi)
+    return st
+
+
+@pytest.mark.parametrize("S_old,S_new", [(0, 4), (6, 0), (6, 3), (6, 6), (6, 11), (12, 5), (30, 17)])
+def test_cache_rebuild_keeps_most_recently_used(S_old, S_new):
+    """Properties that hold whatever the order of the work: the kept count, no
+    dropped resident used later than a kept one, map = inverse of owner,
+    usage carried with its expert, recency and step unchanged."""
+    rng = np.random.default_rng(S_old * 31 + S_new)
+    for trial in range(20):
+        st = _random_state(rng, 3, 12, S_old, int(rng.integers(0, 40)))
+        before = st.copy()
+        new, src = oracle.cache_rebuild(st, S_new)
+        for n in ("slot_owner", "map", "usage", "recency", "step"):  # the old state is only read
+            assert np.array_equal(getattr(st, n), getattr(before, n))
+        resident = [s for s in range(S_old) if st.slot_owner[s] >= 0]
+        kept = [d for d in range(S_new) if new.slot_owner[d] >= 0]
+        assert len(kept) == min(len(resident), S_new)
+        assert kept == list(range(len(kept)))  # packed into the first slots
+        moved = {int(src[d]) for d in kept}
+        assert moved <= set(resident) and len(moved) == len(kept)
+        for d in kept:
+            s = int(src[d])
+            assert new.slot_owner[d] == st.slot_owner[s] and new.usage[d] == st.usage[s]
+        dropped = [s for s in resident if s not in moved]
+        if kept and dropped:
+            assert min(new.usage[d] for d in kept) >= max(st.usage[s] for s in dropped)
+        assert all(new.usage[d] >= new.usage[d + 1] for d in range(len(kept) - 1))
+        inv = np.full(st.L * st.E, -1, np.int32)
+        for d in kept:
+            inv[new.slot_owner[d]] = d
+        assert np.array_equal(new.map, inv)
+        assert all(new.usage[d] == -1 and src[d] == -1 for d in range(len(kept), S_new))
+        assert np.array_equal(new.recency, st.recency) and new.step[0] == st.step[0]
+
+
+def test_cache_rebuild_then_resolve_still_covers_every_pair_once():
+    """After a rebuild to any size, resolve keeps its exactly-once rule: every
+    (token, rank) pair lands on the slot of its expert or on -1, never on a
+    slot holding another expert."""
+    rng = np.random.default_rng(5)
+    st = _random_state(rng, 2, 16, 10, 60)
+    for S_new in (0, 3, 10, 20):
+        new, _ = oracle.cache_rebuild(st, S_new)
+        for _ in range(15):
+            layer = int(rng.integers(0, 2))
+            ids = np.stack([rng.choice(16, 4, replace=False) for _ in range(3)]).astype(np.int32)
+            sl, nf, ff, fs = oracle.resolve(new, layer, ids, int(rng.integers(0, 65537)))
+            for (t, j), s in np.ndenumerate(sl):
+                assert s == -1 or new.slot_owner[s] == layer * 16 + ids[t, j]
+
+
+def test_cache_rebuild_rejects_bad_owner():
+    st = oracle.CacheState(1, 4, 3)
+    st.slot_owner[1] = 9  # outside L*E
+    st.usage[1] = 0
+    with pytest.raises(ValueError):
+        oracle.cache_rebuild(st, 2)
