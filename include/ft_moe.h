@@ -83,7 +83,7 @@ enum {
   FT_NVFP4 = 1   /* E2M1 code * E4M3 scale per 16 K elements * fp32 per-tensor scale */
 };
 
-enum { FT_DECODE = 0, FT_PREFILL = 1 };
+enum { FT_DECODE = 0, FT_PREFILL = 1, FT_DECODE_HOST = 2 };
 enum { FT_OUT_F32 = 0, FT_OUT_BF16 = 1 };
 enum { FT_XP_BF16 = 0, FT_XP_F16 = 1 };  /* permuted-batch formats of ft_moe_permute */
 
@@ -254,6 +254,14 @@ FT_API ft_status ft_moe_cache_rebuild(const ft_cache_state* old_state_host, cons
  *   h is kept in fp32.  Two pairs of one expert each read its rows (the
  *   repeat is served from L2).  Limits:
  *   T*k <= 256, T <= 16.  offsets unused (NULL).
+ * FT_DECODE_HOST: as FT_DECODE but only the pairs with slot -1, read from
+ *   pool (required); pairs with slot >= 0 are skipped.  With FT_DECODE on the
+ *   cache alone (pool NULL) it splits one layer call into two disjoint
+ *   partial sums that can run at the same time on two streams, the host path
+ *   next to the fetch and the cache GEMV (deep-dive pattern 3: host work
+ *   submitted first, the copy meanwhile, partial sums merged at the end;
+ *   FreeToken paper post, sec. 6: the two branches add exactly);
+ *   ft_moe_merge_partials adds them.
  * FT_PREFILL: x is the permuted batch Xp [T*k, H] in f16 as ft_moe_permute
  *   writes it with FT_XP_F16, x_scale [T*k] its per-row factors; offsets
  *   [E+1] its expert segments; slot_ids is a per-expert table [E] (the block
@@ -313,6 +321,15 @@ FT_API ft_status ft_moe_permute(const int32_t* topk_ids, int32_t T, int32_t k, i
                          const uint16_t* x, int32_t H, int32_t* perm, int32_t* inv,
                          int32_t* offsets, uint16_t* xp, int32_t xp_format, float* xp_scale,
                          void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * ft_moe_merge_partials -- out[i] = a[i] + b[i] for i < n (fp32 inputs;
+ * out fp32 or bf16 by out_dtype): the final merge of a decode layer call
+ * split into its cache and host-path partial sums (FT_DECODE on the cache,
+ * FT_DECODE_HOST on the pool).  out may alias a or b.
+ */
+FT_API ft_status ft_moe_merge_partials(const float* a, const float* b, int64_t n, void* out,
+                                       int32_t out_dtype, void* stream);
 
 /*
  * ft_moe_combine -- out[t] = sum_j topk_w[t,j] * yp[inv[t,j]] in j order,

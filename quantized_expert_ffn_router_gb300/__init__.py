@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(PKG, "libft_moe.so")
 (FT_OK, FT_ERR_INVALID, FT_ERR_UNSUPPORTED, FT_ERR_CUDA, FT_ERR_TIMEOUT, FT_ERR_BAD_ID, FT_ERR_RANGE,
  FT_ERR_REJECTED) = range(8)
 FT_INT4, FT_NVFP4 = 0, 1
-FT_DECODE, FT_PREFILL = 0, 1
+FT_DECODE, FT_PREFILL, FT_DECODE_HOST = 0, 1, 2
 FT_OUT_F32, FT_OUT_BF16 = 0, 1
 FT_XP_BF16, FT_XP_F16 = 0, 1
 
@@ -65,6 +65,7 @@ _SIGS = {
     "ft_moe_permute": (_I32, [_V, _I32, _I32, _I32, _V, _I32, _V, _V, _V, _V, _I32, _V, _V, _SZ, _V,
                               _V]),
     "ft_moe_combine": (_I32, [_V, _V, _V, _I32, _I32, _I32, _V, _V, _V]),
+    "ft_moe_merge_partials": (_I32, [_V, _V, _I64, _V, _I32, _V]),
 }
 
 
@@ -254,3 +255,9 @@ def get_status(dev_status) -> int:
     v = ctypes.c_int32(0)
     _check(load().ft_moe_get_status(_ptr(dev_status), ctypes.byref(v)))
     return int(v.value)
+
+
+def merge_partials(a, b, out, stream=None):
+    """out = a + b (fp32 partial sums; out fp32 or bf16)."""
+    out_dtype = FT_OUT_BF16 if out.dtype.itemsize == 2 else FT_OUT_F32
+    _check(load().ft_moe_merge_partials(_ptr(a), _ptr(b), a.numel(), _ptr(out), out_dtype, _stream(stream)))

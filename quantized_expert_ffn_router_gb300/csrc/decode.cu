@@ -363,7 +363,8 @@ ft_status ft_moe_experts_fwd(const ft_bank* cache, const ft_bank* pool, int32_t 
     return ft::experts_prefill(cache, pool, layer, E, x, x_scale, T, k, slot_ids, offsets,
                                static_cast<uint16_t*>(out), ws, ws_bytes, dev_status, s);
   }
-  FT_REQUIRE(mode == FT_DECODE, "experts: unknown mode %d", mode);
+  FT_REQUIRE(mode == FT_DECODE || mode == FT_DECODE_HOST, "experts: unknown mode %d", mode);
+  FT_REQUIRE(mode != FT_DECODE_HOST || pool != nullptr, "experts: FT_DECODE_HOST needs the pool");
   FT_REQUIRE(out_dtype == FT_OUT_F32 || out_dtype == FT_OUT_BF16, "experts: bad out_dtype");
   if (T == 0) return FT_OK;
   const int64_t n = static_cast<int64_t>(T) * k;
@@ -404,6 +405,7 @@ ft_status ft_moe_experts_fwd(const ft_bank* cache, const ft_bank* pool, int32_t 
   a.h = static_cast<float*>(ws);
   a.out = out;
   a.out_bf16 = (out_dtype == FT_OUT_BF16);
+  a.host_only = (mode == FT_DECODE_HOST);
   a.dev_status = dev_status;
   st = ft::decode_streaming(a, s);
   if (st != FT_ERR_UNSUPPORTED) return st;

@@ -173,6 +173,7 @@ __device__ __forceinline__ const uint8_t* pair_block(const DecArgs& a, int p, bo
     return nullptr;
   }
   if (s >= 0) {
+    if (a.host_only) return nullptr;  // a cache pair: the FT_DECODE call on the cache computes it
     if (s < a.cblocks) return a.cache + static_cast<uint64_t>(s) * a.cstride;
     if (report) record_status(a.dev_status, FT_ERR_BAD_ID);
     return nullptr;

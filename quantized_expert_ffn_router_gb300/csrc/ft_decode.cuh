@@ -27,6 +27,7 @@ struct DecArgs {
   float* h;             // [T*k, I] fp32
   void* out;
   int out_bf16;
+  int host_only;        // 1: only the pairs with slot -1, from the pool (FT_DECODE_HOST)
   int32_t* dev_status;
 };
 
@@ -102,7 +103,9 @@ __device__ __forceinline__ bool groups_sorted(const DecArgs& a, Groups& g) {
         if (e < 0 || e >= a.E) {
           if (blockIdx.x == 0) record_status(a.dev_status, FT_ERR_BAD_ID);
         } else if (s >= 0) {
-          if (s < a.cblocks) {
+          if (a.host_only) {
+            // a cache pair: computed by the FT_DECODE call on the cache
+          } else if (s < a.cblocks) {
             blk = a.cache + static_cast<uint64_t>(s) * a.cstride;
             cached = 1;
           } else if (blockIdx.x == 0) {

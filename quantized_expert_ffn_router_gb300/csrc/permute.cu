@@ -200,6 +200,19 @@ int sms() {
   return n > 0 ? n : 148;
 }
 
+// out = a + b elementwise, written as fp32 or bf16: the merge of two fp32
+// partial sums over disjoint pair sets (the cache pairs and the host-path
+// pairs of one decode layer call).
+__global__ void merge_kernel(const float* a, const float* b, int64_t n, void* out,
+                             bool bf16) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float v = a[i] + b[i];
+    if (bf16) static_cast<uint16_t*>(out)[i] = f32_to_bf16(v);
+    else static_cast<float*>(out)[i] = v;
+  }
+}
+
 }  // namespace
 }  // namespace ft
 
@@ -276,6 +289,18 @@ ft_status ft_moe_combine(const uint16_t* yp, const int32_t* inv, const float* to
   ft::combine_kernel<<<grid, 256, 0, ft::as_stream(stream)>>>(yp, inv, topk_w, T, k, H,
                                                               host_partial, out);
   return ft::launch_check("combine");
+}
+
+ft_status ft_moe_merge_partials(const float* a, const float* b, int64_t n, void* out, int32_t out_dtype,
+                                void* stream) {
+  FT_REQUIRE(n >= 0, "merge: n < 0");
+  FT_REQUIRE(out_dtype == FT_OUT_F32 || out_dtype == FT_OUT_BF16, "merge: bad out_dtype");
+  if (n == 0) return FT_OK;
+  FT_REQUIRE(a && b && out, "merge: NULL pointer");
+  const int64_t blocks = std::min<int64_t>((n + 255) / 256, 65535ll * 16);
+  ft::merge_kernel<<<static_cast<unsigned>(blocks), 256, 0, ft::as_stream(stream)>>>(a, b, n, out,
+                                                                                     out_dtype == FT_OUT_BF16);
+  return ft::launch_check("merge_partials");
 }
 
 }  // extern "C"

@@ -1,0 +1,180 @@
+"""Decode layer pipelines and the calibration of the q* split, over the C ABI.
+
+Stream orchestration only: every step is a call into libft_moe.so.
+
+* DecodeLayer runs one decode layer call:
+    serial      route -> resolve -> fetch -> experts (cache and host path in
+                one call, combine fused)
+    overlapped  route -> resolve -> fork:
+                  host stream  experts FT_DECODE_HOST (the -1 pairs, read in
+                               place from the pinned pool)
+                  main stream  fetch -> experts FT_DECODE on the cache
+                -> join -> merge_partials
+  The overlapped form follows the pages' decode step ("FreeToken 딥다이브",
+  design pattern 3: the host work is submitted first, the copy of the
+  missing experts runs meanwhile, then the GPU experts, and the two partial
+  sums are added; "FreeToken: 让消费级电脑跑起 284B MoE", sec. 6: the merge is
+  exact).  Both forms capture into one CUDA graph (the fork and join are
+  events).
+
+* frac_q16_from_bandwidths and calibrate_frac_q16: the split fraction
+  phi = B_P / B_H in Q16 (deep-dive pattern 2; paper post sec. 6, q* = m *
+  B_P / B_H), where B_P is the bandwidth of copying expert blocks from the
+  pool into the cache and B_H that of computing experts in place on the pool.
+  The deep-dive notes that the profile prefers the two measured while both
+  run at once (they share host memory), and calibrate_frac_q16 does so.
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+from . import (FT_DECODE, FT_DECODE_HOST, DeviceCacheState, FtBank, experts_fwd, experts_workspace, fetch,
+               merge_partials, resolve_slots, route, route_workspace)
+
+
+def frac_q16_from_bandwidths(b_p: float, b_h: float) -> int:
+    """phi = B_P / B_H as a Q16 integer in [1, 65536].  B_P >= B_H means every
+    miss is worth fetching (65536); phi is never 0, which the split reads as
+    "no cap"."""
+    if not (b_p > 0 and b_h > 0):
+        raise ValueError("bandwidths must be positive")
+    return int(min(65536, max(1, round(65536.0 * b_p / b_h))))
+
+
+class DecodeLayer:
+    """Buffers and streams for decode layer calls of T tokens (allocated once,
+    so that calls can be captured in a CUDA graph)."""
+
+    def __init__(self, state: DeviceCacheState, cache: FtBank, pool: FtBank | None, E: int, k: int, T: int,
+                 device="cuda"):
+        import torch
+
+        self.state, self.cache, self.pool, self.E, self.k, self.T = state, cache, pool, E, k, T
+        H, I = cache.H, cache.I
+        n = T * k
+        ml = max(min(n, state.S), 1)
+        i32 = dict(dtype=torch.int32, device=device)
+        self.ids = torch.empty((T, k), **i32)
+        self.w = torch.empty((T, k), dtype=torch.float32, device=device)
+        self.slot_ids = torch.empty((T, k), **i32)
+        self.num_fetch = torch.zeros(1, **i32)
+        self.fetch_fid = torch.empty(ml, **i32)
+        self.fetch_slot = torch.empty(ml, **i32)
+        self.route_ws = torch.zeros(route_workspace(T, E), dtype=torch.uint8, device=device)
+        wsb = experts_workspace(FT_DECODE, T, k, H, I, E)
+        self.ws = torch.zeros(wsb, dtype=torch.uint8, device=device)
+        self.ws_host = torch.zeros(wsb, dtype=torch.uint8, device=device)
+        self.part_cache = torch.empty((T, H), dtype=torch.float32, device=device)
+        self.part_host = torch.empty((T, H), dtype=torch.float32, device=device)
+        self.status = torch.zeros(1, **i32)
+        self.host_stream = torch.cuda.Stream(device=device)
+        self.ev_fork = torch.cuda.Event()
+        self.ev_join = torch.cuda.Event()
+
+    def __call__(self, layer: int, x, w_router, frac_q16: int, out, overlapped: bool = True):
+        """x [T,H] bf16, w_router [E,H] fp32 -> out [T,H] (fp32 or bf16), on the
+        current stream (plus the host stream when overlapped)."""
+        import torch
+
+        main = torch.cuda.current_stream()
+        route(x, w_router, self.k, self.ids, self.w, self.route_ws, stream=main)
+        resolve_slots(self.state, layer, self.ids, frac_q16, self.slot_ids, self.num_fetch, self.fetch_fid,
+                      self.fetch_slot, self.status, stream=main)
+        if not overlapped or self.pool is None:
+            if self.pool is not None:
+                fetch(self.pool, self.cache, self.num_fetch, self.fetch_fid, self.fetch_slot, self.status,
+                      stream=main)
+            experts_fwd(self.cache, self.pool, layer, self.E, x, self.T, self.k, self.slot_ids, self.ids, self.w,
+                        out, self.ws, dev_status=self.status, stream=main)
+            return out
+        self.ev_fork.record(main)
+        self.host_stream.wait_event(self.ev_fork)
+        experts_fwd(self.cache, self.pool, layer, self.E, x, self.T, self.k, self.slot_ids, self.ids, self.w,
+                    self.part_host, self.ws_host, mode=FT_DECODE_HOST, dev_status=self.status,
+                    stream=self.host_stream)
+        self.ev_join.record(self.host_stream)
+        fetch(self.pool, self.cache, self.num_fetch, self.fetch_fid, self.fetch_slot, self.status, stream=main)
+        experts_fwd(self.cache, None, layer, self.E, x, self.T, self.k, self.slot_ids, self.ids, self.w,
+                    self.part_cache, self.ws, dev_status=self.status, stream=main)
+        main.wait_event(self.ev_join)
+        merge_partials(self.part_cache, self.part_host, out, stream=main)
+        return out
+
+
+def calibrate_frac_q16(pool: FtBank, cache: FtBank, E: int, k: int, n_fetch: int, reps: int = 10,
+                       device="cuda") -> dict:
+    """Measure B_P (ft_moe_fetch of n_fetch blocks pool -> cache slots) and
+    B_H (FT_DECODE_HOST experts over k pool experts of one token), each alone
+    and both at once on two streams, and derive frac_q16 from the pair
+    measured at once.  Repetition i draws n_fetch + k distinct experts of
+    layer i mod (pool blocks / E), so that repetitions read different blocks.
+    Needs E >= n_fetch + k and n_fetch cache slots."""
+    import torch
+
+    from . import block_bytes
+
+    nbytes = block_bytes(cache.fmt, cache.H, cache.I, cache.group)[0]
+    n_layers = int(pool.n_blocks) // E
+    if n_layers < 1 or E < n_fetch + k or int(cache.n_blocks) < n_fetch:
+        raise ValueError("calibrate: pool or cache too small for the requested sizes")
+    gen = torch.Generator().manual_seed(0)
+    i32 = dict(dtype=torch.int32, device=device)
+    draws = []
+    for i in range(reps):
+        layer = i % n_layers
+        perm = torch.randperm(E, generator=gen)
+        draws.append((layer, (perm[:n_fetch] + layer * E).to(**i32), perm[n_fetch:n_fetch + k].view(1, k).to(**i32)))
+    fs = torch.arange(n_fetch, **i32)
+    nf = torch.tensor([n_fetch], **i32)
+    slots = torch.full((1, k), -1, **i32)
+    w = torch.full((1, k), 1.0 / k, dtype=torch.float32, device=device)
+    x = torch.randn((1, cache.H), generator=gen).to(torch.bfloat16).view(torch.int16).to(device)
+    out = torch.empty((1, cache.H), dtype=torch.float32, device=device)
+    ws = torch.zeros(experts_workspace(FT_DECODE, 1, k, cache.H, cache.I, E), dtype=torch.uint8, device=device)
+    status = torch.zeros(1, **i32)
+    s_p, s_h = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+
+    def run_fetch(i, st):
+        fetch(pool, cache, nf, draws[i][1], fs, status, stream=st)
+
+    def run_host(i, st):
+        experts_fwd(cache, pool, draws[i][0], E, x, 1, k, slots, draws[i][2], w, out, ws, mode=FT_DECODE_HOST,
+                    dev_status=status, stream=st)
+
+    def timed(st, fn, i):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        fn(i, st)
+        e1.record(st)
+        return e0, e1
+
+    torch.cuda.synchronize()
+    run_fetch(0, s_p)  # warm-up: loads the kernels
+    run_host(0, s_h)
+    torch.cuda.synchronize()
+    us = {"alone_fetch": [], "alone_host": [], "both_fetch": [], "both_host": []}
+    for i in range(reps):
+        j = (i + reps // 2) % reps
+        ev = {"alone_fetch": timed(s_p, run_fetch, i)}
+        torch.cuda.synchronize()
+        ev["alone_host"] = timed(s_h, run_host, j)
+        torch.cuda.synchronize()
+        ev["both_fetch"] = timed(s_p, run_fetch, j)
+        ev["both_host"] = timed(s_h, run_host, i)
+        torch.cuda.synchronize()
+        for key, (e0, e1) in ev.items():
+            us[key].append(e0.elapsed_time(e1) * 1e3)
+    med = {key: sorted(v)[len(v) // 2] for key, v in us.items()}
+    gbs = lambda n, t_us: n / (t_us * 1e-6) / 1e9
+    res = {
+        "B_P_alone_GBs": gbs(n_fetch * nbytes, med["alone_fetch"]),
+        "B_H_alone_GBs": gbs(k * nbytes, med["alone_host"]),
+        "B_P_GBs": gbs(n_fetch * nbytes, med["both_fetch"]),
+        "B_H_GBs": gbs(k * nbytes, med["both_host"]),
+        "n_fetch": n_fetch, "k": k, "block_bytes": nbytes, "reps": reps,
+    }
+    res["frac_q16"] = frac_q16_from_bandwidths(res["B_P_GBs"], res["B_H_GBs"])
+    res["frac_q16_alone"] = frac_q16_from_bandwidths(res["B_P_alone_GBs"], res["B_H_alone_GBs"])
+    res["status"] = int(status.item())
+    return res
