@@ -320,6 +320,9 @@ __global__ void __launch_bounds__(kThreads, 2) pm_down_kernel(DecArgs a, int gsh
   const int t = blockIdx.y, k = a.k;
   const int H = a.H, I = a.I, IC = I / 32;
   const int row = (blockIdx.x * kWarps + warp) * RPWd + lane / LPR;
+  // the next call (the next layer's router) may start its launch now: it
+  // waits for this grid before it reads anything
+  pdl_launch_dependents();
   const int sub = lane % LPR;
   const uint32_t rowB = static_cast<uint32_t>(I / 2);
   const uint32_t sbB = (FMT == FT_INT4) ? static_cast<uint32_t>((I / a.group) * 2) : static_cast<uint32_t>(I / 16);
