@@ -13,6 +13,7 @@ namespace {
 constexpr int kResThreads = 1024;
 constexpr int kResMaxE = 4096;
 constexpr int kResMaxN = 4096;
+constexpr size_t kResSmemCap = 220 * 1024;  // dynamic shared memory the resolve kernel may use
 
 // The q* rule in Q16 fixed point: lo = floor(m*phi / 2^16); fetch lo or lo+1,
 // whichever gives the smaller slower-branch time max(f*(2^16-phi), (m-f)*phi)
@@ -37,6 +38,7 @@ __global__ void split_q16_kernel(const int32_t* __restrict__ m, int32_t n, int32
 
 struct ResolveArgs {
   int32_t E, S, layer, n, phi, max_list;
+  int32_t staged;  // 1: the victim search reads the slots' usage and hit flags from shared memory
   int32_t* slot_owner;
   int32_t* map;
   int64_t* usage;
@@ -56,6 +58,12 @@ __host__ __device__ inline size_t resolve_smem_bytes(int E, int n) {
   size_t ints = 2 * static_cast<size_t>(E) + 5 * static_cast<size_t>(cap);
   ints = (ints + 1) & ~static_cast<size_t>(1);
   return ints * 4 + 3 * static_cast<size_t>(cap) * 8;
+}
+
+// The victim search's copy of the slot state in shared memory, after the
+// arrays above: usage[S] int64, then a hit flag per slot.
+__host__ __device__ inline size_t resolve_stage_bytes(int S) {
+  return static_cast<size_t>(S) * 8 + ((static_cast<size_t>(S) + 15) & ~static_cast<size_t>(15));
 }
 
 // Is slot s owned by an expert of this call that is already resident (a hit)?
@@ -235,12 +243,29 @@ __global__ void __launch_bounds__(kResThreads, 1) resolve_kernel(ResolveArgs a) 
     if (r < nf) fe[r] = ej;
   }
 
-  // 4. the victims: the nf smallest (usage, slot) among non-hit slots
+  // 4. the victims: the nf smallest (usage, slot) among non-hit slots.  Each
+  // scan below reads a slot's usage and whether it is a hit; when the host
+  // found room (a.staged), one coalesced pass copies both into shared memory
+  // first, so the scans (several per call) read shared memory, not L2.
+  int64_t* su = nullptr;
+  unsigned char* shit = nullptr;
+  if (nf > 0 && a.staged) {
+    su = reinterpret_cast<int64_t*>(smem + resolve_smem_bytes(E, n));
+    shit = reinterpret_cast<unsigned char*>(su + S);
+#pragma unroll 4
+    for (int s = tid; s < S; s += nt) {
+      su[s] = a.usage[s];
+      shit[s] = is_hit_slot(a.slot_owner, s, base, E, inU);
+    }
+    __syncthreads();
+  }
+  auto slot_hit = [&](int s) -> bool { return shit ? shit[s] != 0 : is_hit_slot(a.slot_owner, s, base, E, inU); };
+  auto slot_use = [&](int s) -> int64_t { return su ? su[s] : a.usage[s]; };
   if (nf > 0) {
     unsigned long long kmin = ~0ull, kmax = 0ull;
     for (int s = tid; s < S; s += nt) {
-      if (is_hit_slot(a.slot_owner, s, base, E, inU)) continue;
-      const unsigned long long k = ukey(a.usage[s]);
+      if (slot_hit(s)) continue;
+      const unsigned long long k = ukey(slot_use(s));
       kmin = min(kmin, k);
       kmax = max(kmax, k);
     }
@@ -263,7 +288,7 @@ __global__ void __launch_bounds__(kResThreads, 1) resolve_kernel(ResolveArgs a) 
     const unsigned long long gmin = s_kmin, gmax = s_kmax;
     int c = 0;
     for (int s = tid; s < S; s += nt)
-      if (!is_hit_slot(a.slot_owner, s, base, E, inU) && ukey(a.usage[s]) == gmin) ++c;
+      if (!slot_hit(s) && ukey(slot_use(s)) == gmin) ++c;
     atomicAdd(&s_cmin, c);
     if (tid == 0) {
       s_prefix = 0ull;
@@ -282,8 +307,8 @@ __global__ void __launch_bounds__(kResThreads, 1) resolve_kernel(ResolveArgs a) 
         __syncthreads();
         const unsigned long long pre = s_prefix;
         for (int s = tid; s < S; s += nt) {
-          if (is_hit_slot(a.slot_owner, s, base, E, inU)) continue;
-          const unsigned long long d = ukey(a.usage[s]) - gmin;
+          if (slot_hit(s)) continue;
+          const unsigned long long d = ukey(slot_use(s)) - gmin;
           const bool match = (shift + 8 >= 64) ? true : ((d >> (shift + 8)) == pre);
           if (match) atomicAdd(&hist[(d >> shift) & 255ull], 1u);
         }
@@ -307,8 +332,8 @@ __global__ void __launch_bounds__(kResThreads, 1) resolve_kernel(ResolveArgs a) 
     if (tid == 0) s_cnt = 0;
     __syncthreads();
     for (int s = tid; s < S; s += nt) {
-      if (is_hit_slot(a.slot_owner, s, base, E, inU)) continue;
-      const int64_t u = a.usage[s];
+      if (slot_hit(s)) continue;
+      const int64_t u = slot_use(s);
       if (ukey(u) < tau) {
         const int p = atomicAdd(&s_cnt, 1);
         if (p < nf) {
@@ -326,8 +351,8 @@ __global__ void __launch_bounds__(kResThreads, 1) resolve_kernel(ResolveArgs a) 
       const int s = t0 + tid;
       int flag = 0;
       int64_t u = 0;
-      if (s < S && !is_hit_slot(a.slot_owner, s, base, E, inU)) {
-        u = a.usage[s];
+      if (s < S && !slot_hit(s)) {
+        u = slot_use(s);
         flag = (ukey(u) == tau);
       }
       int total;
@@ -499,9 +524,14 @@ ft_status ft_moe_resolve_slots(const ft_cache_state* st, int32_t layer, const in
   a.fetch_fid = fetch_fid;
   a.fetch_slot = fetch_slot;
   a.dev_status = dev_status;
-  const size_t smem = ft::resolve_smem_bytes(st->E, n);
+  // the slot state is staged in shared memory when it fits beside the
+  // resolve's own arrays (every cache up to ~24k slots at E <= 256)
+  size_t smem = ft::resolve_smem_bytes(st->E, n);
+  const size_t staged = smem + ft::resolve_stage_bytes(st->S);
+  a.staged = (st->S > 0 && staged <= ft::kResSmemCap) ? 1 : 0;
+  if (a.staged) smem = staged;
   if (smem > 48 * 1024) {
-    static const size_t kMax = ft::resolve_smem_bytes(ft::kResMaxE, ft::kResMaxN);
+    static const size_t kMax = ft::kResSmemCap;
     cudaError_t e = cudaFuncSetAttribute(ft::resolve_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kMax));

@@ -139,8 +139,12 @@ def test_resolve_hand_worked_trace(cuda_lib):
 
 
 @pytest.mark.parametrize("L,E,S,k,T", [(1, 16, 6, 2, 8), (3, 64, 40, 4, 3), (2, 512, 300, 10, 1),
-                                       (4, 256, 0, 8, 2), (1, 256, 256, 8, 8), (2, 40, 79, 6, 8)])
+                                       (4, 256, 0, 8, 2), (1, 256, 256, 8, 8), (2, 40, 79, 6, 8),
+                                       (8, 4096, 30000, 8, 4), (40, 256, 2560, 8, 8)])
 def test_resolve_random_sequences(cuda_lib, L, E, S, k, T):
+    """Random resolve sequences against the oracle.  Caches up to ~24k slots
+    run the victim search on a shared-memory copy of the slot state; the
+    30000-slot case does not fit and runs it on global memory."""
     ft = cuda_lib
     rng = np.random.default_rng(E * 1000 + S)
     host = oracle.CacheState(L, E, S)
