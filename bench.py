@@ -225,38 +225,53 @@ class DecodeWorkload:
                                device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
 
-    # one pass of the hot path over all layers (enqueue only); `ev` holds
-    # per-layer events: 2 around the experts call of every EXP_EVERY-th layer
-    # (an event node between kernels costs microseconds and breaks the
-    # programmatic launch chain, so the timed graph samples), or 5 around
-    # every op of every layer (per_op, the breakdown graph)
+    # one pass of the hot path over all layers (enqueue only).  fused: route
+    # and resolve in one launch (ft_moe_route_resolve), then fetch and the
+    # experts -- 4 kernels per layer; otherwise route, resolve, fetch, experts
+    # -- 5 kernels per layer; the same results (tested bit for bit).  `ev`
+    # holds per-layer events: 2 around the experts call of every EXP_EVERY-th
+    # layer (an event node between kernels costs microseconds and breaks the
+    # programmatic launch chain, so the timed graph samples), or one before
+    # each op and one after the last (per_op, the breakdown graph)
     EXP_EVERY = 8
+    OPS = {True: ["route+resolve", "fetch", "experts"], False: ["route", "resolve", "fetch", "experts"]}
+    KERNELS_PER_LAYER = {True: 4, False: 5}
 
-    def step(self, ev=None, per_op=False):
+    def step(self, ev=None, per_op=False, fused=True):
         ft, cfg, T = self.ft, self.cfg, self.T
+        nops = len(self.OPS[fused])
 
         def mark(l, i):
             if ev is None:
                 return
             if per_op:
                 ev[l][i].record()
-            elif i in (3, 4) and l % self.EXP_EVERY == 0:
-                ev[l // self.EXP_EVERY][i - 3].record()
+            elif i in (nops - 1, nops) and l % self.EXP_EVERY == 0:
+                ev[l // self.EXP_EVERY][i - nops + 1].record()
 
         for l in range(cfg.L):
-            mark(l, 0)
-            ft.route(self.x_stage[l], self.W[l], cfg.k, self.ids[l], self.w[l], self.rws)
-            mark(l, 1)
-            ft.resolve_slots(self.state, l, self.ids[l], self.phi, self.slot[l], self.nf[l], self.ff[l],
-                             self.fs[l], self.status)
-            mark(l, 2)
+            x = self.x_stage[l]
+            i = 0
+            mark(l, i)
+            if fused:
+                ft.route_resolve(x, self.W[l], cfg.k, self.state, l, self.phi, self.ids[l], self.w[l],
+                                 self.slot[l], self.nf[l], self.ff[l], self.fs[l], self.rws, dev_status=self.status)
+            else:
+                ft.route(x, self.W[l], cfg.k, self.ids[l], self.w[l], self.rws)
+                i += 1
+                mark(l, i)
+                ft.resolve_slots(self.state, l, self.ids[l], self.phi, self.slot[l], self.nf[l], self.ff[l],
+                                 self.fs[l], self.status)
+            i += 1
+            mark(l, i)
             ft.fetch(self.pool_b, self.cache_b, self.nf[l], self.ff[l], self.fs[l], self.status)
-            mark(l, 3)
-            ft.experts_fwd(self.cache_b, self.pool_b, l, cfg.E, self.x_stage[l], T, cfg.k, self.slot[l],
+            i += 1
+            mark(l, i)
+            ft.experts_fwd(self.cache_b, self.pool_b, l, cfg.E, x, T, cfg.k, self.slot[l],
                            self.ids[l], self.w[l], self.out[l], self.ews, dev_status=self.status)
-            mark(l, 4)
+            mark(l, i + 1)
 
-    def capture(self):
+    def capture(self, fused=True):
         """Two graphs of one step: `graph` (timed) with events only around the
         experts calls, `graph_ops` with events around every op (breakdown)."""
         import torch
@@ -265,18 +280,50 @@ class DecodeWorkload:
             return [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(n)]
                     for _ in range(rows)]
 
+        self.fused = fused
         self.ev_exp = events(2, (self.cfg.L + self.EXP_EVERY - 1) // self.EXP_EVERY)
-        self.ev_ops = events(5, self.cfg.L)
+        self.ev_ops = events(len(self.OPS[fused]) + 1, self.cfg.L)
         self.x_stage.copy_(self.x_all[0])
-        self.step()  # eager warm-up (attributes, lazy init) before capture
+        self.step(fused=fused)  # eager warm-up (attributes, lazy init) before capture
         torch.cuda.synchronize()
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph):
-            self.step(self.ev_exp)
+            self.step(self.ev_exp, fused=fused)
         self.graph_ops = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph_ops):
-            self.step(self.ev_ops, per_op=True)
+            self.step(self.ev_ops, per_op=True, fused=fused)
         torch.cuda.synchronize()
+
+    def settle(self, steps: int, seed: int = 1):
+        """Replay the step on `steps` fresh random token batches (generated on
+        the device, untimed) so the slot cache reaches its steady state under
+        the router's own routing before anything is timed: the seeded Zipf
+        history that warmed it has the router's popularity but not its
+        per-token draws, and the hit rate keeps improving for a few hundred
+        steps after it."""
+        import torch
+
+        g = torch.Generator(device=self.dev)
+        g.manual_seed(seed)
+        xv = self.x_stage.view(torch.bfloat16)
+        for _ in range(steps):
+            xv.normal_(generator=g)
+            xv[..., 0] = 1.0  # the router's bias feature
+            self.graph.replay()
+        torch.cuda.synchronize()
+
+    def fetch_rate(self, first: int, reps: int = 20):
+        """Mean fetched experts and host-path pairs per step over `reps` replays
+        on the inputs first.. (outside the timed region)."""
+        import torch
+
+        nf = hp = 0
+        for i in range(reps):
+            self.x_stage.copy_(self.x_all[(first + i) % self.x_all.shape[0]])
+            self.graph.replay()
+            nf += int(self.nf.sum().item())
+            hp += int((self.slot < 0).sum().item())
+        return nf / reps, hp / reps
 
     def experts_us(self):
         """Mean device time (us) of one experts call (gate/up + down) over the
@@ -289,7 +336,7 @@ class DecodeWorkload:
         outside the timed region."""
         import torch
 
-        names = ["route", "resolve", "fetch", "experts"]
+        names = self.OPS[self.fused]
         runs = []
         for i in range(reps):
             self.x_stage.copy_(self.x_all[(first + i) % self.x_all.shape[0]])
@@ -316,12 +363,15 @@ class DecodeWorkload:
         return int(self.nf.sum().item()), int((sl < 0).sum())
 
 
-def time_device(wl, steps: int, warmup: int, reduce_fn, world: int, clocks=None):
+def time_device(wl, steps: int, warmup: int, reduce_fn, world: int, clocks=None, first: int = 0):
+    """Device time of `steps` replays of the captured step on inputs
+    first+warmup.. (after `warmup` untimed replays on inputs first..)."""
     import torch
 
     s = torch.cuda.current_stream()
+    n_in = wl.x_all.shape[0]
     for i in range(warmup):
-        wl.x_stage.copy_(wl.x_all[i % wl.x_all.shape[0]])
+        wl.x_stage.copy_(wl.x_all[(first + i) % n_in])
         wl.graph.replay()
     torch.cuda.synchronize()
     if world > 1:
@@ -336,7 +386,7 @@ def time_device(wl, steps: int, warmup: int, reduce_fn, world: int, clocks=None)
     torch.cuda.cudart().cudaProfilerStart()  # a profiler started with --profile-from-start off sees only this
     e0.record(s)
     for i in range(steps):
-        wl.x_stage.copy_(wl.x_all[(warmup + i) % wl.x_all.shape[0]])
+        wl.x_stage.copy_(wl.x_all[(first + warmup + i) % n_in])
         wl.graph.replay()
     e1.record(s)
     torch.cuda.synchronize()
@@ -552,6 +602,72 @@ def prefill_bench(T: int, steps: int, warmup: int, device, log=print, state=None
     return res, state
 
 
+def prefill_pipeline_bench(T: int, n_layers: int, device, log=print, reps: int = 2):
+    """Prefill of n_layers consecutive layers of the prefill config with the
+    experts streamed from pinned host memory through the whole-layer double
+    buffer (pipeline.PrefillLayers: each layer copied by the copy engine into
+    one half of the cache's first 2E slots while the previous layer computes).
+    Returns the time per layer, the time of one layer's copy alone, and the
+    host-link rate they imply."""
+    import torch
+
+    import quantized_expert_ffn_router_gb300 as ft
+    import synth
+    from quantized_expert_ffn_router_gb300.pipeline import PrefillLayers
+
+    cfg = synth.get_config("prefill")
+    H, I, E, k = cfg.H, cfg.I, cfg.E, cfg.k
+    _, stride = synth.block_layout(cfg.fmt, H, I, cfg.g)
+    t0 = time.time()
+    pool = torch.empty((n_layers * E, stride), dtype=torch.uint8).pin_memory()
+    tmp = torch.empty((32, stride), dtype=torch.uint8, device=device)
+    for f0 in range(0, n_layers * E, 32):
+        synth.bank_blocks_torch(cfg.seed, range(f0, f0 + 32), cfg.fmt, H, I, cfg.g, tmp)
+        pool[f0:f0 + 32].copy_(tmp)
+    del tmp
+    torch.cuda.synchronize()
+    log(f"prefill pool: {n_layers} layers x {E} experts ({pool.numel() / 1e9:.1f} GB pinned) in {time.time() - t0:.1f}s")
+    ts = torch.from_numpy(synth.tensor_scales(cfg.fmt, H, I, n_layers * E)).to(device)
+    cache = torch.empty((2 * E, stride), dtype=torch.uint8, device=device)
+    pb = ft.make_bank(cfg.fmt, H, I, cfg.g, pool, ts)
+    cb = ft.make_bank(cfg.fmt, H, I, cfg.g, cache, ts)
+    state = ft.DeviceCacheState(n_layers, E, 2 * E, device=device)
+    xs = [torch.from_numpy(synth.normal_bf16(synth.stream_key(cfg.seed, "prefill-pipe-x", T, l), (T, H))
+                           .view(np.int16)).to(device) for l in range(n_layers)]
+    Ws = [torch.from_numpy(synth.router_weights(cfg.seed, l, E, H, cfg.router_std)).to(device)
+          for l in range(n_layers)]
+    outs = [torch.empty((T, H), dtype=torch.int16, device=device) for _ in range(n_layers)]
+    pl = PrefillLayers(state, cb, pb, E, k, T, device=device)
+    layers = list(range(n_layers))
+    pl(layers, xs, Ws, outs)  # warm-up (kernel attributes, tensor maps)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    per_layer = []
+    for _ in range(reps):
+        e0.record()
+        pl(layers, xs, Ws, outs)
+        e1.record()
+        torch.cuda.synchronize()
+        per_layer.append(e0.elapsed_time(e1) / n_layers)
+    copy_ms = []
+    for l in range(n_layers):
+        e0.record()
+        ft.fetch_layer(pb, cb, l, E, 0)
+        e1.record()
+        torch.cuda.synchronize()
+        copy_ms.append(e0.elapsed_time(e1))
+    if ft.get_status(pl.status) != 0:
+        raise RuntimeError(f"device status {ft.get_status(pl.status)} in the prefill pipeline")
+    layer_bytes = E * stride
+    res = {"T": T, "layers": n_layers, "ms_per_layer": min(per_layer),
+           "tokens_per_s_per_layer": T / (min(per_layer) * 1e-3),
+           "layer_copy_ms": statistics.median(copy_ms), "layer_bytes": layer_bytes,
+           "host_link_GBs": layer_bytes / (statistics.median(copy_ms) * 1e-3) / 1e9}
+    log(f"prefill pipeline T={T}: {res['ms_per_layer']:.2f} ms/layer, one layer's copy {res['layer_copy_ms']:.2f} ms "
+        f"({res['host_link_GBs']:.0f} GB/s)")
+    return res
+
+
 # ----------------------------------------------------- small cases for ncu --
 def kernel_case(name: str, T: int):
     """A small standalone workload for kernel profiling: a few calls of one
@@ -636,9 +752,15 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--tokens", type=int, default=1, help="decode batch (1 or 8)")
     ap.add_argument("--phi", type=int, default=65536, help="frac_q16 of the q* split")
+    ap.add_argument("--step", choices=["fused", "separate"], default="fused",
+                    help="fused: ft_moe_route_resolve per layer; separate: ft_moe_route + ft_moe_resolve_slots")
+    ap.add_argument("--settle", type=int, default=512,
+                    help="untimed steps on fresh tokens before timing, so the cache reaches steady state")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--extra-batch", type=int, default=8, help="also time this batch (0: off)")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill layer measurement")
+    ap.add_argument("--prefill-layers", type=int, default=3,
+                    help="layers streamed from host memory through the prefill double buffer (0: skip)")
     ap.add_argument("--case", choices=["decode", "decode-flash", "prefill"],
                     help="run a small kernel case for a profiler instead of the benchmark")
     args = ap.parse_args()
@@ -676,7 +798,9 @@ def main():
         dist.init_process_group("nccl", device_id=device)
         reduce_fn = torch_reduce_fn(device)
 
-    n_steps = args.warmup + 2 * args.steps + 5  # device-timed steps, e2e steps, per-op breakdown
+    # device-timed steps, e2e steps, per-op breakdown, fetch statistics
+    n_steps = args.warmup + 2 * args.steps + 5 + 20
+    fused = args.step == "fused"
     results = {}
     batches = [args.tokens] + ([args.extra_batch] if args.extra_batch and args.extra_batch != args.tokens else [])
     wl = None
@@ -685,7 +809,8 @@ def main():
             wl = DecodeWorkload(cfg, T, args.phi, n_steps, device, log)
         else:
             wl = reshape_workload(wl, T, n_steps)
-        wl.capture()
+        wl.capture(fused=fused)
+        wl.settle(args.settle)
         clocks = ClockSampler(local) if bi == 0 else None
         secs = time_device(wl, args.steps, args.warmup, reduce_fn, world, clocks)
         units = T * cfg.L * args.steps
@@ -693,7 +818,7 @@ def main():
         exp_us = wl.experts_us()
         ebytes = wl.distinct_expert_bytes()
         kt = None
-        nfetch, host_pairs = wl.misses()
+        nfetch, host_pairs = wl.fetch_rate(first=args.warmup + 2 * args.steps + 5)
         e2e_secs, h2d, d2h = time_e2e(wl, args.steps, args.warmup)
         kt = wl.op_times(first=args.warmup + 2 * args.steps)
         e2e_val, _, _ = aggregate(units, e2e_secs, world, reduce_fn)
@@ -715,6 +840,10 @@ def main():
             res, pst = prefill_bench(Tp, max(3, min(args.steps, 20)), args.warmup, device, log, pst)
             prefill[str(Tp)] = res
         del pst
+        torch.cuda.empty_cache()
+        if args.prefill_layers > 0:
+            prefill["streamed"] = prefill_pipeline_bench(synth.get_config("prefill").tokens[0], args.prefill_layers,
+                                                         device, log)
     if rank != 0:
         return
     peaks, peak_kind = measured_peaks()
@@ -743,7 +872,7 @@ def main():
         cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"{n} single-layer calls of {args.tokens} token(s) (route, resolve, fp64 experts) "
                          f"on 2 of 40 layers, {dt:.1f} s, single-threaded C++"}
-    launches_per_step = cfg.L * 6
+    launches_per_step = cfg.L * DecodeWorkload.KERNELS_PER_LAYER[fused]
     line = {
         "metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["secs"] / args.steps * 1e3, "higher_is_better": True,
@@ -765,15 +894,21 @@ def main():
             "model_tokens_per_s": r["value"] / cfg.L,
             "per_op_us_per_step": kt,
             "expert_bytes_per_step": r["ebytes"],
+            "step": ("per layer: ft_moe_route_resolve (route and resolve, one kernel), ft_moe_fetch, "
+                     "ft_moe_experts_fwd (two kernels)") if fused else
+                    "per layer: ft_moe_route, ft_moe_resolve_slots, ft_moe_fetch, ft_moe_experts_fwd (two kernels)",
+            "settle_steps": args.settle,
             "fetched_experts_per_step": r["nfetch"],
             "host_path_pairs_per_step": r["host_pairs"],
+            "fetch_stats": "mean of 20 steps after the timed region",
             "prefill": None if prefill is None else {
                 "workload": "one prefill MoE layer: NVFP4, H 4096, I 2048, 256 experts, top-6, all experts "
                             "resident; route -> permute -> grouped SwiGLU on tcgen05 -> combine",
                 "tensor_peak_tflops": peaks["bf16_tflops"],
                 "tensor_peak_kind": f"{peak_kind} bf16 dense (f16 runs at the bf16 rate)",
                 "by_tokens": {t: dict(v, tensor_frac=v["grouped_gemm_tflops"] / peaks["bf16_tflops"])
-                              for t, v in prefill.items()}},
+                              for t, v in prefill.items() if t != "streamed"},
+                "streamed_from_host": prefill.get("streamed")},
             "other_batches": {str(T): {"value": v["value"], "ms_per_step": v["secs"] / args.steps * 1e3,
                                        "per_op_us_per_step": v["kt"], "expert_bytes_per_step": v["ebytes"],
                                        "experts_us_per_call": v["exp_us"],

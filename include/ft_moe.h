@@ -6,11 +6,15 @@
  *   ft_moe_route          router logits, softmax, top-k
  *   ft_moe_resolve_slots  (layer, expert) -> cache slot or -1, q* split inside
  *   ft_moe_fetch          copy the chosen misses from the pool into the cache
+ *   ft_moe_fetch_layer    copy a whole layer into a slot range (prefill buffer)
+ *   ft_moe_cache_install  the state's bookkeeping for such a layer
  *   ft_moe_experts_fwd    quantized SwiGLU experts (decode: combine fused)
  *   ft_moe_permute        token permutation by expert (prefill)
  *   ft_moe_combine        top-k weighted sum of permuted expert rows (prefill)
  *   ft_moe_split_q16      the q* rule alone, batched (the resolve kernel runs
  *                         the same device function)
+ *   ft_moe_route_resolve  route + resolve in one launch (decode; bit-identical
+ *                         to the two calls)
  *
  * Sources, by page title and section:
  *   "FreeToken 딥다이브" (fiv.co.kr) -- design pattern 1 (whole-layer double
@@ -166,6 +170,24 @@ FT_API ft_status ft_moe_route(const uint16_t* x, int32_t T, int32_t H, const flo
                        void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * ft_moe_route_resolve -- ft_moe_route followed by ft_moe_resolve_slots in
+ * one launch, for decode (T <= 16): the router's last CTA, once it has the
+ * top-k of every token, resolves them against the slot cache itself (the
+ * FreeToken paper post, sec. 6: the decisions stay in GPU data, in one
+ * kernel; the deep-dive's design pattern 2: no host round trip inside the
+ * decode graph).  Arguments, outputs, state update, limits and errors are
+ * those of the two calls (ws as for ft_moe_route; state_host->E must equal
+ * E); the results are bit-identical to the two calls in a row.  T == 0 runs
+ * the resolve alone (it still advances the step).
+ */
+FT_API ft_status ft_moe_route_resolve(const uint16_t* x, int32_t T, int32_t H, const float* w_router,
+                                      int32_t E, int32_t k, int32_t renorm, const ft_cache_state* state_host,
+                                      int32_t layer, int32_t frac_q16, int32_t* topk_ids, float* topk_w,
+                                      int32_t* slot_ids, int32_t* num_fetch, int32_t* fetch_fid,
+                                      int32_t* fetch_slot, int32_t max_list, void* ws, size_t ws_bytes,
+                                      int32_t* dev_status, void* stream);
+
+/*
  * ft_moe_split_q16 -- the bandwidth-matched q* rule in Q16 fixed point
  * (FreeToken deep-dive, design pattern 2; paper post, sec. 6).  For each m =
  * num_missing[i] and phi = frac_q16 = round(65536 * B_P / B_H):
@@ -214,6 +236,36 @@ FT_API ft_status ft_moe_fetch(const ft_bank* pool_host, const ft_bank* cache_hos
                        const int32_t* num_fetch, const int32_t* fetch_fid,
                        const int32_t* fetch_slot, int32_t max_list, int32_t* dev_status,
                        void* stream);
+
+/*
+ * ft_moe_fetch_layer -- copy every expert block of one layer, pool flat ids
+ * layer*E .. layer*E+E-1, into cache slots slot0 .. slot0+E-1 with one
+ * copy-engine transfer (no kernel: the SMs stay free for the experts).  It
+ * is the load of prefill's whole-layer double buffer: layer l's experts in
+ * slots (l%2)*E .., the next layer copied into the other half while this one
+ * computes (FreeToken deep-dive, design pattern 1; paper post, sec. 5).
+ * Pool and cache must have the same format and shape; the flat ids must be
+ * inside the pool and the slots inside the cache (FT_ERR_INVALID otherwise,
+ * checked on the host).  The cache state is not touched: pair it with
+ * ft_moe_cache_install.
+ */
+FT_API ft_status ft_moe_fetch_layer(const ft_bank* pool_host, const ft_bank* cache_host, int32_t layer,
+                                    int32_t E, int32_t slot0, void* stream);
+
+/*
+ * ft_moe_cache_install -- the slot cache's bookkeeping for a whole layer
+ * placed in slots slot0 .. slot0+E-1 (the prefill double buffer above, which
+ * then seeds decode).  With the end state of installing expert e = 0, 1, ..
+ * in turn: a copy of flat id layer*E+e held in another slot outside the
+ * range is dropped (owner -1, usage -1); the slot's previous owner is
+ * evicted (map -1); slot slot0+e takes flat id layer*E+e with usage = the
+ * current step.  Recency and the step are left alone (no routing happened).
+ * Limits: E <= 4096, layer < L, slot0 + E <= S (FT_ERR_INVALID otherwise).
+ * One small kernel on the stream; order it after the copy that fills the
+ * slots when decode may run in between.
+ */
+FT_API ft_status ft_moe_cache_install(const ft_cache_state* state_host, int32_t layer, int32_t slot0,
+                                      void* stream);
 
 /*
  * ft_moe_cache_rebuild -- rebuild the slot cache at a new size (FreeToken

@@ -20,6 +20,8 @@ Parity status per function (what pins it is in the "not gpu" tests):
   expert, layer    pinned: closed forms on one-hot quantised matrices.
   permute          pinned: numpy stable argsort, segment invariants.
   combine          pinned: one-hot weights, linearity.
+  cache_rebuild    pinned: invariants, brute force on small states.
+  cache_install    pinned: a hand-worked example, invariants on random states.
 """
 
 from __future__ import annotations
@@ -87,6 +89,9 @@ def lib():
             L.orc_resolve_many.argtypes = ([c.c_int] * 3 + [c.c_void_p] * 5 + [c.c_int, c.c_void_p,
                                            c.c_int, c.c_int, c.c_int32, c.c_int] + [c.c_void_p] * 4
                                            + [c.c_int])
+            L.orc_cache_install.restype = c.c_int
+            L.orc_cache_install.argtypes = [c.c_int, c.c_int, c.c_int, c.c_void_p, c.c_void_p, c.c_void_p,
+                                            c.c_void_p, c.c_int, c.c_int]
             L.orc_cache_rebuild.restype = c.c_int
             L.orc_cache_rebuild.argtypes = [c.c_int, c.c_int, c.c_int, c.c_void_p, c.c_void_p, c.c_int,
                                             c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p]
@@ -277,6 +282,15 @@ def cache_rebuild(st: CacheState, S_new: int):
     new.recency[:] = st.recency
     new.step[:] = st.step
     return new, src
+
+
+def cache_install(st: CacheState, layer: int, slot0: int):
+    """Install all E experts of `layer` in slots slot0..slot0+E-1, in place
+    (see orc_cache_install)."""
+    rc = lib().orc_cache_install(st.L, st.E, st.S, _ptr(st.slot_owner), _ptr(st.map), _ptr(st.usage),
+                                 _ptr(st.step), int(layer), int(slot0))
+    if rc != 0:
+        raise ValueError("orc_cache_install: layer or slot range out of bounds")
 
 
 def permute(ids: np.ndarray, E: int):

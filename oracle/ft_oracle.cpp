@@ -449,6 +449,39 @@ int orc_cache_rebuild(int L, int E, int S_old, const int32_t* owner_old, const i
   return 0;
 }
 
+// -------------------------------------------------------------- install ----
+// [FT-KR] design pattern 1 and [FT-ZH] sec. 5: prefill holds a whole layer's
+// experts on the GPU in one half of a two-layer buffer made of the cache's
+// first 2E slots (layer l in slots (l%2)*E ..), which then seeds decode.  The
+// pages do not spell out the bookkeeping; the reading taken here installs
+// expert e of `layer` (flat id layer*E+e) in slot slot0+e, one expert after
+// the other in e order: a copy of that flat id held in any other slot is
+// dropped (slot emptied, usage -1), the slot's previous owner (another flat
+// id) is evicted (its map entry -1), and the slot takes the flat id with
+// usage = the current step.  Recency and the step do not change (no routing
+// happened).  Returns -1 when layer or the slot range is out of bounds.
+// Parity: pinned by a hand-worked example and by invariants.
+int orc_cache_install(int L, int E, int S, int32_t* slot_owner, int32_t* map, int64_t* usage,
+                      const int64_t* step, int layer, int slot0) {
+  if (layer < 0 || layer >= L || slot0 < 0 || static_cast<int64_t>(slot0) + E > S) return -1;
+  for (int e = 0; e < E; ++e) {
+    const int32_t fid = layer * E + e;
+    const int s = slot0 + e;
+    const int32_t was = map[fid];
+    if (was >= 0 && was != s) {
+      slot_owner[was] = -1;
+      usage[was] = -1;
+      map[fid] = -1;
+    }
+    const int32_t old = slot_owner[s];
+    if (old >= 0 && old != fid) map[old] = -1;
+    slot_owner[s] = fid;
+    map[fid] = s;
+    usage[s] = step[0];
+  }
+  return 0;
+}
+
 // -------------------------------------------------------------- permute ----
 // Stable sort of the T*k (token, rank) pairs by expert: expert ascending, then
 // token, then rank.  perm[pos] = pair index t*k+j, inv[t*k+j] = pos,

@@ -52,9 +52,13 @@ _SIGS = {
     "ft_moe_get_status": (_I32, [_V, _V]),
     "ft_moe_route_workspace": (_SZ, [_I32, _I32]),
     "ft_moe_route": (_I32, [_V, _I32, _I32, _V, _I32, _I32, _I32, _V, _V, _V, _SZ, _V]),
+    "ft_moe_route_resolve": (_I32, [_V, _I32, _I32, _V, _I32, _I32, _I32, _V, _I32, _I32, _V, _V, _V, _V, _V,
+                                    _V, _I32, _V, _SZ, _V, _V]),
     "ft_moe_split_q16": (_I32, [_V, _I32, _I32, _V, _V]),
     "ft_moe_resolve_slots": (_I32, [_V, _I32, _V, _I32, _I32, _I32, _V, _V, _V, _V, _I32, _V, _V]),
     "ft_moe_fetch": (_I32, [_V, _V, _V, _V, _V, _I32, _V, _V]),
+    "ft_moe_fetch_layer": (_I32, [_V, _V, _I32, _I32, _I32, _V]),
+    "ft_moe_cache_install": (_I32, [_V, _I32, _I32, _V]),
     "ft_moe_cache_rebuild": (_I32, [_V, _V, _V, _V, _U64, _V, _V]),
     "ft_moe_experts_workspace": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
     "ft_moe_experts_fwd": (_I32, [_V, _V, _I32, _I32, _V, _V, _I32, _V, _V, _V, _I32, _I32, _V, _V,
@@ -166,6 +170,20 @@ def route(x, w_router, k: int, topk_ids, topk_w, ws, renorm: bool = False, strea
                                _ptr(topk_w), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
+def route_resolve(x, w_router, k: int, state: DeviceCacheState, layer: int, frac_q16: int, topk_ids, topk_w,
+                  slot_ids, num_fetch, fetch_fid, fetch_slot, ws, dev_status=None, renorm: bool = False,
+                  stream=None):
+    """route then resolve_slots, in one launch (T <= 16)."""
+    T, H = x.shape
+    E = w_router.shape[0]
+    st = state.struct()
+    _check(load().ft_moe_route_resolve(_ptr(x), T, H, _ptr(w_router), E, k, int(bool(renorm)), ctypes.byref(st),
+                                       layer, int(frac_q16), _ptr(topk_ids), _ptr(topk_w), _ptr(slot_ids),
+                                       _ptr(num_fetch), _ptr(fetch_fid), _ptr(fetch_slot), fetch_fid.numel(),
+                                       _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status),
+                                       _stream(stream)))
+
+
 def split_q16(num_missing, frac_q16: int, num_fetch, stream=None):
     _check(load().ft_moe_split_q16(_ptr(num_missing), num_missing.numel(), int(frac_q16),
                                    _ptr(num_fetch), _stream(stream)))
@@ -185,6 +203,17 @@ def fetch(pool: FtBank, cache: FtBank, num_fetch, fetch_fid, fetch_slot, dev_sta
     _check(load().ft_moe_fetch(ctypes.byref(pool), ctypes.byref(cache), _ptr(num_fetch),
                                _ptr(fetch_fid), _ptr(fetch_slot), fetch_fid.numel(),
                                _ptr(dev_status), _stream(stream)))
+
+
+def fetch_layer(pool: FtBank, cache: FtBank, layer: int, E: int, slot0: int, stream=None):
+    """Copy layer `layer`'s E expert blocks from the pool into cache slots slot0.. (copy engine)."""
+    _check(load().ft_moe_fetch_layer(ctypes.byref(pool), ctypes.byref(cache), layer, E, slot0, _stream(stream)))
+
+
+def cache_install(state: DeviceCacheState, layer: int, slot0: int, stream=None):
+    """Record layer `layer`'s experts as resident in slots slot0..slot0+E-1."""
+    st = state.struct()
+    _check(load().ft_moe_cache_install(ctypes.byref(st), layer, slot0, _stream(stream)))
 
 
 def cache_rebuild(old_state, old_cache: FtBank, new_state, new_cache: FtBank, budget_bytes: int,

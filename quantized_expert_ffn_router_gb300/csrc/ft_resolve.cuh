@@ -1,0 +1,419 @@
+// ft_resolve.cuh -- the resolve of a layer's top-k ids against the global
+// slot cache, as a device function that one CTA runs: the resolve kernel
+// (cache.cu) and the fused route + resolve kernel (route.cu) share it.
+//
+// Sources: "FreeToken 딥다이브" (fiv.co.kr), design patterns 2, 3, 5;
+// "FreeToken: 让消费级电脑跑起 284B MoE" (fengjutian.github.io), sec. 6 (one
+// kernel does dedup, residency, q, victims and the id rewrite).
+#pragma once
+
+#include "ft_common.cuh"
+
+namespace ft {
+
+constexpr int kResMaxE = 4096;
+constexpr int kResMaxN = 4096;
+constexpr size_t kResSmemCap = 220 * 1024;  // dynamic shared memory the resolve kernel may use
+
+struct ResolveArgs {
+  int32_t E, S, layer, n, phi, max_list;
+  int32_t staged;  // 1: the victim search reads the slots' usage and hit flags from shared memory
+  int32_t* slot_owner;
+  int32_t* map;
+  int64_t* usage;
+  int64_t* recency;
+  int64_t* step;
+  const int32_t* ids;
+  int32_t* slot_ids;
+  int32_t* num_fetch;
+  int32_t* fetch_fid;
+  int32_t* fetch_slot;
+  int32_t* dev_status;
+};
+
+__host__ __device__ inline size_t resolve_smem_bytes(int E, int n) {
+  const int cap = n < E ? n : E;
+  // inU[E] slotOf[E] U[cap] M[cap] fe[cap] vs[cap] vs2[cap] | mrec[cap] vu[cap] vu2[cap]
+  size_t ints = 2 * static_cast<size_t>(E) + 5 * static_cast<size_t>(cap);
+  ints = (ints + 1) & ~static_cast<size_t>(1);
+  return ints * 4 + 3 * static_cast<size_t>(cap) * 8;
+}
+
+// The victim search's copy of the slot state in shared memory, after the
+// arrays above: usage[S] int64, then a hit flag per slot.
+__host__ __device__ inline size_t resolve_stage_bytes(int S) {
+  return static_cast<size_t>(S) * 8 + ((static_cast<size_t>(S) + 15) & ~static_cast<size_t>(15));
+}
+// Host: check a resolve call's arguments and fill its device arguments,
+// deciding whether the victim search may stage the slot state in shared
+// memory: when the total stays within stage_cap bytes (FT_ERR_INVALID with a
+// message when a check fails; `what` names the call).  *smem_out: the
+// dynamic shared memory the resolve needs.
+ft_status resolve_prepare(const ft_cache_state* st, int32_t layer, const int32_t* topk_ids, int32_t T,
+                          int32_t k, int32_t frac_q16, int32_t* slot_ids, int32_t* num_fetch,
+                          int32_t* fetch_fid, int32_t* fetch_slot, int32_t max_list, int32_t* dev_status,
+                          const char* what, size_t stage_cap, ResolveArgs* out, size_t* smem_out);
+
+namespace {
+
+// The q* rule in Q16 fixed point: lo = floor(m*phi / 2^16); fetch lo or lo+1,
+// whichever gives the smaller slower-branch time max(f*(2^16-phi), (m-f)*phi)
+// (ties to lo), capped at m.  phi == 0 applies no cap.  64-bit intermediates.
+__device__ __forceinline__ int32_t split_q16_dev(int32_t m, int32_t phi) {
+  if (m <= 0) return 0;
+  if (phi <= 0) return m;
+  const int64_t q = 65536;
+  const int64_t M = m, P = phi;
+  const int64_t lo = (M * P) >> 16;
+  const int64_t c_lo = max(lo * (q - P), (M - lo) * P);
+  const int64_t c_hi = max((lo + 1) * (q - P), (M - lo - 1) * P);
+  const int64_t f = (c_lo <= c_hi) ? lo : lo + 1;
+  return static_cast<int32_t>(min(M, f));
+}
+// Is slot s owned by an expert of this call that is already resident (a hit)?
+__device__ __forceinline__ bool is_hit_slot(const int32_t* __restrict__ owner, int s, int base,
+                                            int E, const int* inU) {
+  const int o = owner[s];
+  return o >= base && o < base + E && inU[o - base] != 0;
+}
+
+__device__ __forceinline__ uint64_t ukey(int64_t u) {
+  return static_cast<uint64_t>(u) ^ 0x8000000000000000ull;
+}
+
+// The common small case in one warp: n <= 32 ids, all valid, and the q*
+// split fetches nothing (every distinct expert hits, or the split or the
+// evictable slots allow no fetch).  Then the state update is only the usage
+// of the hit slots and the recency of the distinct experts, and the outputs
+// are the map lookups -- the same results as the general path below.
+// Returns true (warp-uniform) when it has done the whole call.
+__device__ bool resolve_small_no_fetch(const ResolveArgs& a) {
+  const int lane = threadIdx.x & 31;
+  const int n = a.n, E = a.E, base = a.layer * a.E;
+  const int64_t now = *a.step;
+  const int e = lane < n ? a.ids[lane] : -1;
+  const bool bad = lane < n && (e < 0 || e >= E);
+  if (__any_sync(0xffffffffu, bad)) return false;
+  const int s = lane < n ? a.map[base + e] : -1;
+  const unsigned same = __match_any_sync(0xffffffffu, e);
+  const bool leader = lane < n && lane == __ffs(same) - 1;
+  const int nhit = __popc(__ballot_sync(0xffffffffu, leader && s >= 0));
+  const int m = __popc(__ballot_sync(0xffffffffu, leader && s < 0));
+  const int nf = max(0, min(split_q16_dev(m, a.phi), a.S - nhit));
+  if (nf > 0) return false;
+  if (leader) {
+    if (s >= 0) a.usage[s] = now;
+    a.recency[base + e] = now;
+  }
+  if (lane < n) a.slot_ids[lane] = s;
+  for (int i = lane; i < a.max_list; i += 32) {
+    a.fetch_fid[i] = -1;
+    a.fetch_slot[i] = -1;
+  }
+  if (lane == 0) {
+    *a.num_fetch = 0;
+    *a.step = now + 1;
+  }
+  return true;
+}
+// The whole resolve call by one CTA (any block size; every thread calls it).
+// smem: the dynamic shared memory resolve_prepare asked for.  ids must be
+// readable by the CTA (written by an earlier grid, or by this CTA before a
+// __syncthreads).
+__device__ __noinline__ void resolve_block(const ResolveArgs& a, unsigned char* smem) {
+  const int E = a.E, n = a.n, S = a.S;
+  const int cap = n < E ? n : E;
+  int* inU = reinterpret_cast<int*>(smem);
+  int* slotOf = inU + E;
+  int* U = slotOf + E;
+  int* M = U + cap;
+  int* fe = M + cap;
+  int* vs = fe + cap;
+  int* vs2 = vs + cap;
+  size_t ints = 2 * static_cast<size_t>(E) + 5 * static_cast<size_t>(cap);
+  ints = (ints + 1) & ~static_cast<size_t>(1);
+  int64_t* mrec = reinterpret_cast<int64_t*>(smem + ints * 4);
+  int64_t* vu = mrec + cap;
+  int64_t* vu2 = vu + cap;
+
+  __shared__ int scan_scratch[33];
+  __shared__ int s_bad, s_nU, s_m, s_nf, s_cnt;
+  __shared__ unsigned int hist[256];
+  __shared__ unsigned long long s_kmin, s_kmax, s_prefix;
+  __shared__ int s_krem, s_cmin;
+  __shared__ long long s_now;
+
+  const int tid = threadIdx.x;
+  const int nt = blockDim.x;
+  const int base = a.layer * E;
+
+  if (n <= 32) {
+    __shared__ int s_done;
+    if (tid < 32) {
+      const bool done = resolve_small_no_fetch(a);
+      if (tid == 0) s_done = done;
+    }
+    __syncthreads();
+    if (s_done) return;
+  }
+
+  for (int e = tid; e < E; e += nt) {
+    inU[e] = 0;
+    slotOf[e] = -1;
+  }
+  if (tid == 0) {
+    s_bad = 0;
+    s_now = *a.step;
+  }
+  __syncthreads();
+  for (int i = tid; i < n; i += nt) {
+    const int e = a.ids[i];
+    if (e < 0 || e >= E)
+      s_bad = 1;
+    else
+      inU[e] = 1;
+  }
+  __syncthreads();
+  if (s_bad) {
+    for (int i = tid; i < n; i += nt) a.slot_ids[i] = -1;
+    for (int i = tid; i < a.max_list; i += nt) {
+      a.fetch_fid[i] = -1;
+      a.fetch_slot[i] = -1;
+    }
+    if (tid == 0) {
+      *a.num_fetch = 0;
+      record_status(a.dev_status, FT_ERR_BAD_ID);
+    }
+    return;
+  }
+
+  // 1. U = distinct experts, ascending (ordered compaction over contiguous ranges)
+  {
+    const int per = (E + nt - 1) / nt;
+    const int lo = min(E, tid * per), hi = min(E, lo + per);
+    int cnt = 0;
+    for (int e = lo; e < hi; ++e) cnt += inU[e];
+    int total;
+    int off = block_excl_scan(cnt, scan_scratch, &total);
+    for (int e = lo; e < hi; ++e)
+      if (inU[e]) U[off++] = e;
+    if (tid == 0) s_nU = total;
+  }
+  __syncthreads();
+  const int nU = s_nU;
+
+  // 2. hits / misses; misses keep ascending order
+  {
+    const int per = (nU + nt - 1) / nt;
+    const int lo = min(nU, tid * per), hi = min(nU, lo + per);
+    int cnt = 0;
+    for (int i = lo; i < hi; ++i) {
+      const int e = U[i];
+      const int s = a.map[base + e];
+      slotOf[e] = s;
+      cnt += (s < 0);
+    }
+    int total;
+    int off = block_excl_scan(cnt, scan_scratch, &total);
+    for (int i = lo; i < hi; ++i) {
+      const int e = U[i];
+      if (slotOf[e] < 0) {
+        M[off] = e;
+        mrec[off] = a.recency[base + e];
+        ++off;
+      }
+    }
+    if (tid == 0) {
+      s_m = total;
+      const int nhit = nU - total;
+      const int evictable = S - nhit;
+      int nf = split_q16_dev(total, a.phi);
+      nf = min(nf, evictable);
+      s_nf = max(nf, 0);
+    }
+  }
+  __syncthreads();
+  const int m = s_m, nf = s_nf;
+
+  // 3. the fetched misses: rank by (recency desc, id asc)
+  for (int j = tid; j < m; j += nt) {
+    const int64_t rj = mrec[j];
+    const int ej = M[j];
+    int r = 0;
+    for (int j2 = 0; j2 < m; ++j2) {
+      const int64_t r2 = mrec[j2];
+      r += (r2 > rj) || (r2 == rj && M[j2] < ej);
+    }
+    if (r < nf) fe[r] = ej;
+  }
+
+  // 4. the victims: the nf smallest (usage, slot) among non-hit slots.  Each
+  // scan below reads a slot's usage and whether it is a hit; when the host
+  // found room (a.staged), one coalesced pass copies both into shared memory
+  // first, so the scans (several per call) read shared memory, not L2.
+  int64_t* su = nullptr;
+  unsigned char* shit = nullptr;
+  if (nf > 0 && a.staged) {
+    su = reinterpret_cast<int64_t*>(smem + resolve_smem_bytes(E, n));
+    shit = reinterpret_cast<unsigned char*>(su + S);
+#pragma unroll 4
+    for (int s = tid; s < S; s += nt) {
+      su[s] = a.usage[s];
+      shit[s] = is_hit_slot(a.slot_owner, s, base, E, inU);
+    }
+    __syncthreads();
+  }
+  auto slot_hit = [&](int s) -> bool { return shit ? shit[s] != 0 : is_hit_slot(a.slot_owner, s, base, E, inU); };
+  auto slot_use = [&](int s) -> int64_t { return su ? su[s] : a.usage[s]; };
+  if (nf > 0) {
+    unsigned long long kmin = ~0ull, kmax = 0ull;
+    for (int s = tid; s < S; s += nt) {
+      if (slot_hit(s)) continue;
+      const unsigned long long k = ukey(slot_use(s));
+      kmin = min(kmin, k);
+      kmax = max(kmax, k);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+      kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+    }
+    if (tid == 0) {
+      s_kmin = ~0ull;
+      s_kmax = 0ull;
+      s_cmin = 0;
+    }
+    __syncthreads();
+    if ((tid & 31) == 0) {
+      atomicMin(&s_kmin, kmin);
+      atomicMax(&s_kmax, kmax);
+    }
+    __syncthreads();
+    const unsigned long long gmin = s_kmin, gmax = s_kmax;
+    int c = 0;
+    for (int s = tid; s < S; s += nt)
+      if (!slot_hit(s) && ukey(slot_use(s)) == gmin) ++c;
+    atomicAdd(&s_cmin, c);
+    if (tid == 0) {
+      s_prefix = 0ull;
+      s_krem = nf;
+    }
+    __syncthreads();
+    unsigned long long tau;
+    if (s_cmin >= nf || gmax == gmin) {
+      tau = gmin;
+    } else {
+      // radix select over d = key - min, 8 bits per pass from the top digit
+      const unsigned long long range = gmax - gmin;
+      const int nbits = 64 - __clzll(static_cast<long long>(range));
+      for (int shift = ((nbits - 1) / 8) * 8; shift >= 0; shift -= 8) {
+        for (int b = tid; b < 256; b += nt) hist[b] = 0;
+        __syncthreads();
+        const unsigned long long pre = s_prefix;
+        for (int s = tid; s < S; s += nt) {
+          if (slot_hit(s)) continue;
+          const unsigned long long d = ukey(slot_use(s)) - gmin;
+          const bool match = (shift + 8 >= 64) ? true : ((d >> (shift + 8)) == pre);
+          if (match) atomicAdd(&hist[(d >> shift) & 255ull], 1u);
+        }
+        __syncthreads();
+        if (tid == 0) {
+          int krem = s_krem;
+          int b = 0;
+          unsigned int cum = 0;
+          for (; b < 256; ++b) {
+            if (cum + hist[b] >= static_cast<unsigned int>(krem)) break;
+            cum += hist[b];
+          }
+          s_krem = krem - static_cast<int>(cum);
+          s_prefix = (pre << 8) | static_cast<unsigned long long>(b);
+        }
+        __syncthreads();
+      }
+      tau = gmin + s_prefix;
+    }
+    // keys below tau: all taken (unordered append)
+    if (tid == 0) s_cnt = 0;
+    __syncthreads();
+    for (int s = tid; s < S; s += nt) {
+      if (slot_hit(s)) continue;
+      const int64_t u = slot_use(s);
+      if (ukey(u) < tau) {
+        const int p = atomicAdd(&s_cnt, 1);
+        if (p < nf) {
+          vs[p] = s;
+          vu[p] = u;
+        }
+      }
+    }
+    __syncthreads();
+    const int nless = min(s_cnt, nf);
+    const int need = nf - nless;
+    // keys equal to tau: the lowest slots first (ordered scan over slots)
+    int running = 0;
+    for (int t0 = 0; t0 < S && running < need; t0 += nt) {
+      const int s = t0 + tid;
+      int flag = 0;
+      int64_t u = 0;
+      if (s < S && !slot_hit(s)) {
+        u = slot_use(s);
+        flag = (ukey(u) == tau);
+      }
+      int total;
+      const int pos = block_excl_scan(flag, scan_scratch, &total) + running;
+      if (flag && pos < need) {
+        vs[nless + pos] = s;
+        vu[nless + pos] = u;
+      }
+      running += total;
+    }
+    __syncthreads();
+    // order the victims by (usage asc, slot asc)
+    for (int i = tid; i < nf; i += nt) {
+      const int64_t ui = vu[i];
+      const int si = vs[i];
+      int r = 0;
+      for (int j = 0; j < nf; ++j) r += (vu[j] < ui) || (vu[j] == ui && vs[j] < si);
+      vs2[r] = si;
+      vu2[r] = ui;
+    }
+  }
+  __syncthreads();
+
+  // 5. state update
+  const int64_t now = s_now;
+  for (int i = tid; i < nU; i += nt) {
+    const int s = slotOf[U[i]];
+    if (s >= 0) a.usage[s] = now;
+  }
+  for (int i = tid; i < nf; i += nt) {
+    const int v = vs2[i];
+    const int old = a.slot_owner[v];
+    if (old >= 0) a.map[old] = -1;
+  }
+  __syncthreads();
+  for (int i = tid; i < nf; i += nt) {
+    const int e = fe[i];
+    const int v = vs2[i];
+    a.slot_owner[v] = base + e;
+    a.map[base + e] = v;
+    a.usage[v] = now;
+    slotOf[e] = v;
+  }
+  for (int i = tid; i < nU; i += nt) a.recency[base + U[i]] = now;
+  __syncthreads();
+
+  // 6. outputs
+  for (int i = tid; i < n; i += nt) a.slot_ids[i] = slotOf[a.ids[i]];
+  for (int i = tid; i < a.max_list; i += nt) {
+    a.fetch_fid[i] = (i < nf) ? base + fe[i] : -1;
+    a.fetch_slot[i] = (i < nf) ? vs2[i] : -1;
+  }
+  if (tid == 0) {
+    *a.num_fetch = nf;
+    *a.step = now + 1;
+  }
+}
+
+}  // namespace
+}  // namespace ft

@@ -23,14 +23,24 @@ Stream orchestration only: every step is a call into libft_moe.so.
   pool into the cache and B_H that of computing experts in place on the pool.
   The deep-dive notes that the profile prefers the two measured while both
   run at once (they share host memory), and calibrate_frac_q16 does so.
+
+* PrefillLayers runs prefill over consecutive layers through the whole-layer
+  double buffer: layer l's experts in cache slots (l%2)*E .., copied from the
+  pool by the copy engine (ft_moe_fetch_layer, then ft_moe_cache_install) on
+  a second stream while the previous layer computes on the main stream
+  (route -> permute -> grouped experts -> combine); the last two layers stay
+  in the cache and seed decode ("FreeToken 딥다이브", design pattern 1;
+  "FreeToken: 让消费级电脑跑起 284B MoE", sec. 5).  With fewer than 2E slots the
+  buffer is single: each layer is copied after the previous one's experts.
 """
 
 from __future__ import annotations
 
 import ctypes
 
-from . import (FT_DECODE, FT_DECODE_HOST, DeviceCacheState, FtBank, experts_fwd, experts_workspace, fetch,
-               merge_partials, resolve_slots, route, route_workspace)
+from . import (FT_DECODE, FT_DECODE_HOST, FT_PREFILL, DeviceCacheState, FtBank, cache_install, combine, experts_fwd,
+               experts_workspace, fetch, fetch_layer, merge_partials, permute, permute_workspace, resolve_slots, route,
+               route_workspace)
 
 
 def frac_q16_from_bandwidths(b_p: float, b_h: float) -> int:
@@ -178,3 +188,83 @@ def calibrate_frac_q16(pool: FtBank, cache: FtBank, E: int, k: int, n_fetch: int
     res["frac_q16_alone"] = frac_q16_from_bandwidths(res["B_P_alone_GBs"], res["B_H_alone_GBs"])
     res["status"] = int(status.item())
     return res
+
+
+class PrefillLayers:
+    """Buffers, streams and events for prefill of T tokens through a run of
+    layers, each layer's experts loaded whole into the cache's first slots.
+
+    The cache must hold at least E slots (state.S and cache.n_blocks); with
+    2E or more the buffer is double (the next layer's copy overlaps this
+    layer's experts), otherwise single.  Routing, permutation, the grouped
+    experts and the combine are the library's calls; the cache state records
+    every installed layer, so afterwards the last layer (two layers, double
+    buffered) are resident for decode."""
+
+    def __init__(self, state: DeviceCacheState, cache: FtBank, pool: FtBank, E: int, k: int, T: int,
+                 device="cuda"):
+        import torch
+
+        slots = min(state.S, int(cache.n_blocks))
+        if slots < E:
+            raise ValueError(f"prefill needs a whole layer in the cache: {slots} slots < E = {E}")
+        self.state, self.cache, self.pool, self.E, self.k, self.T = state, cache, pool, E, k, T
+        self.n_buf = 2 if slots >= 2 * E else 1
+        H, I = cache.H, cache.I
+        n = T * k
+        i32 = dict(dtype=torch.int32, device=device)
+        self.slot_of = [torch.arange(b * E, (b + 1) * E, **i32) for b in range(self.n_buf)]
+        self.ids = torch.empty((T, k), **i32)
+        self.w = torch.empty((T, k), dtype=torch.float32, device=device)
+        self.route_ws = torch.zeros(route_workspace(T, E), dtype=torch.uint8, device=device)
+        self.perm = torch.empty(n, **i32)
+        self.inv = torch.empty((T, k), **i32)
+        self.offsets = torch.empty(E + 1, **i32)
+        self.xp = torch.empty((n, H), dtype=torch.int16, device=device)
+        self.xp_scale = torch.empty(n, dtype=torch.float32, device=device)
+        self.perm_ws = torch.empty(permute_workspace(T, k, E), dtype=torch.uint8, device=device)
+        self.yp = torch.empty((n, H), dtype=torch.int16, device=device)
+        self.ws = torch.empty(experts_workspace(FT_PREFILL, T, k, H, I, E), dtype=torch.uint8, device=device)
+        self.status = torch.zeros(1, **i32)
+        self.copy_stream = torch.cuda.Stream(device=device)
+        self.ev_loaded = [torch.cuda.Event() for _ in range(self.n_buf)]
+        self.ev_free = [torch.cuda.Event() for _ in range(self.n_buf)]
+
+    def __call__(self, layers, xs, ws_router, outs):
+        """layers: flat-id layer indices in order; xs[i] [T,H] bf16 input of
+        layers[i]; ws_router[i] [E,H] fp32 its router; outs[i] [T,H] bf16 its
+        MoE output.  Enqueues on the current stream (and the copy stream)."""
+        import torch
+
+        main = torch.cuda.current_stream()
+        E, k, T, nb = self.E, self.k, self.T, self.n_buf
+
+        def load(i):
+            b = i % nb
+            if i == 0:
+                self.copy_stream.wait_stream(main)  # the state and slots as earlier work on the stream left them
+            if i >= nb:
+                self.copy_stream.wait_event(self.ev_free[b])  # buffer b's previous layer has run its experts
+            fetch_layer(self.pool, self.cache, layers[i], E, b * E, stream=self.copy_stream)
+            cache_install(self.state, layers[i], b * E, stream=self.copy_stream)
+            self.ev_loaded[b].record(self.copy_stream)
+
+        load(0)
+        for i, layer in enumerate(layers):
+            b = i % nb
+            if nb == 2 and i + 1 < len(layers):
+                load(i + 1)  # copied while this layer computes
+            main.wait_event(self.ev_loaded[b])
+            route(xs[i], ws_router[i], k, self.ids, self.w, self.route_ws, stream=main)
+            permute(self.ids, E, xs[i], self.perm, self.inv, self.offsets, self.xp, self.perm_ws,
+                    dev_status=self.status, stream=main, xp_scale=self.xp_scale)
+            experts_fwd(self.cache, None, layer, E, self.xp, T, k, self.slot_of[b], None, None, self.yp, self.ws,
+                        mode=FT_PREFILL, offsets=self.offsets, dev_status=self.status, stream=main,
+                        x_scale=self.xp_scale)
+            self.ev_free[b].record(main)
+            combine(self.yp, self.inv, self.w, outs[i], stream=main)
+            if nb == 1 and i + 1 < len(layers):
+                load(i + 1)  # single buffer: after this layer's experts
+        main.wait_stream(self.copy_stream)
+        return outs
+
