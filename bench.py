@@ -225,73 +225,62 @@ class DecodeWorkload:
                                device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
 
-    # one pass of the hot path over all layers (enqueue only).  fused: route
-    # and resolve in one launch (ft_moe_route_resolve), then fetch and the
-    # experts -- 4 kernels per layer; otherwise route, resolve, fetch, experts
-    # -- 5 kernels per layer; the same results (tested bit for bit).  `ev`
-    # holds per-layer events: 2 around the experts call of every EXP_EVERY-th
-    # layer (an event node between kernels costs microseconds and breaks the
-    # programmatic launch chain, so the timed graph samples), or one before
-    # each op and one after the last (per_op, the breakdown graph)
+    # one pass of the hot path over all layers (enqueue only): route, resolve,
+    # fetch, experts (two kernels) per layer.  `ev` holds per-layer events: 2
+    # around the experts call of every EXP_EVERY-th layer (an event node
+    # between kernels costs microseconds and breaks the programmatic launch
+    # chain, so the timed graph samples), or 5 around every op of every layer
+    # (per_op, the breakdown graph)
     EXP_EVERY = 8
-    OPS = {True: ["route+resolve", "fetch", "experts"], False: ["route", "resolve", "fetch", "experts"]}
-    KERNELS_PER_LAYER = {True: 4, False: 5}
+    OPS = ["route", "resolve", "fetch", "experts"]
+    KERNELS_PER_LAYER = 5
 
-    def step(self, ev=None, per_op=False, fused=True):
+    def step(self, ev=None, per_op=False):
         ft, cfg, T = self.ft, self.cfg, self.T
-        nops = len(self.OPS[fused])
 
         def mark(l, i):
             if ev is None:
                 return
             if per_op:
                 ev[l][i].record()
-            elif i in (nops - 1, nops) and l % self.EXP_EVERY == 0:
-                ev[l // self.EXP_EVERY][i - nops + 1].record()
+            elif i in (3, 4) and l % self.EXP_EVERY == 0:
+                ev[l // self.EXP_EVERY][i - 3].record()
 
         for l in range(cfg.L):
-            x = self.x_stage[l]
-            i = 0
-            mark(l, i)
-            if fused:
-                ft.route_resolve(x, self.W[l], cfg.k, self.state, l, self.phi, self.ids[l], self.w[l],
-                                 self.slot[l], self.nf[l], self.ff[l], self.fs[l], self.rws, dev_status=self.status)
-            else:
-                ft.route(x, self.W[l], cfg.k, self.ids[l], self.w[l], self.rws)
-                i += 1
-                mark(l, i)
-                ft.resolve_slots(self.state, l, self.ids[l], self.phi, self.slot[l], self.nf[l], self.ff[l],
-                                 self.fs[l], self.status)
-            i += 1
-            mark(l, i)
+            mark(l, 0)
+            ft.route(self.x_stage[l], self.W[l], cfg.k, self.ids[l], self.w[l], self.rws)
+            mark(l, 1)
+            ft.resolve_slots(self.state, l, self.ids[l], self.phi, self.slot[l], self.nf[l], self.ff[l],
+                             self.fs[l], self.status)
+            mark(l, 2)
             ft.fetch(self.pool_b, self.cache_b, self.nf[l], self.ff[l], self.fs[l], self.status)
-            i += 1
-            mark(l, i)
-            ft.experts_fwd(self.cache_b, self.pool_b, l, cfg.E, x, T, cfg.k, self.slot[l],
+            mark(l, 3)
+            ft.experts_fwd(self.cache_b, self.pool_b, l, cfg.E, self.x_stage[l], T, cfg.k, self.slot[l],
                            self.ids[l], self.w[l], self.out[l], self.ews, dev_status=self.status)
-            mark(l, i + 1)
+            mark(l, 4)
 
-    def capture(self, fused=True):
+    def capture(self):
         """Two graphs of one step: `graph` (timed) with events only around the
-        experts calls, `graph_ops` with events around every op (breakdown)."""
+        experts calls, `graph_ops` with events around every op (breakdown).
+        Each recapture replaces both graphs and their events together."""
         import torch
 
         def events(n, rows):
             return [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(n)]
                     for _ in range(rows)]
 
-        self.fused = fused
+        self.graph = self.graph_ops = None  # before their events go
         self.ev_exp = events(2, (self.cfg.L + self.EXP_EVERY - 1) // self.EXP_EVERY)
-        self.ev_ops = events(len(self.OPS[fused]) + 1, self.cfg.L)
+        self.ev_ops = events(len(self.OPS) + 1, self.cfg.L)
         self.x_stage.copy_(self.x_all[0])
-        self.step(fused=fused)  # eager warm-up (attributes, lazy init) before capture
+        self.step()  # eager warm-up (attributes, lazy init) before capture
         torch.cuda.synchronize()
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph):
-            self.step(self.ev_exp, fused=fused)
+            self.step(self.ev_exp)
         self.graph_ops = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph_ops):
-            self.step(self.ev_ops, per_op=True, fused=fused)
+            self.step(self.ev_ops, per_op=True)
         torch.cuda.synchronize()
 
     def settle(self, steps: int, seed: int = 1):
@@ -336,7 +325,7 @@ class DecodeWorkload:
         outside the timed region."""
         import torch
 
-        names = self.OPS[self.fused]
+        names = self.OPS
         runs = []
         for i in range(reps):
             self.x_stage.copy_(self.x_all[(first + i) % self.x_all.shape[0]])
@@ -752,8 +741,6 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--tokens", type=int, default=1, help="decode batch (1 or 8)")
     ap.add_argument("--phi", type=int, default=65536, help="frac_q16 of the q* split")
-    ap.add_argument("--step", choices=["fused", "separate"], default="fused",
-                    help="fused: ft_moe_route_resolve per layer; separate: ft_moe_route + ft_moe_resolve_slots")
     ap.add_argument("--settle", type=int, default=512,
                     help="untimed steps on fresh tokens before timing, so the cache reaches steady state")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -800,7 +787,6 @@ def main():
 
     # device-timed steps, e2e steps, per-op breakdown, fetch statistics
     n_steps = args.warmup + 2 * args.steps + 5 + 20
-    fused = args.step == "fused"
     results = {}
     batches = [args.tokens] + ([args.extra_batch] if args.extra_batch and args.extra_batch != args.tokens else [])
     wl = None
@@ -809,7 +795,7 @@ def main():
             wl = DecodeWorkload(cfg, T, args.phi, n_steps, device, log)
         else:
             wl = reshape_workload(wl, T, n_steps)
-        wl.capture(fused=fused)
+        wl.capture()
         wl.settle(args.settle)
         clocks = ClockSampler(local) if bi == 0 else None
         secs = time_device(wl, args.steps, args.warmup, reduce_fn, world, clocks)
@@ -872,7 +858,7 @@ def main():
         cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"{n} single-layer calls of {args.tokens} token(s) (route, resolve, fp64 experts) "
                          f"on 2 of 40 layers, {dt:.1f} s, single-threaded C++"}
-    launches_per_step = cfg.L * DecodeWorkload.KERNELS_PER_LAYER[fused]
+    launches_per_step = cfg.L * DecodeWorkload.KERNELS_PER_LAYER
     line = {
         "metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["secs"] / args.steps * 1e3, "higher_is_better": True,
@@ -894,9 +880,7 @@ def main():
             "model_tokens_per_s": r["value"] / cfg.L,
             "per_op_us_per_step": kt,
             "expert_bytes_per_step": r["ebytes"],
-            "step": ("per layer: ft_moe_route_resolve (route and resolve, one kernel), ft_moe_fetch, "
-                     "ft_moe_experts_fwd (two kernels)") if fused else
-                    "per layer: ft_moe_route, ft_moe_resolve_slots, ft_moe_fetch, ft_moe_experts_fwd (two kernels)",
+            "step": "per layer: ft_moe_route, ft_moe_resolve_slots, ft_moe_fetch, ft_moe_experts_fwd (two kernels)",
             "settle_steps": args.settle,
             "fetched_experts_per_step": r["nfetch"],
             "host_path_pairs_per_step": r["host_pairs"],

@@ -13,8 +13,6 @@
  *   ft_moe_combine        top-k weighted sum of permuted expert rows (prefill)
  *   ft_moe_split_q16      the q* rule alone, batched (the resolve kernel runs
  *                         the same device function)
- *   ft_moe_route_resolve  route + resolve in one launch (decode; bit-identical
- *                         to the two calls)
  *
  * Sources, by page title and section:
  *   "FreeToken 딥다이브" (fiv.co.kr) -- design pattern 1 (whole-layer double
@@ -168,24 +166,6 @@ FT_API size_t ft_moe_route_workspace(int32_t T, int32_t E);
 FT_API ft_status ft_moe_route(const uint16_t* x, int32_t T, int32_t H, const float* w_router,
                        int32_t E, int32_t k, int32_t renorm, int32_t* topk_ids, float* topk_w,
                        void* ws, size_t ws_bytes, void* stream);
-
-/*
- * ft_moe_route_resolve -- ft_moe_route followed by ft_moe_resolve_slots in
- * one launch, for decode (T <= 16): the router's last CTA, once it has the
- * top-k of every token, resolves them against the slot cache itself (the
- * FreeToken paper post, sec. 6: the decisions stay in GPU data, in one
- * kernel; the deep-dive's design pattern 2: no host round trip inside the
- * decode graph).  Arguments, outputs, state update, limits and errors are
- * those of the two calls (ws as for ft_moe_route; state_host->E must equal
- * E); the results are bit-identical to the two calls in a row.  T == 0 runs
- * the resolve alone (it still advances the step).
- */
-FT_API ft_status ft_moe_route_resolve(const uint16_t* x, int32_t T, int32_t H, const float* w_router,
-                                      int32_t E, int32_t k, int32_t renorm, const ft_cache_state* state_host,
-                                      int32_t layer, int32_t frac_q16, int32_t* topk_ids, float* topk_w,
-                                      int32_t* slot_ids, int32_t* num_fetch, int32_t* fetch_fid,
-                                      int32_t* fetch_slot, int32_t max_list, void* ws, size_t ws_bytes,
-                                      int32_t* dev_status, void* stream);
 
 /*
  * ft_moe_split_q16 -- the bandwidth-matched q* rule in Q16 fixed point

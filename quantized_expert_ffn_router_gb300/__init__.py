@@ -52,8 +52,6 @@ _SIGS = {
     "ft_moe_get_status": (_I32, [_V, _V]),
     "ft_moe_route_workspace": (_SZ, [_I32, _I32]),
     "ft_moe_route": (_I32, [_V, _I32, _I32, _V, _I32, _I32, _I32, _V, _V, _V, _SZ, _V]),
-    "ft_moe_route_resolve": (_I32, [_V, _I32, _I32, _V, _I32, _I32, _I32, _V, _I32, _I32, _V, _V, _V, _V, _V,
-                                    _V, _I32, _V, _SZ, _V, _V]),
     "ft_moe_split_q16": (_I32, [_V, _I32, _I32, _V, _V]),
     "ft_moe_resolve_slots": (_I32, [_V, _I32, _V, _I32, _I32, _I32, _V, _V, _V, _V, _I32, _V, _V]),
     "ft_moe_fetch": (_I32, [_V, _V, _V, _V, _V, _I32, _V, _V]),
@@ -168,20 +166,6 @@ def route(x, w_router, k: int, topk_ids, topk_w, ws, renorm: bool = False, strea
     E = w_router.shape[0]
     _check(load().ft_moe_route(_ptr(x), T, H, _ptr(w_router), E, k, int(bool(renorm)), _ptr(topk_ids),
                                _ptr(topk_w), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
-
-
-def route_resolve(x, w_router, k: int, state: DeviceCacheState, layer: int, frac_q16: int, topk_ids, topk_w,
-                  slot_ids, num_fetch, fetch_fid, fetch_slot, ws, dev_status=None, renorm: bool = False,
-                  stream=None):
-    """route then resolve_slots, in one launch (T <= 16)."""
-    T, H = x.shape
-    E = w_router.shape[0]
-    st = state.struct()
-    _check(load().ft_moe_route_resolve(_ptr(x), T, H, _ptr(w_router), E, k, int(bool(renorm)), ctypes.byref(st),
-                                       layer, int(frac_q16), _ptr(topk_ids), _ptr(topk_w), _ptr(slot_ids),
-                                       _ptr(num_fetch), _ptr(fetch_fid), _ptr(fetch_slot), fetch_fid.numel(),
-                                       _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status),
-                                       _stream(stream)))
 
 
 def split_q16(num_missing, frac_q16: int, num_fetch, stream=None):

@@ -1,6 +1,6 @@
 // ft_resolve.cuh -- the resolve of a layer's top-k ids against the global
-// slot cache, as a device function that one CTA runs: the resolve kernel
-// (cache.cu) and the fused route + resolve kernel (route.cu) share it.
+// slot cache, as a device function that one CTA runs (the resolve kernel in
+// cache.cu), with its host-side argument checks.
 //
 // Sources: "FreeToken 딥다이브" (fiv.co.kr), design patterns 2, 3, 5;
 // "FreeToken: 让消费级电脑跑起 284B MoE" (fengjutian.github.io), sec. 6 (one

@@ -8,11 +8,8 @@
 // per expert row) and a tiled SIMT GEMM for long prompts.  Then one warp per
 // token does the softmax and the top-k selection, launched as a programmatic
 // dependent so it is resident before the logits are done.
-#include <algorithm>
-
 #include "ft_async.cuh"
 #include "ft_common.cuh"
-#include "ft_resolve.cuh"
 
 namespace ft {
 namespace {
@@ -20,9 +17,6 @@ namespace {
 constexpr int kGemvMaxT = 16;
 constexpr int kRouteMaxK = 32;
 constexpr int kRouteMaxE = 4096;
-// every CTA of the fused route + resolve kernel carries the resolve's shared
-// memory: its victim search is staged only while that stays small
-constexpr size_t kRouteStageCap = 64 * 1024;
 
 size_t route_logits_bytes(int T, int E) {
   return (static_cast<size_t>(T) * E * sizeof(float) + 255) & ~static_cast<size_t>(255);
@@ -36,17 +30,13 @@ size_t route_logits_bytes(int T, int E) {
 __device__ __forceinline__ void topk_warp(const float* __restrict__ l, float* ls, int E, int k, int renorm,
                                           int32_t* __restrict__ ids_t, float* __restrict__ wts_t);
 
-// With RESOLVE, the last CTA then also resolves the new ids against the slot
-// cache (the resolve kernel's work, ft_resolve.cuh), so a decode layer's
-// routing decisions take one launch: ra.ids must be `ids`.
-template <int TMAX, bool RESOLVE>
+template <int TMAX>
 __global__ void __launch_bounds__(256) route_rows_kernel(const uint16_t* __restrict__ x, int T, int H,
                                                          const float* __restrict__ W, int E,
                                                          float* __restrict__ logits, unsigned* counter,
-                                                         int k, int renorm, int32_t* ids,
-                                                         float* __restrict__ wts, ResolveArgs ra) {
-  // last CTA: [min(T, 8)][E] logits, then (RESOLVE) the resolve's arrays
-  extern __shared__ __align__(16) float lsm[];
+                                                         int k, int renorm, int32_t* __restrict__ ids,
+                                                         float* __restrict__ wts) {
+  extern __shared__ float lsm[];  // last CTA: [min(T, 8)][E] logits
   __shared__ float part[8][TMAX];
   __shared__ int s_last;
   pdl_wait();               // x may come from the previous kernel in the stream
@@ -113,10 +103,6 @@ __global__ void __launch_bounds__(256) route_rows_kernel(const uint16_t* __restr
   for (int t = warp; t < T; t += 8)
     topk_warp(logits + static_cast<size_t>(t) * E, lsm + static_cast<size_t>(warp) * E, E, k, renorm,
               ids + static_cast<size_t>(t) * k, wts + static_cast<size_t>(t) * k);
-  if constexpr (RESOLVE) {
-    __syncthreads();  // every token's ids are written (and visible to the CTA)
-    resolve_block(ra, reinterpret_cast<unsigned char*>(lsm));
-  }
 }
 
 // Tiled SIMT GEMM: a 64-token x 64-expert tile per CTA, 256 threads with 4x4
@@ -277,26 +263,19 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
 }
 
 
-// Host: launch route_rows_kernel (T <= kGemvMaxT); with `ra`, the fused
-// route + resolve form, whose resolve needs `rsmem` bytes of the dynamic
-// shared memory (the logits' part is free again by then).  The arrival
-// counter follows the logits in ws.
+// Host: launch route_rows_kernel (T <= kGemvMaxT), logits and top-k in one
+// kernel; the arrival counter follows the logits in ws.
 ft_status launch_rows(const uint16_t* x, int T, int H, const float* W, int E, int k, int renorm,
-                      int32_t* ids, float* wts, void* ws, const ResolveArgs* ra, size_t rsmem, cudaStream_t s) {
+                      int32_t* ids, float* wts, void* ws, cudaStream_t s) {
   float* logits = static_cast<float*>(ws);
   unsigned* counter = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + route_logits_bytes(T, E));
-  size_t smem = static_cast<size_t>(T < 8 ? T : 8) * E * sizeof(float);
-  if (ra != nullptr) smem = std::max(smem, rsmem);
+  const size_t smem = static_cast<size_t>(T < 8 ? T : 8) * E * sizeof(float);
   static bool attr = false;
   if (!attr) {
     const int mx = 8 * kRouteMaxE * static_cast<int>(sizeof(float));
-    cudaFuncSetAttribute(route_rows_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-    cudaFuncSetAttribute(route_rows_kernel<4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-    cudaFuncSetAttribute(route_rows_kernel<16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-    const int mr = static_cast<int>(std::max(static_cast<size_t>(mx), kResSmemCap));
-    cudaFuncSetAttribute(route_rows_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, mr);
-    cudaFuncSetAttribute(route_rows_kernel<4, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, mr);
-    cudaFuncSetAttribute(route_rows_kernel<16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, mr);
+    cudaFuncSetAttribute(route_rows_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    cudaFuncSetAttribute(route_rows_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    cudaFuncSetAttribute(route_rows_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
     attr = true;
   }
   cudaLaunchConfig_t rc = {};
@@ -309,27 +288,17 @@ ft_status launch_rows(const uint16_t* x, int T, int H, const float* W, int E, in
   at[0].val.programmaticStreamSerializationAllowed = 1;
   rc.attrs = at;
   rc.numAttrs = 1;
-  ResolveArgs r = {};
-  if (ra != nullptr) r = *ra;
   cudaError_t le;
-  if (ra == nullptr) {
-    if (T <= 1)
-      le = cudaLaunchKernelEx(&rc, route_rows_kernel<1, false>, x, T, H, W, E, logits, counter, k, renorm, ids, wts, r);
-    else if (T <= 4)
-      le = cudaLaunchKernelEx(&rc, route_rows_kernel<4, false>, x, T, H, W, E, logits, counter, k, renorm, ids, wts, r);
-    else
-      le = cudaLaunchKernelEx(&rc, route_rows_kernel<16, false>, x, T, H, W, E, logits, counter, k, renorm, ids, wts, r);
-  } else {
-    if (T <= 1)
-      le = cudaLaunchKernelEx(&rc, route_rows_kernel<1, true>, x, T, H, W, E, logits, counter, k, renorm, ids, wts, r);
-    else if (T <= 4)
-      le = cudaLaunchKernelEx(&rc, route_rows_kernel<4, true>, x, T, H, W, E, logits, counter, k, renorm, ids, wts, r);
-    else
-      le = cudaLaunchKernelEx(&rc, route_rows_kernel<16, true>, x, T, H, W, E, logits, counter, k, renorm, ids, wts, r);
-  }
+  if (T <= 1)
+    le = cudaLaunchKernelEx(&rc, route_rows_kernel<1>, x, T, H, W, E, logits, counter, k, renorm, ids, wts);
+  else if (T <= 4)
+    le = cudaLaunchKernelEx(&rc, route_rows_kernel<4>, x, T, H, W, E, logits, counter, k, renorm, ids, wts);
+  else
+    le = cudaLaunchKernelEx(&rc, route_rows_kernel<16>, x, T, H, W, E, logits, counter, k, renorm, ids, wts);
   if (le != cudaSuccess) return fail(FT_ERR_CUDA, "route: %s", cudaGetErrorString(le));
-  return launch_check(ra != nullptr ? "route_resolve" : "route");
+  return launch_check("route");
 }
+
 }  // namespace
 }  // namespace ft
 
@@ -356,7 +325,7 @@ ft_status ft_moe_route(const uint16_t* x, int32_t T, int32_t H, const float* w_r
   cudaStream_t s = ft::as_stream(stream);
   float* logits = static_cast<float*>(ws);
   if (T <= ft::kGemvMaxT)  // logits and top-k in one kernel
-    return ft::launch_rows(x, T, H, w_router, E, k, renorm, topk_ids, topk_w, ws, nullptr, 0, s);
+    return ft::launch_rows(x, T, H, w_router, E, k, renorm, topk_ids, topk_w, ws, s);
   {
     FT_REQUIRE(H % ft::kTK == 0, "route: H %d must be a multiple of 32 for T > 16", H);
     dim3 grid((E + ft::kTN - 1) / ft::kTN, (T + ft::kTM - 1) / ft::kTM);
@@ -381,33 +350,6 @@ ft_status ft_moe_route(const uint16_t* x, int32_t T, int32_t H, const float* w_r
   cudaError_t e = cudaLaunchKernelEx(&cfg, ft::route_topk_kernel, lg, T, E, k, renorm, topk_ids, topk_w);
   if (e != cudaSuccess) return ft::fail(FT_ERR_CUDA, "route topk: %s", cudaGetErrorString(e));
   return ft::launch_check("route topk");
-}
-
-ft_status ft_moe_route_resolve(const uint16_t* x, int32_t T, int32_t H, const float* w_router, int32_t E,
-                               int32_t k, int32_t renorm, const ft_cache_state* state_host, int32_t layer,
-                               int32_t frac_q16, int32_t* topk_ids, float* topk_w, int32_t* slot_ids,
-                               int32_t* num_fetch, int32_t* fetch_fid, int32_t* fetch_slot, int32_t max_list,
-                               void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
-  FT_REQUIRE(T >= 0 && T <= ft::kGemvMaxT, "route_resolve: T %d outside [0, %d]", T, ft::kGemvMaxT);
-  FT_REQUIRE(E >= 1 && E <= 4096, "route_resolve: E %d outside [1, 4096]", E);
-  FT_REQUIRE(k >= 1 && k <= E && k <= ft::kRouteMaxK, "route_resolve: k %d outside [1, min(E, 32)]", k);
-  FT_REQUIRE(H >= 8 && H % 8 == 0, "route_resolve: H %d must be a positive multiple of 8", H);
-  ft::ResolveArgs ra;
-  size_t rsmem = 0;
-  ft_status ps = ft::resolve_prepare(state_host, layer, topk_ids, T, k, frac_q16, slot_ids, num_fetch, fetch_fid,
-                                     fetch_slot, max_list, dev_status, "route_resolve", ft::kRouteStageCap, &ra,
-                                     &rsmem);
-  if (ps != FT_OK) return ps;
-  FT_REQUIRE(state_host->E == E, "route_resolve: state E %d != E %d", state_host->E, E);
-  if (T == 0)  // nothing to route; the resolve still takes its step, as ft_moe_resolve_slots does
-    return ft_moe_resolve_slots(state_host, layer, topk_ids, 0, k, frac_q16, slot_ids, num_fetch, fetch_fid,
-                                fetch_slot, max_list, dev_status, stream);
-  FT_REQUIRE(x && w_router && topk_w && ws, "route_resolve: NULL pointer");
-  FT_REQUIRE(ws_bytes >= ft_moe_route_workspace(T, E), "route_resolve: workspace %zu < %zu", ws_bytes,
-             ft_moe_route_workspace(T, E));
-  FT_REQUIRE(reinterpret_cast<uintptr_t>(x) % 16 == 0 && reinterpret_cast<uintptr_t>(w_router) % 16 == 0,
-             "route_resolve: x and w_router must be 16-byte aligned");
-  return ft::launch_rows(x, T, H, w_router, E, k, renorm, topk_ids, topk_w, ws, &ra, rsmem, ft::as_stream(stream));
 }
 
 }  // extern "C"

@@ -93,27 +93,6 @@ def test_host_validation_without_gpu(ft):
     assert ft.load().ft_status_string(ft.FT_ERR_BAD_ID).decode() == "expert id out of range"
 
 
-def test_route_resolve_refuses_on_host(ft):
-    """ft_moe_route_resolve checks its arguments on the host: the route's and
-    the resolve's limits and the state's E (nothing is dereferenced)."""
-    lib = ft.load()
-    V = ctypes.c_void_p
-    dummy = V(16)
-    st = ft.FtCacheState(2, 8, 4, dummy, dummy, dummy, dummy, dummy)
-
-    def rr(T=1, E=8, k=2, layer=0, phi=100, ml=4, H=64):
-        return lib.ft_moe_route_resolve(dummy, T, H, dummy, E, k, 0, ctypes.byref(st), layer, phi, dummy, dummy,
-                                        dummy, dummy, dummy, dummy, ml, dummy, 1 << 20, None, None)
-
-    assert rr(T=17) == ft.FT_ERR_INVALID           # more tokens than one router launch takes
-    assert rr(E=16) == ft.FT_ERR_INVALID           # router E differs from the state's
-    assert rr(k=9) == ft.FT_ERR_INVALID
-    assert rr(layer=2) == ft.FT_ERR_INVALID
-    assert rr(phi=65537) == ft.FT_ERR_INVALID
-    assert rr(ml=1) == ft.FT_ERR_INVALID           # fetch list shorter than min(T*k, S)
-    assert rr(H=60) == ft.FT_ERR_INVALID
-    assert "route_resolve" in lib.ft_last_error().decode()
-
 
 def test_cache_rebuild_refusals_without_gpu(ft):
     """Every refusal is decided on the host, before anything is enqueued."""

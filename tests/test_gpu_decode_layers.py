@@ -1,13 +1,8 @@
-"""GPU: ft_moe_route_resolve (route and resolve in one launch) gives the
-separate calls' results.
-
-It is checked against ft_moe_route followed by ft_moe_resolve_slots and
-against the CPU oracle, call after call on an evolving cache state: ids, slot
-ids, fetch lists and every state array bit-exact, weights bit-identical to the
-separate router.  Then whole decode layers (route_resolve, fetch, experts
-against route, resolve, fetch, experts) run side by side over many steps and
-layers, also replayed from a CUDA graph: outputs, cache bytes and states
-bit-identical, the last layer call within tolerance of the oracle."""
+"""GPU: whole decode layers (route, resolve, fetch, experts) over many steps
+and layers on an evolving slot cache, eager and replayed from one CUDA graph
+(the programmatic launch chain across layers): outputs, cache bytes and
+states bit-identical between the two, and the last layer call within
+tolerance of the oracle."""
 
 import numpy as np
 import pytest
@@ -15,7 +10,7 @@ import torch
 
 import oracle
 import synth
-from gpu_helpers import assert_close, gapped_tokens, oracle_pairs_output
+from gpu_helpers import assert_close, oracle_pairs_output
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -38,16 +33,6 @@ def _dev_state(ft, host):
     return st
 
 
-def _same_state(dev, host):
-    S = host.S
-    assert np.array_equal(dev.map.cpu().numpy(), host.map)
-    assert np.array_equal(dev.recency.cpu().numpy(), host.recency)
-    assert int(dev.step.item()) == int(host.step[0])
-    if S:
-        assert np.array_equal(dev.slot_owner[:S].cpu().numpy(), host.slot_owner)
-        assert np.array_equal(dev.usage[:S].cpu().numpy(), host.usage)
-
-
 def _seeded_host_state(L, E, S, seed, filled=0.5):
     host = oracle.CacheState(L, E, S)
     rng = np.random.default_rng(seed)
@@ -57,58 +42,6 @@ def _seeded_host_state(L, E, S, seed, filled=0.5):
         host.seed_slots(list(fids), usages=list(rng.integers(0, 50, n)))
     host.step[0] = 60
     return host
-
-
-# ------------------------------------------------------------ route_resolve
-@pytest.mark.parametrize("name,T,S", [("tiny", 8, 6), ("tiny", 2, 6), ("d35b", 1, 64), ("d35b", 8, 200),
-                                      ("flash", 1, 100), ("d35b", 4, 0), ("d35b", 8, 9000)])
-def test_route_resolve_matches_separate_calls_and_oracle(cuda_lib, name, T, S):
-    """The 9000-slot cache is too large for the fused kernel to stage its
-    victim search in shared memory (the separate resolve kernel does)."""
-    ft = cuda_lib
-    cfg = synth.get_config(name)
-    L, E, k = min(cfg.L, 3), cfg.E, cfg.k
-    # about half of the flat ids resident, so that calls miss and fetch
-    host = _seeded_host_state(L, E, S, seed=T * 7 + S, filled=min(0.5, 0.5 * L * E / max(S, 1)))
-    dev_f, dev_s = _dev_state(ft, host), _dev_state(ft, host)
-    Ws = [synth.router_weights(cfg.seed, l, E, cfg.H, cfg.router_std, zipf_bias=cfg.zipf) for l in range(L)]
-    Wd = [_t(W) for W in Ws]
-    ws_f = torch.zeros(ft.route_workspace(T, E), dtype=torch.uint8, device=DEV)
-    ws_s = torch.zeros(ft.route_workspace(T, E), dtype=torch.uint8, device=DEV)
-    ml = T * k
-    status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    phis = [65536, 26214, 0, 1, 49152]
-    fetched = 0
-    for it in range(12):
-        layer, phi = it % L, phis[it % len(phis)]
-        x, _ = gapped_tokens(cfg.seed, f"fused-rr-{name}-{T}-{it}", T, cfg.H, Ws[layer], k, cfg.gap,
-                             bias_feature=cfg.zipf is not None)
-        ids_o, w_o = oracle.route(x, Ws[layer], k)
-        o_sl, o_nf, o_ff, o_fs = oracle.resolve(host, layer, ids_o, phi, ml)
-        xd = _t(x)
-        f = dict(ids=_i32(T, k), w=torch.empty((T, k), device=DEV), sl=_i32(T, k), nf=_i32(1), ff=_i32(ml),
-                 fs=_i32(ml))
-        s = dict(ids=_i32(T, k), w=torch.empty((T, k), device=DEV), sl=_i32(T, k), nf=_i32(1), ff=_i32(ml),
-                 fs=_i32(ml))
-        ft.route_resolve(xd, Wd[layer], k, dev_f, layer, phi, f["ids"], f["w"], f["sl"], f["nf"], f["ff"],
-                         f["fs"], ws_f, dev_status=status)
-        ft.route(xd, Wd[layer], k, s["ids"], s["w"], ws_s)
-        ft.resolve_slots(dev_s, layer, s["ids"], phi, s["sl"], s["nf"], s["ff"], s["fs"], status)
-        torch.cuda.synchronize()
-        for key in f:
-            assert torch.equal(f[key], s[key]), (it, key)
-        assert np.array_equal(f["ids"].cpu().numpy(), ids_o), it
-        np.testing.assert_allclose(f["w"].cpu().numpy(), w_o, rtol=2e-5, atol=1e-7)
-        assert np.array_equal(f["sl"].cpu().numpy(), o_sl), it
-        assert int(f["nf"].item()) == o_nf, it
-        assert np.array_equal(f["ff"].cpu().numpy(), o_ff) and np.array_equal(f["fs"].cpu().numpy(), o_fs), it
-        fetched += o_nf
-    assert ft.get_status(status) == 0
-    assert not ws_f[-256:].any()  # the arrival counter is back at zero
-    _same_state(dev_f, host)
-    _same_state(dev_s, host)
-    if S > 0:
-        assert fetched > 0  # the general resolve path (with victims) ran, not only the one-warp path
 
 
 # ------------------------------------------------------------ whole layers
@@ -134,8 +67,7 @@ def _cache_from_state(host, pool, stride):
 
 
 class _Layer:
-    """One decode layer's buffers; `fused` runs route_resolve, fetch, experts,
-    otherwise route, resolve, fetch, experts."""
+    """One decode layer's buffers: route, resolve, fetch, experts."""
 
     def __init__(self, ft, T, k, E, H, I, ml):
         self.ft = ft
@@ -145,21 +77,17 @@ class _Layer:
         self.ews = torch.zeros(ft.experts_workspace(ft.FT_DECODE, T, k, H, I, E), dtype=torch.uint8, device=DEV)
         self.status = torch.zeros(1, dtype=torch.int32, device=DEV)
 
-    def __call__(self, fused, st, cache_b, pool_b, layer, E, k, phi, x, W, out):
+    def __call__(self, st, cache_b, pool_b, layer, E, k, phi, x, W, out):
         ft, T = self.ft, x.shape[0]
-        if fused:
-            ft.route_resolve(x, W, k, st, layer, phi, self.ids, self.w, self.sl, self.nf, self.ff, self.fs,
-                             self.rws, dev_status=self.status)
-        else:
-            ft.route(x, W, k, self.ids, self.w, self.rws)
-            ft.resolve_slots(st, layer, self.ids, phi, self.sl, self.nf, self.ff, self.fs, self.status)
+        ft.route(x, W, k, self.ids, self.w, self.rws)
+        ft.resolve_slots(st, layer, self.ids, phi, self.sl, self.nf, self.ff, self.fs, self.status)
         ft.fetch(pool_b, cache_b, self.nf, self.ff, self.fs, self.status)
         ft.experts_fwd(cache_b, pool_b, layer, E, x, T, k, self.sl, self.ids, self.w, out, self.ews,
                        dev_status=self.status)
 
 
 @pytest.mark.parametrize("name,T,S,phi", [("tiny", 8, 6, 26214), ("d35b", 1, 48, 65536), ("d35b", 8, 48, 49160)])
-def test_fused_layers_equal_separate_layers_and_replay(cuda_lib, name, T, S, phi):
+def test_layers_eager_graph_and_oracle(cuda_lib, name, T, S, phi):
     ft = cuda_lib
     cfg = synth.get_config(name)
     L, E, k, H, I = 2, cfg.E, cfg.k, cfg.H, cfg.I
@@ -174,7 +102,7 @@ def test_fused_layers_equal_separate_layers_and_replay(cuda_lib, name, T, S, phi
     Ws = [_t(synth.router_weights(cfg.seed, l, E, H, cfg.router_std, zipf_bias=cfg.zipf)) for l in range(L)]
     layers = [_Layer(ft, T, k, E, H, I, T * k) for _ in range(2)]
     steps = 6
-    xs = synth.normal_bf16(synth.stream_key(cfg.seed, "fused-layers", T), (steps, L, T, H))
+    xs = synth.normal_bf16(synth.stream_key(cfg.seed, "decode-layers", T), (steps, L, T, H))
     if cfg.zipf is not None:
         xs[..., 0] = synth.bf16_bits(np.array([1.0], np.float32))[0]
     x_all = _t(xs)
@@ -182,7 +110,7 @@ def test_fused_layers_equal_separate_layers_and_replay(cuda_lib, name, T, S, phi
     for s in range(steps):
         for l in range(L):
             for v in range(2):
-                layers[v](v == 0, states[v], cbs[v], pb, l, E, k, phi, x_all[s, l], Ws[l], outs[v][s, l])
+                layers[v](states[v], cbs[v], pb, l, E, k, phi, x_all[s, l], Ws[l], outs[v][s, l])
     torch.cuda.synchronize()
     # the last layer call against the oracle (every pair computed, from the cache or the pool):
     # its ids and weights are still in the layer's buffers
@@ -198,7 +126,8 @@ def test_fused_layers_equal_separate_layers_and_replay(cuda_lib, name, T, S, phi
                  (states[0].usage, states[1].usage), (states[0].recency, states[1].recency),
                  (states[0].step, states[1].step)]:
         assert torch.equal(a, b)
-    # the fused layers replayed from one CUDA graph continue both histories alike
+    # two identical histories so far; now history 0 continues from one CUDA graph of
+    # all layers, history 1 eagerly
     x_stage = torch.empty((L, T, H), dtype=torch.int16, device=DEV)
     g_out = torch.empty((L, T, H), dtype=torch.float32, device=DEV)
     x_stage.copy_(x_all[0])
@@ -209,7 +138,7 @@ def test_fused_layers_equal_separate_layers_and_replay(cuda_lib, name, T, S, phi
     with torch.cuda.stream(side):
         with torch.cuda.graph(g, stream=side):
             for l in range(L):
-                layers[0](True, states[0], cbs[0], pb, l, E, k, phi, x_stage[l], Ws[l], g_out[l])
+                layers[0](states[0], cbs[0], pb, l, E, k, phi, x_stage[l], Ws[l], g_out[l])
     torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
     e_out = torch.empty((L, T, H), dtype=torch.float32, device=DEV)
@@ -217,7 +146,7 @@ def test_fused_layers_equal_separate_layers_and_replay(cuda_lib, name, T, S, phi
         x_stage.copy_(x_all[(s + 2) % steps])
         g.replay()
         for l in range(L):
-            layers[1](False, states[1], cbs[1], pb, l, E, k, phi, x_stage[l], Ws[l], e_out[l])
+            layers[1](states[1], cbs[1], pb, l, E, k, phi, x_stage[l], Ws[l], e_out[l])
         torch.cuda.synchronize()
         assert torch.equal(g_out, e_out), s
     assert torch.equal(caches[0], caches[1])
