@@ -37,8 +37,8 @@ METRIC = "MoE-layer tokens/s; decode expert-weight HBM GB/s; prefill grouped-GEM
 # DRAM bytes (read + write) of one experts call (gate/up + down kernels) from
 # an ncu capture of the same kernels on this workload's shape, L2 kept
 # between the kernels (`bench.py --case decode --tokens T` under
-# `ncu --cache-control none`; profiles/decode_experts_d35b_T1.md)
-TRAFFIC_PER_CALL = {1: 13_376_256, 8: 103_728_640}
+# `ncu --cache-control none`, summarised under profiles/)
+TRAFFIC_PER_CALL = {1: 13_377_280, 8: 103_692_544}
 UNIT = "MoE-layer tokens/s"
 
 

@@ -337,7 +337,7 @@ def test_experts_decode_single_token_reuses_workspace(cuda_lib, name):
         assert_close(got, ref, f"{name} call {call}")
 
 
-@pytest.mark.parametrize("name,T", [("tiny", 8), ("d35b", 8), ("flash", 1)])
+@pytest.mark.parametrize("name,T", [("tiny", 8), ("d35b", 8), ("d35b", 1), ("flash", 1)])
 def test_experts_decode_masked_partial_plus_host_partial(cuda_lib, name, T):
     """Masked mode (no pool): the GPU partial over cached pairs plus the
     oracle's partial over the -1 pairs equals the full output (each pair once)."""
