@@ -27,8 +27,8 @@ size_t route_logits_bytes(int T, int E) {
 // once; partial sums meet in shared memory (fixed order).  The last CTA to
 // finish (an arrival counter after the logits in the workspace, back at zero
 // when the call ends) then runs the softmax and top-k of every token.
-__device__ __forceinline__ void topk_warp(const float* __restrict__ l, float* ls, int E, int k, int renorm,
-                                          int32_t* __restrict__ ids_t, float* __restrict__ wts_t);
+__device__ __forceinline__ void topk_any(const float* __restrict__ l, float* ls, int E, int k, int renorm,
+                                         int32_t* __restrict__ ids_t, float* __restrict__ wts_t);
 
 template <int TMAX>
 __global__ void __launch_bounds__(256) route_rows_kernel(const uint16_t* __restrict__ x, int T, int H,
@@ -101,8 +101,8 @@ __global__ void __launch_bounds__(256) route_rows_kernel(const uint16_t* __restr
   if (!s_last) return;
   __threadfence();  // every other CTA's logits after their arrivals
   for (int t = warp; t < T; t += 8)
-    topk_warp(logits + static_cast<size_t>(t) * E, lsm + static_cast<size_t>(warp) * E, E, k, renorm,
-              ids + static_cast<size_t>(t) * k, wts + static_cast<size_t>(t) * k);
+    topk_any(logits + static_cast<size_t>(t) * E, lsm + static_cast<size_t>(warp) * E, E, k, renorm,
+             ids + static_cast<size_t>(t) * k, wts + static_cast<size_t>(t) * k);
 }
 
 // Tiled SIMT GEMM: a 64-token x 64-expert tile per CTA, 256 threads with 4x4
@@ -249,6 +249,85 @@ __device__ __forceinline__ void topk_warp(const float* __restrict__ l, float* ls
   }
 }
 
+// The same top-k for E <= 32 * VPL with the token's logits in registers
+// (lane l holds e = l, l+32, ...): each round every lane offers its best
+// untaken logit as an order-preserving 32-bit key, one redux.sync takes the
+// warp's maximum key and a second the lowest expert id among the lanes
+// holding it (ties to the lower id, as above).  The softmax denominator is
+// summed in the same order as topk_warp, so ids and weights are the same.
+// -0 ranks as +0; a NaN logit ranks below every number.
+__device__ __forceinline__ uint32_t order_key(float v) {
+  if (v != v) return 0u;  // NaN: lowest
+  if (v == 0.f) v = 0.f;  // -0 -> +0
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+template <int VPL>
+__device__ __forceinline__ void topk_warp_reg(const float* __restrict__ l, int E, int k, int renorm,
+                                              int32_t* __restrict__ ids_t, float* __restrict__ wts_t) {
+  const int lane = threadIdx.x & 31;
+  float v[VPL];
+  uint32_t key[VPL];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? __ldcg(l + e) : -INFINITY;
+    key[i] = e < E ? order_key(v[i]) : 0u;
+    if (e < E) mx = fmaxf(mx, v[i]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float z = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i)
+    if (lane + 32 * i < E) z += expf(v[i] - mx);
+  z = warp_sum(z);
+  uint32_t taken = 0u;
+  float sel_sum = 0.f, my_w = 0.f;
+  int my_id = 0;
+  for (int j = 0; j < k; ++j) {
+    uint32_t bk = 0u;
+    int bi = -1;
+    float bv = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+      if (lane + 32 * i < E && !((taken >> i) & 1u) && (bi < 0 || key[i] > bk)) {
+        bk = key[i];
+        bi = i;
+        bv = v[i];
+      }
+    const uint32_t m = __reduce_max_sync(0xffffffffu, bi >= 0 ? bk : 0u);
+    const uint32_t cand = (bi >= 0 && bk == m) ? static_cast<uint32_t>(lane + 32 * bi) : 0xffffffffu;
+    const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+    const float wv = __shfl_sync(0xffffffffu, bv, static_cast<int>(win & 31u));
+    const float p = expf(wv - mx) / z;
+    sel_sum += p;
+    if (lane == j) {
+      my_w = p;
+      my_id = static_cast<int>(win);
+    }
+    if (static_cast<int>(win & 31u) == lane) taken |= 1u << (win >> 5);
+  }
+  if (lane < k) {
+    ids_t[lane] = my_id;
+    wts_t[lane] = renorm ? my_w / sel_sum : my_w;
+  }
+}
+
+// Top-k of one token by one warp: the register form for E <= 512, else the
+// shared-memory form (ls: this warp's E floats).
+__device__ __forceinline__ void topk_any(const float* __restrict__ l, float* ls, int E, int k, int renorm,
+                                         int32_t* __restrict__ ids_t, float* __restrict__ wts_t) {
+  if (E <= 32) topk_warp_reg<1>(l, E, k, renorm, ids_t, wts_t);
+  else if (E <= 64) topk_warp_reg<2>(l, E, k, renorm, ids_t, wts_t);
+  else if (E <= 128) topk_warp_reg<4>(l, E, k, renorm, ids_t, wts_t);
+  else if (E <= 256) topk_warp_reg<8>(l, E, k, renorm, ids_t, wts_t);
+  else if (E <= 512) topk_warp_reg<16>(l, E, k, renorm, ids_t, wts_t);
+  else topk_warp(l, ls, E, k, renorm, ids_t, wts_t);
+}
+
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T,
                                                          int E, int k, int renorm,
                                                          int32_t* __restrict__ ids,
@@ -258,8 +337,8 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   const int warp = threadIdx.x >> 5;
   const int t = blockIdx.x * (blockDim.x >> 5) + warp;
   if (t >= T) return;
-  topk_warp(logits + static_cast<size_t>(t) * E, lsm + static_cast<size_t>(warp) * E, E, k, renorm,
-            ids + static_cast<size_t>(t) * k, wts + static_cast<size_t>(t) * k);
+  topk_any(logits + static_cast<size_t>(t) * E, lsm + static_cast<size_t>(warp) * E, E, k, renorm,
+           ids + static_cast<size_t>(t) * k, wts + static_cast<size_t>(t) * k);
 }
 
 
