@@ -22,6 +22,10 @@ Parity status per function (what pins it is in the "not gpu" tests):
   combine          pinned: one-hot weights, linearity.
   cache_rebuild    pinned: invariants, brute force on small states.
   cache_install    pinned: a hand-worked example, invariants on random states.
+  prefetch         pinned: a hand-worked trace, brute force over the fetched
+                   and victim sets on tiny states, invariants.  Which
+                   predicted misses come first when slots run short follows
+                   the resolve's reading (recency descending, lower id).
 """
 
 from __future__ import annotations
@@ -89,6 +93,9 @@ def lib():
             L.orc_resolve_many.argtypes = ([c.c_int] * 3 + [c.c_void_p] * 5 + [c.c_int, c.c_void_p,
                                            c.c_int, c.c_int, c.c_int32, c.c_int] + [c.c_void_p] * 4
                                            + [c.c_int])
+            L.orc_prefetch.restype = c.c_int
+            L.orc_prefetch.argtypes = ([c.c_int] * 3 + [c.c_void_p] * 5 + [c.c_int, c.c_void_p,
+                                       c.c_int, c.c_int, c.c_int32] + [c.c_void_p] * 3 + [c.c_int])
             L.orc_cache_install.restype = c.c_int
             L.orc_cache_install.argtypes = [c.c_int, c.c_int, c.c_int, c.c_void_p, c.c_void_p, c.c_void_p,
                                             c.c_void_p, c.c_int, c.c_int]
@@ -266,6 +273,26 @@ def resolve_many(st: CacheState, layer: int, ids: np.ndarray, phi: int, max_list
     if rc != 0:
         raise ValueError("orc_resolve_many rejected its arguments")
     return sl, nf, ff, fs
+
+
+def prefetch(st: CacheState, layer: int, pred_ids: np.ndarray, max_prefetch: int,
+             max_list: int | None = None):
+    """A speculative fetch of `layer`'s predicted experts, one layer ahead of
+    its resolve (see orc_prefetch); mutates st.  Returns (num, fetch_fid,
+    fetch_slot)."""
+    pred = _c(pred_ids, np.int32)
+    T, k = pred.shape
+    if max_list is None:
+        max_list = T * k
+    nf = np.zeros(1, np.int32)
+    ff = np.empty(max_list, np.int32)
+    fs = np.empty(max_list, np.int32)
+    rc = lib().orc_prefetch(st.L, st.E, st.S, _ptr(st.slot_owner), _ptr(st.map), _ptr(st.usage),
+                            _ptr(st.recency), _ptr(st.step), layer, _ptr(pred), T, k, int(max_prefetch),
+                            _ptr(nf), _ptr(ff), _ptr(fs), max_list)
+    if rc != 0:
+        raise ValueError("orc_prefetch rejected its arguments")
+    return int(nf[0]), ff, fs
 
 
 # ------------------------------------------------------------------ permute

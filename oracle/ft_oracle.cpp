@@ -405,6 +405,93 @@ int orc_resolve_many(int L, int E, int S, int32_t* slot_owner, int32_t* map, int
   return 0;
 }
 
+// ------------------------------------------------------------- prefetch ----
+// [NVMe] "Where the time actually goes", speculative copies: layer l+1's router
+// run on layer l's MoE input predicts layer l+1's experts, so most of its
+// copies can start one layer early, while layer l still computes.  The pages
+// give the idea, not the bookkeeping; the reading taken here is a fetch made
+// ahead of its resolve, with the resolve's own choice rules:
+//   1. U = the distinct predicted experts (pred_ids of `layer`), ascending.
+//   2. hits = {e in U : map[fid] >= 0}; M = U \ hits; m = |M|.
+//   3. A slot may not be a victim when a predicted hit owns it, or when it is
+//      held (owner >= 0) with usage >= step - 1: the last resolve used it at
+//      step - 1, so the current layer's experts may still be reading it, and
+//      usage == step marks an earlier prefetch or install not yet consumed.
+//   4. num = min(m, max_prefetch, eligible slots).
+//   5. fetched = the first num of M by (recency desc, id asc); victims = the
+//      first num eligible slots by (usage asc, slot asc); the i-th fetched
+//      expert goes to the i-th victim.
+//   6. Evict the victims' owners (map -1) and install: owner = fid, map =
+//      slot, usage = step (the step the next resolve runs at).  Nothing is
+//      routed, so recency, the usage of hit slots and the step stay as they
+//      are.
+// The fetch list has resolve's form: (fid, slot) for i < num, -1 after that,
+// up to max_list entries.  Returns 0, or -1 (state untouched) for an id
+// outside [0, E), a negative max_prefetch or a bad shape.
+// Parity: pinned by a hand-worked trace, brute force over the fetched and
+// victim sets on tiny states, and invariants (no busy or hit slot evicted,
+// every prefetched expert resident, outputs unchanged).
+int orc_prefetch(int L, int E, int S, int32_t* slot_owner, int32_t* map, int64_t* usage,
+                 const int64_t* recency, const int64_t* step, int layer, const int32_t* pred_ids,
+                 int T, int k, int32_t max_prefetch, int32_t* num_out, int32_t* fetch_fid,
+                 int32_t* fetch_slot, int max_list) {
+  if (layer < 0 || layer >= L || E <= 0 || S < 0 || T < 0 || k < 0 || max_prefetch < 0) return -1;
+  const int n = T * k;
+  for (int i = 0; i < n; ++i)
+    if (pred_ids[i] < 0 || pred_ids[i] >= E) return -1;
+  const int64_t base = static_cast<int64_t>(layer) * E;
+  const int64_t now = *step;
+
+  std::vector<int> U(pred_ids, pred_ids + n);
+  std::sort(U.begin(), U.end());
+  U.erase(std::unique(U.begin(), U.end()), U.end());
+
+  std::vector<char> blocked(static_cast<size_t>(S), 0);
+  std::vector<int> misses;
+  for (int e : U) {
+    const int32_t s = map[base + e];
+    if (s >= 0)
+      blocked[s] = 1;
+    else
+      misses.push_back(e);
+  }
+  for (int s = 0; s < S; ++s)
+    if (slot_owner[s] >= 0 && usage[s] >= now - 1) blocked[s] = 1;
+
+  std::vector<int> cand;
+  for (int s = 0; s < S; ++s)
+    if (!blocked[s]) cand.push_back(s);
+  const int m = static_cast<int>(misses.size());
+  const int nf = std::min(std::min(m, static_cast<int>(max_prefetch)), static_cast<int>(cand.size()));
+
+  std::vector<int> ranked = misses;
+  std::sort(ranked.begin(), ranked.end(), [&](int a, int b) {
+    int64_t ra = recency[base + a], rb = recency[base + b];
+    if (ra != rb) return ra > rb;
+    return a < b;
+  });
+  std::sort(cand.begin(), cand.end(), [&](int a, int b) {
+    if (usage[a] != usage[b]) return usage[a] < usage[b];
+    return a < b;
+  });
+
+  for (int i = 0; i < nf; ++i) {
+    const int e = ranked[i];
+    const int v = cand[i];
+    const int32_t old = slot_owner[v];
+    if (old >= 0) map[old] = -1;
+    slot_owner[v] = static_cast<int32_t>(base + e);
+    map[base + e] = v;
+    usage[v] = now;
+  }
+  *num_out = nf;
+  for (int i = 0; i < max_list; ++i) {
+    fetch_fid[i] = (i < nf) ? static_cast<int32_t>(base + ranked[i]) : -1;
+    fetch_slot[i] = (i < nf) ? cand[i] : -1;
+  }
+  return 0;
+}
+
 // -------------------------------------------------------------- rebuild ----
 // [FT-ZH] sec. 7 item 1 and [FT-KR] design pattern 7: the slot cache is rebuilt
 // at a new size at a safe point, after its new geometry has been checked; the
