@@ -5,6 +5,8 @@
  * The layer, one call per step, all on one CUDA stream with no host sync:
  *   ft_moe_route          router logits, softmax, top-k
  *   ft_moe_resolve_slots  (layer, expert) -> cache slot or -1, q* split inside
+ *   ft_moe_prefetch       speculative plan: the next layer's predicted misses
+ *                         into eligible slots, one layer ahead of its resolve
  *   ft_moe_fetch          copy the chosen misses from the pool into the cache
  *   ft_moe_fetch_layer    copy a whole layer into a slot range (prefill buffer)
  *   ft_moe_cache_install  the state's bookkeeping for such a layer
@@ -202,6 +204,37 @@ FT_API ft_status ft_moe_resolve_slots(const ft_cache_state* state_host, int32_t 
                                int32_t frac_q16, int32_t* slot_ids, int32_t* num_fetch,
                                int32_t* fetch_fid, int32_t* fetch_slot, int32_t max_list,
                                int32_t* dev_status, void* stream);
+
+/*
+ * ft_moe_prefetch -- plan a speculative fetch of the next layer's experts
+ * (NVMe-streaming post, "Where the time actually goes", speculative copies:
+ * layer l+1's router run on layer l's MoE input picks most of layer l+1's
+ * experts, so their copies can start one layer early, while layer l
+ * computes).  pred_ids [T,k] int32 are the predicted ids of `layer` (from
+ * ft_moe_route with that layer's router on the previous layer's input).  One
+ * device kernel, the resolve's rules without the routing bookkeeping:
+ *   U = distinct predicted experts; misses: map[layer*E+e] < 0, m of them;
+ *   a slot may not be a victim if a predicted hit owns it, or if it is held
+ *   (owner >= 0) with usage >= step-1 (the layer resolved last may still be
+ *   reading it; usage == step marks an earlier prefetch not yet consumed);
+ *   num_fetch = min(m, max_prefetch, eligible slots); the fetched misses are
+ *   the first by (recency desc, id asc), the victims the eligible slots by
+ *   (usage asc, slot asc), paired in order; victims' owners are evicted
+ *   (map -1) and each victim takes its expert with usage = step.  Recency,
+ *   hit usage and the step do not change.
+ * Outputs have resolve's form (num_fetch [1]; fetch_fid / fetch_slot
+ * [max_list], -1 after num_fetch; max_list >= min(T*k, S)), ready for
+ * ft_moe_fetch on the same stream.  Ordering is the caller's: run it after
+ * the resolve of the current layer and before the resolve of `layer`, and
+ * let that layer's fetch and experts wait for the prefetch's copy.  An id
+ * outside [0, E) records FT_ERR_BAD_ID, leaves the state untouched and
+ * writes num_fetch = 0.  max_prefetch < 0 and the resolve's limits are
+ * FT_ERR_INVALID.
+ */
+FT_API ft_status ft_moe_prefetch(const ft_cache_state* state_host, int32_t layer, const int32_t* pred_ids,
+                                 int32_t T, int32_t k, int32_t max_prefetch, int32_t* num_fetch,
+                                 int32_t* fetch_fid, int32_t* fetch_slot, int32_t max_list,
+                                 int32_t* dev_status, void* stream);
 
 /*
  * ft_moe_fetch -- copy each fetched expert block pool[fetch_fid[i]] ->

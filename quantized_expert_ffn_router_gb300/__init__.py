@@ -54,6 +54,7 @@ _SIGS = {
     "ft_moe_route": (_I32, [_V, _I32, _I32, _V, _I32, _I32, _I32, _V, _V, _V, _SZ, _V]),
     "ft_moe_split_q16": (_I32, [_V, _I32, _I32, _V, _V]),
     "ft_moe_resolve_slots": (_I32, [_V, _I32, _V, _I32, _I32, _I32, _V, _V, _V, _V, _I32, _V, _V]),
+    "ft_moe_prefetch": (_I32, [_V, _I32, _V, _I32, _I32, _I32, _V, _V, _V, _I32, _V, _V]),
     "ft_moe_fetch": (_I32, [_V, _V, _V, _V, _V, _I32, _V, _V]),
     "ft_moe_fetch_layer": (_I32, [_V, _V, _I32, _I32, _I32, _V]),
     "ft_moe_cache_install": (_I32, [_V, _I32, _I32, _V]),
@@ -181,6 +182,17 @@ def resolve_slots(state: DeviceCacheState, layer: int, topk_ids, frac_q16: int, 
                                        _ptr(slot_ids), _ptr(num_fetch), _ptr(fetch_fid),
                                        _ptr(fetch_slot), fetch_fid.numel(), _ptr(dev_status),
                                        _stream(stream)))
+
+
+def prefetch(state: DeviceCacheState, layer: int, pred_ids, max_prefetch: int, num_fetch, fetch_fid,
+             fetch_slot, dev_status=None, stream=None):
+    """Plan a speculative fetch of `layer`'s predicted ids (ft_moe_prefetch);
+    the copy itself is fetch() with the same list."""
+    T, k = pred_ids.shape
+    st = state.struct()
+    _check(load().ft_moe_prefetch(ctypes.byref(st), layer, _ptr(pred_ids), T, k, int(max_prefetch),
+                                  _ptr(num_fetch), _ptr(fetch_fid), _ptr(fetch_slot), fetch_fid.numel(),
+                                  _ptr(dev_status), _stream(stream)))
 
 
 def fetch(pool: FtBank, cache: FtBank, num_fetch, fetch_fid, fetch_slot, dev_status=None, stream=None):

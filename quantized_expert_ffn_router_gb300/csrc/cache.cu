@@ -117,6 +117,8 @@ ft_status resolve_prepare(const ft_cache_state* st, int32_t layer, const int32_t
   a.fetch_fid = fetch_fid;
   a.fetch_slot = fetch_slot;
   a.dev_status = dev_status;
+  a.prefetch = 0;
+  a.max_prefetch = 0;
   // the slot state is staged in shared memory when it fits beside the
   // resolve's own arrays (every cache up to ~24k slots at E <= 256)
   const size_t base = resolve_smem_bytes(st->E, n);
@@ -126,7 +128,54 @@ ft_status resolve_prepare(const ft_cache_state* st, int32_t layer, const int32_t
   return FT_OK;
 }
 
+ft_status prefetch_prepare(const ft_cache_state* st, int32_t layer, const int32_t* pred_ids, int32_t T,
+                           int32_t k, int32_t max_prefetch, int32_t* num_fetch, int32_t* fetch_fid,
+                           int32_t* fetch_slot, int32_t max_list, int32_t* dev_status, size_t stage_cap,
+                           ResolveArgs* out, size_t* smem_out) {
+  FT_REQUIRE(max_prefetch >= 0, "prefetch: max_prefetch %d < 0", max_prefetch);
+  // the resolve's checks, with pred_ids standing in for the (unwritten) slot_ids
+  ft_status s = resolve_prepare(st, layer, pred_ids, T, k, 0, const_cast<int32_t*>(pred_ids), num_fetch,
+                                fetch_fid, fetch_slot, max_list, dev_status, "prefetch", stage_cap, out,
+                                smem_out);
+  if (s != FT_OK) return s;
+  out->slot_ids = nullptr;
+  out->prefetch = 1;
+  out->max_prefetch = max_prefetch;
+  return FT_OK;
+}
+
 }  // namespace ft
+
+namespace {
+
+// One CTA runs a resolve or a prefetch (both set up by *_prepare), chained to
+// the previous kernel on the stream by programmatic launch.
+ft_status launch_resolve(const ft::ResolveArgs& a, size_t smem, void* stream, const char* what) {
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(ft::resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(ft::kResSmemCap));
+    if (e != cudaSuccess)
+      return ft::fail(FT_ERR_CUDA, "%s: smem attribute: %s", what, cudaGetErrorString(e));
+  }
+  // small calls usually finish in the one-warp path; 256 threads keep the
+  // rest cheap to synchronise.  Larger calls get the whole block.
+  const int threads = a.n <= 32 ? 256 : ft::kResThreads;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = ft::as_stream(stream);
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, ft::resolve_kernel, a);
+  if (e != cudaSuccess) return ft::fail(FT_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return ft::launch_check(what);
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -153,29 +202,18 @@ ft_status ft_moe_resolve_slots(const ft_cache_state* st, int32_t layer, const in
   ft_status ps = ft::resolve_prepare(st, layer, topk_ids, T, k, frac_q16, slot_ids, num_fetch, fetch_fid,
                                      fetch_slot, max_list, dev_status, "resolve", ft::kResSmemCap, &a, &smem);
   if (ps != FT_OK) return ps;
-  const int n = a.n;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(ft::resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(ft::kResSmemCap));
-    if (e != cudaSuccess)
-      return ft::fail(FT_ERR_CUDA, "resolve: smem attribute: %s", cudaGetErrorString(e));
-  }
-  // small calls usually finish in the one-warp path; 256 threads keep the
-  // rest cheap to synchronise.  Larger calls get the whole block.
-  const int threads = n <= 32 ? 256 : ft::kResThreads;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(1);
-  cfg.blockDim = dim3(threads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = ft::as_stream(stream);
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, ft::resolve_kernel, a);
-  if (e != cudaSuccess) return ft::fail(FT_ERR_CUDA, "resolve_slots: %s", cudaGetErrorString(e));
-  return ft::launch_check("resolve_slots");
+  return launch_resolve(a, smem, stream, "resolve_slots");
+}
+
+ft_status ft_moe_prefetch(const ft_cache_state* st, int32_t layer, const int32_t* pred_ids, int32_t T,
+                          int32_t k, int32_t max_prefetch, int32_t* num_fetch, int32_t* fetch_fid,
+                          int32_t* fetch_slot, int32_t max_list, int32_t* dev_status, void* stream) {
+  ft::ResolveArgs a;
+  size_t smem = 0;
+  ft_status ps = ft::prefetch_prepare(st, layer, pred_ids, T, k, max_prefetch, num_fetch, fetch_fid,
+                                      fetch_slot, max_list, dev_status, ft::kResSmemCap, &a, &smem);
+  if (ps != FT_OK) return ps;
+  return launch_resolve(a, smem, stream, "prefetch");
 }
 
 ft_status ft_moe_fetch(const ft_bank* pool, const ft_bank* cache, const int32_t* num_fetch,

@@ -18,6 +18,10 @@ constexpr size_t kResSmemCap = 220 * 1024;  // dynamic shared memory the resolve
 struct ResolveArgs {
   int32_t E, S, layer, n, phi, max_list;
   int32_t staged;  // 1: the victim search reads the slots' usage and hit flags from shared memory
+  // 1: a speculative prefetch of predicted ids (no split, cap = max_prefetch,
+  // held slots with usage >= step-1 are not victims, no routing bookkeeping,
+  // no slot_ids); 0: a resolve
+  int32_t prefetch, max_prefetch;
   int32_t* slot_owner;
   int32_t* map;
   int64_t* usage;
@@ -44,6 +48,12 @@ __host__ __device__ inline size_t resolve_smem_bytes(int E, int n) {
 __host__ __device__ inline size_t resolve_stage_bytes(int S) {
   return static_cast<size_t>(S) * 8 + ((static_cast<size_t>(S) + 15) & ~static_cast<size_t>(15));
 }
+// Host: check a prefetch call's arguments the same way (phi unused, no
+// slot_ids) and fill the prefetch fields.
+ft_status prefetch_prepare(const ft_cache_state* st, int32_t layer, const int32_t* pred_ids, int32_t T,
+                           int32_t k, int32_t max_prefetch, int32_t* num_fetch, int32_t* fetch_fid,
+                           int32_t* fetch_slot, int32_t max_list, int32_t* dev_status, size_t stage_cap,
+                           ResolveArgs* out, size_t* smem_out);
 // Host: check a resolve call's arguments and fill its device arguments,
 // deciding whether the victim search may stage the slot state in shared
 // memory: when the total stays within stage_cap bytes (FT_ERR_INVALID with a
@@ -147,7 +157,7 @@ __device__ __noinline__ void resolve_block(const ResolveArgs& a, unsigned char* 
   const int nt = blockDim.x;
   const int base = a.layer * E;
 
-  if (n <= 32) {
+  if (n <= 32 && !a.prefetch) {
     __shared__ int s_done;
     if (tid < 32) {
       const bool done = resolve_small_no_fetch(a);
@@ -175,7 +185,8 @@ __device__ __noinline__ void resolve_block(const ResolveArgs& a, unsigned char* 
   }
   __syncthreads();
   if (s_bad) {
-    for (int i = tid; i < n; i += nt) a.slot_ids[i] = -1;
+    if (!a.prefetch)
+      for (int i = tid; i < n; i += nt) a.slot_ids[i] = -1;
     for (int i = tid; i < a.max_list; i += nt) {
       a.fetch_fid[i] = -1;
       a.fetch_slot[i] = -1;
@@ -230,9 +241,44 @@ __device__ __noinline__ void resolve_block(const ResolveArgs& a, unsigned char* 
       int nf = split_q16_dev(total, a.phi);
       nf = min(nf, evictable);
       s_nf = max(nf, 0);
+      s_cnt = 0;
     }
   }
   __syncthreads();
+  const int64_t now = s_now;
+  // The victim search's view of the slots: whether a slot may not be a victim
+  // (a hit; for a prefetch also a held slot with usage >= now-1, which the
+  // layer resolved last may still be reading, or an earlier prefetch not yet
+  // consumed), and its usage.  When the host found room (a.staged), one
+  // coalesced pass copies both into shared memory, so the scans below (several
+  // per call) read shared memory, not L2.
+  int64_t* su = nullptr;
+  unsigned char* shit = nullptr;
+  auto blocked_global = [&](int s) -> bool {
+    if (is_hit_slot(a.slot_owner, s, base, E, inU)) return true;
+    return a.prefetch && a.slot_owner[s] >= 0 && a.usage[s] >= now - 1;
+  };
+  if (a.prefetch) {
+    // a prefetch's count is capped by its eligible slots: count them (and stage)
+    if (a.staged) {
+      su = reinterpret_cast<int64_t*>(smem + resolve_smem_bytes(E, n));
+      shit = reinterpret_cast<unsigned char*>(su + S);
+    }
+    int c = 0;
+    for (int s = tid; s < S; s += nt) {
+      const bool b = blocked_global(s);
+      if (su) {
+        su[s] = a.usage[s];
+        shit[s] = b;
+      }
+      c += b;
+    }
+    c = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(c)));
+    if ((tid & 31) == 0) atomicAdd(&s_cnt, c);
+    __syncthreads();
+    if (tid == 0) s_nf = max(0, min(min(s_m, a.max_prefetch), S - s_cnt));
+    __syncthreads();
+  }
   const int m = s_m, nf = s_nf;
 
   // 3. the fetched misses: rank by (recency desc, id asc)
@@ -247,13 +293,9 @@ __device__ __noinline__ void resolve_block(const ResolveArgs& a, unsigned char* 
     if (r < nf) fe[r] = ej;
   }
 
-  // 4. the victims: the nf smallest (usage, slot) among non-hit slots.  Each
-  // scan below reads a slot's usage and whether it is a hit; when the host
-  // found room (a.staged), one coalesced pass copies both into shared memory
-  // first, so the scans (several per call) read shared memory, not L2.
-  int64_t* su = nullptr;
-  unsigned char* shit = nullptr;
-  if (nf > 0 && a.staged) {
+  // 4. the victims: the nf smallest (usage, slot) among the slots that may be
+  // victims (staged first for a resolve, see above).
+  if (nf > 0 && a.staged && !a.prefetch) {
     su = reinterpret_cast<int64_t*>(smem + resolve_smem_bytes(E, n));
     shit = reinterpret_cast<unsigned char*>(su + S);
 #pragma unroll 4
@@ -263,7 +305,7 @@ __device__ __noinline__ void resolve_block(const ResolveArgs& a, unsigned char* 
     }
     __syncthreads();
   }
-  auto slot_hit = [&](int s) -> bool { return shit ? shit[s] != 0 : is_hit_slot(a.slot_owner, s, base, E, inU); };
+  auto slot_hit = [&](int s) -> bool { return shit ? shit[s] != 0 : blocked_global(s); };
   auto slot_use = [&](int s) -> int64_t { return su ? su[s] : a.usage[s]; };
   if (nf > 0) {
     unsigned long long kmin = ~0ull, kmax = 0ull;
@@ -380,12 +422,13 @@ __device__ __noinline__ void resolve_block(const ResolveArgs& a, unsigned char* 
   }
   __syncthreads();
 
-  // 5. state update
-  const int64_t now = s_now;
-  for (int i = tid; i < nU; i += nt) {
-    const int s = slotOf[U[i]];
-    if (s >= 0) a.usage[s] = now;
-  }
+  // 5. state update (a prefetch routes nothing: hit usage, recency and the
+  // step stay as they are)
+  if (!a.prefetch)
+    for (int i = tid; i < nU; i += nt) {
+      const int s = slotOf[U[i]];
+      if (s >= 0) a.usage[s] = now;
+    }
   for (int i = tid; i < nf; i += nt) {
     const int v = vs2[i];
     const int old = a.slot_owner[v];
@@ -400,18 +443,20 @@ __device__ __noinline__ void resolve_block(const ResolveArgs& a, unsigned char* 
     a.usage[v] = now;
     slotOf[e] = v;
   }
-  for (int i = tid; i < nU; i += nt) a.recency[base + U[i]] = now;
+  if (!a.prefetch)
+    for (int i = tid; i < nU; i += nt) a.recency[base + U[i]] = now;
   __syncthreads();
 
   // 6. outputs
-  for (int i = tid; i < n; i += nt) a.slot_ids[i] = slotOf[a.ids[i]];
+  if (!a.prefetch)
+    for (int i = tid; i < n; i += nt) a.slot_ids[i] = slotOf[a.ids[i]];
   for (int i = tid; i < a.max_list; i += nt) {
     a.fetch_fid[i] = (i < nf) ? base + fe[i] : -1;
     a.fetch_slot[i] = (i < nf) ? vs2[i] : -1;
   }
   if (tid == 0) {
     *a.num_fetch = nf;
-    *a.step = now + 1;
+    if (!a.prefetch) *a.step = now + 1;
   }
 }
 

@@ -24,6 +24,12 @@ Stream orchestration only: every step is a call into libft_moe.so.
   The deep-dive notes that the profile prefers the two measured while both
   run at once (they share host memory), and calibrate_frac_q16 does so.
 
+* SpeculativeDecode runs a decode step over consecutive layers with the
+  speculative next-layer copies of the NVMe-streaming post ("Where the time
+  actually goes"): layer l+1's router on layer l's input predicts its
+  experts, ft_moe_prefetch plans their copies and ft_moe_fetch starts them on
+  a second stream while layer l computes.
+
 * PrefillLayers runs prefill over consecutive layers through the whole-layer
   double buffer: layer l's experts in cache slots (l%2)*E .., copied from the
   pool by the copy engine (ft_moe_fetch_layer, then ft_moe_cache_install) on
@@ -39,8 +45,8 @@ from __future__ import annotations
 import ctypes
 
 from . import (FT_DECODE, FT_DECODE_HOST, FT_PREFILL, DeviceCacheState, FtBank, cache_install, combine, experts_fwd,
-               experts_workspace, fetch, fetch_layer, merge_partials, permute, permute_workspace, resolve_slots, route,
-               route_workspace)
+               experts_workspace, fetch, fetch_layer, merge_partials, permute, permute_workspace, prefetch,
+               resolve_slots, route, route_workspace)
 
 
 def frac_q16_from_bandwidths(b_p: float, b_h: float) -> int:
@@ -110,6 +116,84 @@ class DecodeLayer:
         main.wait_event(self.ev_join)
         merge_partials(self.part_cache, self.part_host, out, stream=main)
         return out
+
+
+class SpeculativeDecode:
+    """One decode step over consecutive layers with speculative next-layer
+    copies (NVMe-streaming post, "Where the time actually goes": layer l+1's
+    router run on layer l's MoE input picks most of layer l+1's experts, so
+    their copies can start a layer early).
+
+    Per layer l, on the current (main) stream: route -> resolve -> fetch ->
+    experts (the serial DecodeLayer call, the pool as host path).  After
+    layer l's resolve, a second stream runs layer l+1's router on layer l's
+    input, plans the prefetch of the predicted misses (ft_moe_prefetch) and
+    copies them (ft_moe_fetch) while layer l's fetch and experts run.  Layer
+    l+1's resolve waits for the plan (the state), its fetch for the copy (the
+    slots).  The prefetch never evicts a slot that layer l uses (usage >=
+    step-1 after layer l's resolve), so the two streams touch disjoint slots.
+    Outputs equal the non-speculative step's bit for bit: only which bytes
+    come from a cache slot or from the pool changes.  Buffers are allocated
+    once, so a step captures into one CUDA graph."""
+
+    def __init__(self, state: DeviceCacheState, cache: FtBank, pool: FtBank, E: int, k: int, T: int,
+                 max_prefetch: int | None = None, device="cuda"):
+        import torch
+
+        if pool is None:
+            raise ValueError("speculative decode copies from a pool")
+        self.layer = DecodeLayer(state, cache, pool, E, k, T, device)
+        self.max_prefetch = T * k if max_prefetch is None else int(max_prefetch)
+        n = T * k
+        ml = max(min(n, state.S), 1)
+        i32 = dict(dtype=torch.int32, device=device)
+        self.pred_ids = torch.empty((T, k), **i32)
+        self.pred_w = torch.empty((T, k), dtype=torch.float32, device=device)
+        self.pred_ws = torch.zeros(route_workspace(T, E), dtype=torch.uint8, device=device)
+        self.pf_num = torch.zeros(1, **i32)
+        self.pf_fid = torch.empty(ml, **i32)
+        self.pf_slot = torch.empty(ml, **i32)
+        self.spec_stream = torch.cuda.Stream(device=device)
+        self.ev_resolved = torch.cuda.Event()
+        self.ev_plan = [torch.cuda.Event() for _ in range(2)]
+        self.ev_copy = [torch.cuda.Event() for _ in range(2)]
+
+    def __call__(self, xs, w_routers, frac_q16: int, outs, speculate: bool = True, layers=None):
+        """xs[i] [T,H] bf16 MoE input and w_routers[i] [E,H] fp32 router of
+        layer layers[i] (default i) -> outs[i].  Enqueues on the current stream
+        (and the speculation stream)."""
+        import torch
+
+        d = self.layer
+        main = torch.cuda.current_stream()
+        P = self.spec_stream
+        n = len(xs)
+        layers = list(range(n)) if layers is None else list(layers)
+        for i in range(n):
+            l = layers[i]
+            route(xs[i], w_routers[i], d.k, d.ids, d.w, d.route_ws, stream=main)
+            if speculate and i > 0:
+                main.wait_event(self.ev_plan[i % 2])  # the prefetch's state update is in
+            resolve_slots(d.state, l, d.ids, frac_q16, d.slot_ids, d.num_fetch, d.fetch_fid, d.fetch_slot,
+                          d.status, stream=main)
+            if speculate and i + 1 < n:
+                b = (i + 1) % 2
+                self.ev_resolved.record(main)
+                P.wait_event(self.ev_resolved)
+                route(xs[i], w_routers[i + 1], d.k, self.pred_ids, self.pred_w, self.pred_ws, stream=P)
+                prefetch(d.state, layers[i + 1], self.pred_ids, self.max_prefetch, self.pf_num, self.pf_fid,
+                         self.pf_slot, d.status, stream=P)
+                self.ev_plan[b].record(P)
+                fetch(d.pool, d.cache, self.pf_num, self.pf_fid, self.pf_slot, d.status, stream=P)
+                self.ev_copy[b].record(P)
+            if speculate and i > 0:
+                main.wait_event(self.ev_copy[i % 2])  # the prefetched blocks are in their slots
+            fetch(d.pool, d.cache, d.num_fetch, d.fetch_fid, d.fetch_slot, d.status, stream=main)
+            experts_fwd(d.cache, d.pool, l, d.E, xs[i], d.T, d.k, d.slot_ids, d.ids, d.w, outs[i], d.ws,
+                        dev_status=d.status, stream=main)
+        if speculate:
+            main.wait_stream(P)
+        return outs
 
 
 def calibrate_frac_q16(pool: FtBank, cache: FtBank, E: int, k: int, n_fetch: int, reps: int = 10,

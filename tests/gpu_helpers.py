@@ -31,9 +31,10 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
 
 
 def gapped_tokens(seed: int, tag: str, T: int, H: int, W: np.ndarray, k: int, gap: float,
-                  bias_feature: bool = False, max_tries: int = 64):
+                  bias_feature: bool = False, max_tries: int = 64, W_more=()):
     """x [T,H] bf16 rows, each redrawn (seeded) until the oracle's sorted logits
-    at ranks 1..k+1 differ pairwise by >= gap.  Returns (x, redraw count)."""
+    at ranks 1..k+1 differ pairwise by >= gap, under W and under every router
+    in W_more.  Returns (x, redraw count)."""
     x = np.empty((T, H), np.uint16)
     redraws = 0
     for t in range(T):
@@ -41,9 +42,12 @@ def gapped_tokens(seed: int, tag: str, T: int, H: int, W: np.ndarray, k: int, ga
             row = synth.normal_bf16(synth.stream_key(seed, tag, t, a), (1, H))
             if bias_feature:
                 row[0, 0] = synth.bf16_bits(np.array([1.0], np.float32))[0]
-            _, _, lg = oracle.route(row, W, k, want_logits=True)
-            top = np.sort(lg[0])[::-1][: k + 1]
-            if np.all(-np.diff(top) >= gap):
+            ok = True
+            for Wr in (W, *W_more):
+                _, _, lg = oracle.route(row, Wr, k, want_logits=True)
+                top = np.sort(lg[0])[::-1][: k + 1]
+                ok = ok and bool(np.all(-np.diff(top) >= gap))
+            if ok:
                 break
             redraws += 1
         else:

@@ -70,6 +70,12 @@ def test_host_validation_without_gpu(ft):
     assert lib.ft_moe_resolve_slots(*args(2, 100, 4)) == ft.FT_ERR_INVALID
     assert lib.ft_moe_resolve_slots(*args(0, -1, 4)) == ft.FT_ERR_INVALID
     assert lib.ft_moe_resolve_slots(*args(0, 100, 1)) == ft.FT_ERR_INVALID
+    # prefetch: negative cap, layer out of range, short fetch list
+    pargs = lambda layer, cap, ml: (ctypes.byref(st), layer, dummy, 1, 2, cap, dummy, dummy, dummy, ml,
+                                    None, None)
+    assert lib.ft_moe_prefetch(*pargs(0, -1, 4)) == ft.FT_ERR_INVALID
+    assert lib.ft_moe_prefetch(*pargs(2, 2, 4)) == ft.FT_ERR_INVALID
+    assert lib.ft_moe_prefetch(*pargs(0, 2, 1)) == ft.FT_ERR_INVALID
     # experts: unsupported bank format / misaligned base
     bad = ft.FtBank(0, 2048, 512, 48, dummy, 1 << 21, 4, None)
     assert lib.ft_moe_experts_fwd(ctypes.byref(bad), None, 0, 8, dummy, None, 1, dummy, dummy, dummy, 2, 0,
