@@ -10,7 +10,11 @@
 //     those gate and up rows and their scales at once, then converts the
 //     token's activations to f16 in registers (exact per-token power-of-two
 //     prescale), dots, reduces with shuffles, and lane r writes row r's
-//     h = silu(g) * u to the fp32 workspace.
+//     h = silu(g) * u to the fp32 workspace.  With few pairs (T*k <= 16) a
+//     second form runs one row per warp in 4-warp CTAs, the activations
+//     converted once per CTA into shared memory: four times the warps, each
+//     with a quarter of the dependent dequant-dot instructions, which is what
+//     bounds a one-token layer (same h, bit for bit).
 //   down: a programmatic dependent of gate/up, grid (H / rows per CTA) x T.
 //     A CTA owns rows of one token's output.  Its lanes first load their
 //     chunks of the down rows of the token's k experts (gate/up has already
@@ -306,7 +310,187 @@ __global__ void __launch_bounds__(kThreads, 2) pm_gateup_kernel(DecArgs a, int g
   }
 }
 
+// ------------------------------------------------------- gate/up, 1 row ---
+// The rows and arithmetic of pm_gateup_kernel with one row per warp and four
+// warps per CTA: four times as many warps, each with a quarter of the
+// dependent instructions, so that the dequant-dot work (not the memory) no
+// longer sets the kernel's length.  The token's activations are converted
+// once per CTA into shared memory (16 f16x2 words per chunk in the format's
+// order, then the chunk's sum; 80-byte stride, conflict-free 16-byte reads)
+// instead of once per warp.  Every h is bit-identical to pm_gateup_kernel's:
+// same prescale, same chunk order, same reduction.
+constexpr int kG1Warps = 4;
+constexpr int kXWords = 20;  // words per staged activation chunk
+
+template <int FMT, int CPL>
+__global__ void __launch_bounds__(kG1Warps * 32, CPL <= 2 ? 8 : 5) pm_gateup1_kernel(DecArgs a, int gshift) {
+  __shared__ __align__(16) uint32_t xsm[32 * CPL * kXWords];
+  __shared__ float s_max[kG1Warps];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int p = blockIdx.y;
+  const int H = a.H, HC = H / 32;
+  const int r = blockIdx.x * kG1Warps + warp;
+  const uint8_t* blk = pair_block(a, p, blockIdx.x == 0 && tid == 0);
+  if (blk == nullptr) return;  // masked (the whole CTA): down skips this pair too
+  const uint32_t rowA = static_cast<uint32_t>(H / 2);
+  const uint32_t sbA = (FMT == FT_INT4) ? static_cast<uint32_t>((H / a.group) * 2) : static_cast<uint32_t>(H / 16);
+
+  // this thread's activation chunk (chunk tid; 32 * CPL <= 128 chunks) first:
+  // it is in L2 and arrives while the weights are in flight
+  const int t = p / a.k;
+  const bool has_x = tid < HC;
+  uint32_t raw[16];
+  if (has_x) {
+    const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * H + 32 * tid);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint4 q = __ldg(src + u);
+      raw[4 * u] = q.x; raw[4 * u + 1] = q.y; raw[4 * u + 2] = q.z; raw[4 * u + 3] = q.w;
+    }
+  }
+  // the warp's gate and up row chunks and scales, all in flight at once
+  uint4 w[2][CPL];
+  uint32_t sc[2][CPL];
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    const uint8_t* row = blk + a.off[m] + static_cast<uint64_t>(r) * rowA;
+    const uint8_t* srow = blk + a.off[3 + m] + static_cast<uint64_t>(r) * sbA;
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+      const int c = lane + 32 * j;
+      if (c < HC) {
+        w[m][j] = __ldg(reinterpret_cast<const uint4*>(row) + c);
+        sc[m][j] = load_scale<FMT>(srow, c, gshift);
+      }
+    }
+  }
+  // this CTA's share of the expert's down matrix and scales goes to L2 now
+  // (cache slots only; pool entries stay on the host path)
+  if (tid == 0 && blk >= a.cache && blk < a.cache + a.cblocks * a.cstride) {
+    const uint64_t dbytes = static_cast<uint64_t>(H) * (a.I / 2);
+    const uint64_t dsb = (FMT == FT_INT4) ? static_cast<uint64_t>(H) * (a.I / a.group) * 2 : static_cast<uint64_t>(H) * (a.I / 16);
+    const uint64_t c0 = (dbytes / gridDim.x + 15) & ~15ull, c1 = (dsb / gridDim.x + 15) & ~15ull;
+    const uint64_t o0 = c0 * blockIdx.x, o1 = c1 * blockIdx.x;
+    if (o0 < dbytes) l2_prefetch(blk + a.off[2] + o0, static_cast<uint32_t>(min(c0, dbytes - o0)));
+    if (o1 < dsb) l2_prefetch(blk + a.off[5] + o1, static_cast<uint32_t>(min(c1, dsb - o1)));
+  }
+  float ts0 = 1.f, ts1 = 1.f;
+  if constexpr (FMT == FT_NVFP4) {
+    const int64_t fid = static_cast<int64_t>(a.layer) * a.E + a.raw_ids[p];
+    ts0 = __ldg(a.tscale + 3 * fid + 0);
+    ts1 = __ldg(a.tscale + 3 * fid + 1);
+  }
+
+  // activations -> f16 words in shared memory, exact power-of-two prescale
+  // from the token's largest magnitude
+  float mx = 0.f;
+  if (has_x)
+#pragma unroll
+    for (int i = 0; i < 16; ++i) mx = fmaxf(mx, fmaxf(fabsf(bf16_lo(raw[i])), fabsf(bf16_hi(raw[i]))));
+  mx = warp_max(mx);
+  if (lane == 0) s_max[warp] = mx;
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < kG1Warps; ++i) mx = fmaxf(mx, s_max[i]);
+  const float mul = f16_prescale(mx);
+  if (has_x) {
+    uint32_t o[16];
+    const float sum = pack32<FMT>(raw, mul, o);
+    uint32_t* dst = xsm + tid * kXWords;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<uint4*>(dst + 4 * q) = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+    dst[16] = __float_as_uint(sum);
+  }
+  __syncthreads();
+  const float inv = 1.f / mul;
+  ts0 *= inv;
+  ts1 *= inv;
+
+  float g = 0.f, u = 0.f;
+#pragma unroll
+  for (int j = 0; j < CPL; ++j) {
+    const int c = lane + 32 * j;
+    if (c < HC) {
+      const uint32_t* src = xsm + c * kXWords;
+      uint32_t xa[16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src + 4 * q);
+        xa[4 * q] = v.x; xa[4 * q + 1] = v.y; xa[4 * q + 2] = v.z; xa[4 * q + 3] = v.w;
+      }
+      const float asum = __uint_as_float(src[16]);
+      g += chunk_dot<FMT>(w[0][j], sc[0][j], xa, asum);
+      u += chunk_dot<FMT>(w[1][j], sc[1][j], xa, asum);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    g += __shfl_xor_sync(0xffffffffu, g, o);
+    u += __shfl_xor_sync(0xffffffffu, u, o);
+  }
+  if (lane == 0) {
+    g *= ts0;
+    u *= ts1;
+    a.h[static_cast<size_t>(p) * a.I + r] = g / (1.f + expf(-g)) * u;
+  }
+}
+
 // ------------------------------------------------------------------ down ---
+// One warp stages pair p's intermediate row (I fp32 values from the gate/up
+// grid) in shared memory as slot j: f16 chunks in the format's order at
+// hsm + (j*IC + c)*kChunkBytes, their sums in hsum[j*IC + c], with an exact
+// power-of-two prescale from the row's largest magnitude, which s_wq[j]
+// (the pair's combine weight) absorbs.
+template <int FMT>
+__device__ __forceinline__ void stage_h(const DecArgs& a, int p, int j, uint8_t* hsm, float* hsum, float* s_wq) {
+  const int lane = threadIdx.x & 31;
+  const int I = a.I, IC = I / 32;
+  const float* hp = a.h + static_cast<size_t>(p) * I;
+  float v[32];
+  float m = 0.f;
+  if (lane < IC) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 f = *reinterpret_cast<const float4*>(hp + 32 * lane + 4 * q);
+      v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
+  }
+  for (int c = lane + 32; c < IC; c += 32) {  // I > 1024: a first pass for the max
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 f = *reinterpret_cast<const float4*>(hp + 32 * c + 4 * q);
+      m = fmaxf(m, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
+    }
+  }
+  const float mul = f16_prescale(warp_max(m));
+  if (lane == 0) s_wq[j] /= mul;
+  uint32_t o[16];
+  if (lane < IC) {
+    hsum[j * IC + lane] = pack32<FMT>(v, mul, o);
+    uint8_t* dst = hsm + static_cast<size_t>(j * IC + lane) * kChunkBytes;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<uint4*>(dst + 16 * q) = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+  }
+  for (int c = lane + 32; c < IC; c += 32) {  // the second read hits L1
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 f = *reinterpret_cast<const float4*>(hp + 32 * c + 4 * q);
+      v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
+    }
+    hsum[j * IC + c] = pack32<FMT>(v, mul, o);
+    uint8_t* dst = hsm + static_cast<size_t>(j * IC + c) * kChunkBytes;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<uint4*>(dst + 16 * q) = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+  }
+}
+
 // LPR lanes per output row (a power of two covering I/32 chunks, CPL chunks
 // per lane); a CTA owns 8 * 32 / LPR rows of one token.
 template <int FMT, int LPR, int CPL>
@@ -369,50 +553,8 @@ __global__ void __launch_bounds__(kThreads, 2) pm_down_kernel(DecArgs a, int gsh
       // h comes from the gate/up grid: wait for it, then stage this token's
       // k rows as f16 chunks (one warp per pair)
       pdl_wait();
-      for (int j = warp; j < k; j += kWarps) {
-        if (s_blk[j] == nullptr) continue;
-        const float* hp = a.h + static_cast<size_t>(t * k + j) * I;
-        float v[32];
-        float m = 0.f;
-        if (lane < IC) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 f = *reinterpret_cast<const float4*>(hp + 32 * lane + 4 * q);
-            v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
-          }
-#pragma unroll
-          for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
-        }
-        for (int c = lane + 32; c < IC; c += 32) {  // I > 1024: a first pass for the max
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 f = *reinterpret_cast<const float4*>(hp + 32 * c + 4 * q);
-            m = fmaxf(m, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
-          }
-        }
-        const float mul = f16_prescale(warp_max(m));
-        if (lane == 0) s_wq[j] /= mul;
-        uint32_t o[16];
-        if (lane < IC) {
-          hsum[j * IC + lane] = pack32<FMT>(v, mul, o);
-          uint8_t* dst = hsm + static_cast<size_t>(j * IC + lane) * kChunkBytes;
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(dst + 16 * q) = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-        }
-        for (int c = lane + 32; c < IC; c += 32) {  // the second read hits L1
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 f = *reinterpret_cast<const float4*>(hp + 32 * c + 4 * q);
-            v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
-          }
-          hsum[j * IC + c] = pack32<FMT>(v, mul, o);
-          uint8_t* dst = hsm + static_cast<size_t>(j * IC + c) * kChunkBytes;
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(dst + 16 * q) = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-        }
-      }
+      for (int j = warp; j < k; j += kWarps)
+        if (s_blk[j] != nullptr) stage_h<FMT>(a, t * k + j, j, hsm, hsum, s_wq);
       __syncthreads();
     }
 #pragma unroll
@@ -463,6 +605,22 @@ ft_status launch_gateup(const DecArgs& a, int gshift, cudaStream_t s) {
   return launch_check("experts decode gate/up");
 }
 
+template <int FMT, int CPL>
+ft_status launch_gateup1(const DecArgs& a, int gshift, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.I / kG1Warps, a.T * a.k);
+  cfg.blockDim = dim3(kG1Warps * 32);
+  cfg.stream = s;
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, pm_gateup1_kernel<FMT, CPL>, a, gshift);
+  if (e != cudaSuccess) return fail(FT_ERR_CUDA, "experts decode gate/up: %s", cudaGetErrorString(e));
+  return launch_check("experts decode gate/up");
+}
+
 template <int FMT, int LPR, int CPL>
 ft_status launch_down(const DecArgs& a, int gshift, cudaStream_t s) {
   const size_t smem = static_cast<size_t>(a.k) * (a.I / 32) * (kChunkBytes + 4);
@@ -490,10 +648,21 @@ template <int FMT>
 ft_status launch_pm(const DecArgs& a, int gshift, cudaStream_t s) {
   const int HC = a.H / 32, IC = a.I / 32;
   ft_status st;
-  // gate/up: chunks per lane x rows per warp = 4 pairs of 16-byte loads
-  if (HC <= 32) st = launch_gateup<FMT, 1, 4>(a, gshift, s);
-  else if (HC <= 64) st = launch_gateup<FMT, 2, 4>(a, gshift, s);
-  else st = launch_gateup<FMT, 4, 1>(a, gshift, s);
+  // gate/up: with few pairs (up to 16) the four-rows-per-warp grid leaves
+  // most SMs idle or nearly so, and one row per warp is faster (d35b, one
+  // token: 10.5 against 13.3 us per experts call in a 40-layer graph); with
+  // more pairs the grids are full and four rows per warp do less work in all
+  // (eight tokens: 43.9 against 45.2 us).
+  if (a.T * a.k <= 16 || a.I % (kWarps * 4) != 0 || HC > 64) {
+    if (HC <= 32) st = launch_gateup1<FMT, 1>(a, gshift, s);
+    else if (HC <= 64) st = launch_gateup1<FMT, 2>(a, gshift, s);
+    else if (HC <= 96) st = launch_gateup1<FMT, 3>(a, gshift, s);
+    else st = launch_gateup1<FMT, 4>(a, gshift, s);
+  } else if (HC <= 32) {
+    st = launch_gateup<FMT, 1, 4>(a, gshift, s);
+  } else {
+    st = launch_gateup<FMT, 2, 4>(a, gshift, s);
+  }
   if (st != FT_OK) return st;
   // down: lanes per row
   if (IC <= 8) return launch_down<FMT, 8, 1>(a, gshift, s);
@@ -510,8 +679,7 @@ ft_status launch_pm(const DecArgs& a, int gshift, cudaStream_t s) {
 ft_status decode_streaming(const DecArgs& a, cudaStream_t s) {
   const int HC = a.H / 32, IC = a.I / 32;
   if (HC > 128 || IC > 128 || a.T * a.k > kMaxPairs || a.T > 65535) return FT_ERR_UNSUPPORTED;
-  const int rpw = HC <= 64 ? 4 : 1;
-  if (a.I % (kWarps * rpw)) return FT_ERR_UNSUPPORTED;
+  if (a.I % kG1Warps) return FT_ERR_UNSUPPORTED;
   const int lpr = IC <= 8 ? 8 : (IC <= 16 ? 16 : 32);
   if (a.H % (kWarps * (32 / lpr))) return FT_ERR_UNSUPPORTED;
   const int gshift = (a.fmt == FT_INT4) ? (a.group == 32 ? 0 : (a.group == 64 ? 1 : 2)) : 0;
