@@ -38,7 +38,7 @@ METRIC = "MoE-layer tokens/s; decode expert-weight HBM GB/s; prefill grouped-GEM
 # an ncu capture of the same kernels on this workload's shape, L2 kept
 # between the kernels (`bench.py --case decode --tokens T` under
 # `ncu --cache-control none`, summarised under profiles/)
-TRAFFIC_PER_CALL = {1: 13_377_280, 8: 103_692_544}
+TRAFFIC_PER_CALL = {1: 13_372_672, 8: 104_289_536}
 UNIT = "MoE-layer tokens/s"
 
 

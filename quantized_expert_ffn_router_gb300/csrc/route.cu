@@ -39,23 +39,37 @@ __global__ void __launch_bounds__(256) route_rows_kernel(const uint16_t* __restr
   extern __shared__ float lsm[];  // last CTA: [min(T, 8)][E] logits
   __shared__ float part[8][TMAX];
   __shared__ int s_last;
-  pdl_wait();               // x may come from the previous kernel in the stream
-  pdl_launch_dependents();  // the next call (resolve) may start its launch now
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x;
   const float4* wrow = reinterpret_cast<const float4*>(W + static_cast<size_t>(e) * H);
   const int nch = H / 8;  // 8-element chunks
+  // The router weights are no kernel's output: the first chunks are
+  // requested before the wait for the previous kernel, so they arrive while
+  // it finishes (the previous layer's experts, started early by its
+  // programmatic launch).
+  float4 wa[2], wb[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int c = warp * 32 + u * 256 + lane;
+    if (c < nch) {
+      wa[u] = __ldg(wrow + 2 * c);
+      wb[u] = __ldg(wrow + 2 * c + 1);
+    }
+  }
+  pdl_wait();               // x may come from the previous kernel in the stream
+  pdl_launch_dependents();  // the next call (resolve) may start its launch now
   float acc[TMAX];
 #pragma unroll
   for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
   for (int c0 = warp * 32; c0 < nch; c0 += 256 * 2) {
-    float4 wa[2], wb[2];
+    if (c0 != warp * 32) {
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int c = c0 + u * 256 + lane;
-      if (c < nch) {
-        wa[u] = __ldg(wrow + 2 * c);
-        wb[u] = __ldg(wrow + 2 * c + 1);
+      for (int u = 0; u < 2; ++u) {
+        const int c = c0 + u * 256 + lane;
+        if (c < nch) {
+          wa[u] = __ldg(wrow + 2 * c);
+          wb[u] = __ldg(wrow + 2 * c + 1);
+        }
       }
     }
 #pragma unroll
