@@ -108,12 +108,18 @@ __global__ void __launch_bounds__(256) route_rows_kernel(const uint16_t* __restr
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();  // this CTA's logits before its arrival
-    s_last = atomicInc(counter, gridDim.x - 1) == gridDim.x - 1;
+    // the arrival releases this CTA's logits (written before the barrier
+    // above) and, for the last CTA, acquires every other CTA's: one
+    // acquire-release atomic instead of a fence on each side
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.inc.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(counter), "r"(gridDim.x - 1)
+                 : "memory");
+    s_last = old == gridDim.x - 1;
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();  // every other CTA's logits after their arrivals
   for (int t = warp; t < T; t += 8)
     topk_any(logits + static_cast<size_t>(t) * E, lsm + static_cast<size_t>(warp) * E, E, k, renorm,
              ids + static_cast<size_t>(t) * k, wts + static_cast<size_t>(t) * k);
