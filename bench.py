@@ -166,8 +166,11 @@ class DecodeWorkload:
         self.block, self.offs = ft.block_bytes(cfg.fmt, H, I, g)
         stride = self.block
         t0 = time.time()
-        # pool: the source of truth, pinned host memory, indexed by flat id
         n_fid = L * E
+        if cfg.slots >= n_fid:
+            self._init_resident(cfg, T, n_steps, device, log)
+            return
+        # pool: the source of truth, pinned host memory, indexed by flat id
         self.pool = torch.empty((n_fid, stride), dtype=torch.uint8, pin_memory=True)
         chunk = 128
         tmp = torch.empty((chunk, stride), dtype=torch.uint8, device=device)
@@ -213,6 +216,59 @@ class DecodeWorkload:
         self.x_stage = torch.empty((L, T, H), dtype=torch.int16, device=device)
         self.out = torch.empty((L, T, H), dtype=torch.int16, device=device)
         # per-layer buffers
+        self.ids = torch.empty((L, T, k), dtype=torch.int32, device=device)
+        self.w = torch.empty((L, T, k), dtype=torch.float32, device=device)
+        self.slot = torch.empty((L, T, k), dtype=torch.int32, device=device)
+        self.nf = torch.zeros((L, 1), dtype=torch.int32, device=device)
+        self.ml = T * k
+        self.ff = torch.empty((L, self.ml), dtype=torch.int32, device=device)
+        self.fs = torch.empty((L, self.ml), dtype=torch.int32, device=device)
+        self.rws = torch.zeros(ft.route_workspace(T, E), dtype=torch.uint8, device=device)
+        self.ews = torch.zeros(ft.experts_workspace(ft.FT_DECODE, T, k, H, I, E), dtype=torch.uint8,
+                               device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def _init_resident(self, cfg, T, n_steps, device, log):
+        """A cache holding every (layer, expert) block (flash: 24,576 x
+        2,764,800 B = 67.9 GB of HBM): slot f holds flat id f, so the cache
+        bank doubles as the pool (nothing is ever fetched) and the state is
+        the identity map; no pinned pool, no history."""
+        import torch
+
+        import synth
+
+        ft = self.ft
+        L, E, k, H, I, g = cfg.L, cfg.E, cfg.k, cfg.H, cfg.I, cfg.g
+        n_fid = L * E
+        t0 = time.time()
+        self.S = n_fid
+        self.pool = None
+        self.cache = torch.empty((n_fid, self.block), dtype=torch.uint8, device=device)
+        for f0 in range(0, n_fid, 256):
+            n = min(256, n_fid - f0)
+            synth.bank_blocks_torch(cfg.seed, range(f0, f0 + n), cfg.fmt, H, I, g, self.cache[f0:f0 + n],
+                                    ref_K=cfg.ref_K)
+        torch.cuda.synchronize()
+        ts = synth.tensor_scales(cfg.fmt, H, I, n_fid)
+        self.tscale = None if ts is None else torch.from_numpy(ts).to(device)
+        self.cache_b = ft.make_bank(cfg.fmt, H, I, g, self.cache, self.tscale)
+        self.pool_b = self.cache_b
+        self.W = torch.stack([torch.from_numpy(synth.router_weights(cfg.seed, l, E, H, cfg.router_std,
+                                                                    zipf_bias=cfg.zipf))
+                              for l in range(L)]).to(device)
+        self.state = ft.DeviceCacheState(L, E, self.S, device=device)
+        ident = torch.arange(n_fid, dtype=torch.int32, device=device)
+        self.state.slot_owner[:n_fid].copy_(ident)
+        self.state.map.copy_(ident)
+        self.state.usage[:n_fid].zero_()
+        self.state.recency.zero_()
+        self.state.step.fill_(1)
+        log(f"resident cache {n_fid} x {self.block} B ({n_fid * self.block / 1e9:.1f} GB) generated in "
+            f"{time.time() - t0:.1f}s")
+        self.x_host = step_inputs(cfg, T, n_steps)
+        self.x_all = self.x_host.to(device)
+        self.x_stage = torch.empty((L, T, H), dtype=torch.int16, device=device)
+        self.out = torch.empty((L, T, H), dtype=torch.int16, device=device)
         self.ids = torch.empty((L, T, k), dtype=torch.int32, device=device)
         self.w = torch.empty((L, T, k), dtype=torch.float32, device=device)
         self.slot = torch.empty((L, T, k), dtype=torch.int32, device=device)
@@ -509,6 +565,41 @@ def run_reference(args, cfg, T):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------- flash decode -----
+def flash_bench(steps: int, warmup: int, device, log=print):
+    """The NVFP4 decode step of the flash config (48 layers x 512 experts,
+    top-10, H 2560, I 640, 2,764,800 B per expert block), every expert
+    resident in HBM (67.9 GB), one token per step: route, resolve (all hits),
+    fetch (nothing), experts per layer, captured in one CUDA graph; the same
+    timing as the headline decode line."""
+    import torch
+
+    import synth
+
+    cfg = synth.get_config("flash")
+    n_steps = warmup + steps + 5
+    wl = DecodeWorkload(cfg, 1, 65536, n_steps, device, log)
+    wl.capture()
+    wl.settle(8)
+    secs = time_device(wl, steps, warmup, None, 1)
+    exp_us = wl.experts_us()
+    ebytes = wl.distinct_expert_bytes()
+    st = wl.ft.get_status(wl.status)
+    if st != 0:
+        raise RuntimeError(f"device status {st} during the flash decode benchmark")
+    per_call = ebytes / cfg.L
+    res = {"workload": "flash-shaped NVFP4 decode: 48 layers x 512 experts, top-10, H2560, I640 "
+                       "(2,764,800 B/expert), every expert resident (67.9 GB), T=1",
+           "value": cfg.L * steps / secs, "unit": UNIT, "ms_per_step": secs / steps * 1e3,
+           "model_tokens_per_s": steps / secs,
+           "experts_us_per_call": exp_us, "expert_bytes_per_call": per_call,
+           "experts_GBs": per_call / (exp_us * 1e-6) / 1e9 if exp_us else None}
+    log(f"flash T=1: {res['value']:.1f} {UNIT}, {res['ms_per_step']:.3f} ms/step, experts {exp_us:.1f} us/call")
+    del wl
+    torch.cuda.empty_cache()
+    return res
+
+
 # ------------------------------------------------------------ prefill -----
 def prefill_bench(T: int, steps: int, warmup: int, device, log=print, state=None):
     """One prefill MoE layer of the prefill config (NVFP4, H 4096, I 2048,
@@ -746,6 +837,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--extra-batch", type=int, default=8, help="also time this batch (0: off)")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill layer measurement")
+    ap.add_argument("--no-flash", action="store_true", help="skip the NVFP4 (flash) decode measurement")
     ap.add_argument("--prefill-layers", type=int, default=3,
                     help="layers streamed from host memory through the prefill double buffer (0: skip)")
     ap.add_argument("--case", choices=["decode", "decode-flash", "prefill"],
@@ -830,6 +922,12 @@ def main():
         if args.prefill_layers > 0:
             prefill["streamed"] = prefill_pipeline_bench(synth.get_config("prefill").tokens[0], args.prefill_layers,
                                                          device, log)
+    flash = None
+    if not args.no_flash:
+        if args.no_prefill:
+            del wl
+        torch.cuda.empty_cache()
+        flash = flash_bench(max(3, min(args.steps, 100)), args.warmup, device, log)
     if rank != 0:
         return
     peaks, peak_kind = measured_peaks()
@@ -893,6 +991,9 @@ def main():
                 "by_tokens": {t: dict(v, tensor_frac=v["grouped_gemm_tflops"] / peaks["bf16_tflops"])
                               for t, v in prefill.items() if t != "streamed"},
                 "streamed_from_host": prefill.get("streamed")},
+            "flash_nvfp4_decode": None if flash is None else dict(
+                flash, experts_frac_of_hbm=(flash["experts_GBs"] / peaks["hbm_gbs"]
+                                            if flash["experts_GBs"] else None)),
             "other_batches": {str(T): {"value": v["value"], "ms_per_step": v["secs"] / args.steps * 1e3,
                                        "per_op_us_per_step": v["kt"], "expert_bytes_per_step": v["ebytes"],
                                        "experts_us_per_call": v["exp_us"],

@@ -10,9 +10,9 @@
 //     those gate and up rows and their scales at once, then converts the
 //     token's activations to f16 in registers (exact per-token power-of-two
 //     prescale), dots, reduces with shuffles, and lane r writes row r's
-//     h = silu(g) * u to the fp32 workspace.  When its grid is resident in one
-//     wave (one token at 35B shapes) a second form runs one row per warp in
-//     4-warp CTAs, the activations
+//     h = silu(g) * u to the fp32 workspace.  For rows wider than 2048, and
+//     when its grid is resident in one wave (one token at 35B shapes), a
+//     second form runs one row per warp in 4-warp CTAs, the activations
 //     converted once per CTA into shared memory: four times the warps, each
 //     with a quarter of the dependent dequant-dot instructions, which is what
 //     bounds a one-token layer (same h, bit for bit).
@@ -324,7 +324,7 @@ constexpr int kG1Warps = 4;
 constexpr int kXWords = 20;  // words per staged activation chunk
 
 template <int FMT, int CPL>
-__global__ void __launch_bounds__(kG1Warps * 32, 8) pm_gateup1_kernel(DecArgs a, int gshift) {
+__global__ void __launch_bounds__(kG1Warps * 32, CPL <= 2 ? 8 : 5) pm_gateup1_kernel(DecArgs a, int gshift) {
   __shared__ __align__(16) uint32_t xsm[32 * CPL * kXWords];
   __shared__ float s_max[kG1Warps];
   pdl_wait();
@@ -656,17 +656,20 @@ int num_sms_dec() {
   return n;
 }
 
-// The one-row gate/up kernel runs when its grid is resident in one wave (8
-// CTAs per SM): then it beats four rows per warp, whose grid leaves most SMs
-// idle or nearly so (d35b, one token: 10.5 against 13.3 us per experts call
-// in a 40-layer graph).  Larger calls keep four rows per warp: their grids
-// fill the GPU, and the dequant-dot instructions, fewer with four rows per
-// warp, bound them (eight tokens: 43.9 against 45.2 us with one row per
+// Which gate/up kernel runs.  Rows wider than 2048 always take the one-row
+// kernel: the other form has one row per warp there too, and converts the
+// activations in every warp (flash, one token: 23.1 against 28.5 us per
+// experts call in a 48-layer graph).  Up to 2048 the one-row kernel runs
+// when its grid is resident in one wave (8 CTAs per SM): then it beats four
+// rows per warp, whose grid leaves most SMs idle or nearly so (d35b, one
+// token: 10.5 against 13.3 us).  Larger calls keep four rows per warp: their
+// grids fill the GPU, and the dequant-dot instructions, fewer with four rows
+// per warp, bound them (eight tokens: 43.9 against 45.2 us with one row per
 // warp, 43.6 with a double-buffered loop over 16 rows per warp).
 bool gateup_one_row(const DecArgs& a) {
   const int HC = a.H / 32;
-  return HC <= 64 && a.I % kG1Warps == 0 &&
-         static_cast<int64_t>(a.I / kG1Warps) * a.T * a.k <= 8ll * num_sms_dec();
+  if (HC > 128 || a.I % kG1Warps != 0) return false;
+  return HC > 64 || static_cast<int64_t>(a.I / kG1Warps) * a.T * a.k <= 8ll * num_sms_dec();
 }
 
 template <int FMT>
@@ -678,13 +681,13 @@ ft_status launch_pm(const DecArgs& a, int gshift, cudaStream_t s) {
   // rows wider than 2048): see gateup_one_row.
   if (gateup_one_row(a)) {
     if (HC <= 32) st = launch_gateup1<FMT, 1>(a, gshift, s);
-    else st = launch_gateup1<FMT, 2>(a, gshift, s);
+    else if (HC <= 64) st = launch_gateup1<FMT, 2>(a, gshift, s);
+    else if (HC <= 96) st = launch_gateup1<FMT, 3>(a, gshift, s);
+    else st = launch_gateup1<FMT, 4>(a, gshift, s);
   } else if (HC <= 32) {
     st = launch_gateup<FMT, 1, 4>(a, gshift, s);
-  } else if (HC <= 64) {
-    st = launch_gateup<FMT, 2, 4>(a, gshift, s);
   } else {
-    st = launch_gateup<FMT, 4, 1>(a, gshift, s);
+    st = launch_gateup<FMT, 2, 4>(a, gshift, s);
   }
   if (st != FT_OK) return st;
   // down: lanes per row
@@ -702,7 +705,7 @@ ft_status launch_pm(const DecArgs& a, int gshift, cudaStream_t s) {
 ft_status decode_streaming(const DecArgs& a, cudaStream_t s) {
   const int HC = a.H / 32, IC = a.I / 32;
   if (HC > 128 || IC > 128 || a.T * a.k > kMaxPairs || a.T > 65535) return FT_ERR_UNSUPPORTED;
-  if (!gateup_one_row(a) && a.I % (kWarps * (HC <= 64 ? 4 : 1)) != 0) return FT_ERR_UNSUPPORTED;
+  if (!gateup_one_row(a) && (HC > 64 || a.I % (kWarps * 4) != 0)) return FT_ERR_UNSUPPORTED;
   const int lpr = IC <= 8 ? 8 : (IC <= 16 ? 16 : 32);
   if (a.H % (kWarps * (32 / lpr))) return FT_ERR_UNSUPPORTED;
   const int gshift = (a.fmt == FT_INT4) ? (a.group == 32 ? 0 : (a.group == 64 ? 1 : 2)) : 0;
