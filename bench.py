@@ -39,6 +39,9 @@ METRIC = "MoE-layer tokens/s; decode expert-weight HBM GB/s; prefill grouped-GEM
 # between the kernels (`bench.py --case decode --tokens T` under
 # `ncu --cache-control none`, summarised under profiles/)
 TRAFFIC_PER_CALL = {1: 13_372_672, 8: 104_289_536}
+# the same for one flash-shaped NVFP4 decode experts call at T = 1
+# (`bench.py --case decode-flash --tokens 1`)
+FLASH_TRAFFIC_PER_CALL = 27_660_544
 UNIT = "MoE-layer tokens/s"
 
 
@@ -593,6 +596,7 @@ def flash_bench(steps: int, warmup: int, device, log=print):
            "value": cfg.L * steps / secs, "unit": UNIT, "ms_per_step": secs / steps * 1e3,
            "model_tokens_per_s": steps / secs,
            "experts_us_per_call": exp_us, "expert_bytes_per_call": per_call,
+           "experts_traffic_per_call": FLASH_TRAFFIC_PER_CALL,
            "experts_GBs": per_call / (exp_us * 1e-6) / 1e9 if exp_us else None}
     log(f"flash T=1: {res['value']:.1f} {UNIT}, {res['ms_per_step']:.3f} ms/step, experts {exp_us:.1f} us/call")
     del wl
@@ -682,7 +686,7 @@ def prefill_bench(T: int, steps: int, warmup: int, device, log=print, state=None
     return res, state
 
 
-def prefill_pipeline_bench(T: int, n_layers: int, device, log=print, reps: int = 2):
+def prefill_pipeline_bench(T: int, n_layers: int, device, log=print, reps: int = 4):
     """Prefill of n_layers consecutive layers of the prefill config with the
     experts streamed from pinned host memory through the whole-layer double
     buffer (pipeline.PrefillLayers: each layer copied by the copy engine into
