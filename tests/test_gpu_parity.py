@@ -315,9 +315,11 @@ def _decode_case(ft, cfg, T, layer, cached_frac, use_pool, pool_pinned=False, ou
 
 
 @pytest.mark.parametrize("name,T", [("tiny", 1), ("tiny", 8), ("tiny", 12), ("d35b", 1), ("d35b", 3), ("d35b", 8),
-                                    ("d35b", 16), ("flash", 1), ("flash", 2), ("flash", 9)])
+                                    ("d35b", 16), ("flash", 1), ("flash", 2), ("flash", 9), ("prefill", 1),
+                                    ("prefill", 2)])
 def test_experts_decode_all_cached(cuda_lib, name, T):
-    """Every batch size up to 16 runs the pair-major kernels."""
+    """Every batch size up to 16 runs the pair-major kernels (the prefill
+    bank's 4096-wide rows at decode: the widest one-row gate/up form)."""
     cfg = synth.get_config(name)
     got, ref, *_ = _decode_case(cuda_lib, cfg, T, layer=1 % cfg.L, cached_frac=1.0, use_pool=False)
     assert_close(got, ref, f"{name} T={T}")
