@@ -38,7 +38,7 @@ METRIC = "MoE-layer tokens/s; decode expert-weight HBM GB/s; prefill grouped-GEM
 # an ncu capture of the same kernels on this workload's shape, L2 kept
 # between the kernels (`bench.py --case decode --tokens T` under
 # `ncu --cache-control none`, summarised under profiles/)
-TRAFFIC_PER_CALL = {1: 13_372_672, 8: 104_289_536}
+TRAFFIC_PER_CALL = {1: 13_372_928, 8: 104_289_536}
 # the same for one flash-shaped NVFP4 decode experts call at T = 1
 # (`bench.py --case decode-flash --tokens 1`)
 FLASH_TRAFFIC_PER_CALL = 27_660_544

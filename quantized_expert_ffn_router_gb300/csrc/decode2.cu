@@ -22,7 +22,9 @@
 //     asked L2 for them; they do not depend on h), then griddepcontrol.wait,
 //     stage the token's k intermediates in shared memory as f16 (exact
 //     power-of-two prescale per pair), and accumulate the top-k weighted sum
-//     of every row in a fixed order (the combine is fused, no atomics).
+//     of every row in a fixed order (the combine is fused, no atomics).  For
+//     one-token calls with rows of 9-16 chunks a second form gives each warp
+//     one row and splits the pairs over the warp's two halves.
 //
 // Pairs are not grouped by expert: two pairs of one expert read its rows
 // twice, and the second read is served by L2 since both are in flight
@@ -590,6 +592,96 @@ __global__ void __launch_bounds__(kThreads, 2) pm_down_kernel(DecArgs a, int gsh
   }
 }
 
+// ------------------------------------------------------ down, half pairs ---
+// pm_down_kernel with one row per warp and the token's pairs split over the
+// warp's two 16-lane halves (half h dots pairs h, h + 2, ...; rows of at
+// most 16 chunks), the halves' sums added with one shuffle: twice the warps
+// on a grid that would otherwise run one 8-warp CTA per SM or fewer, each
+// lane with half the dependent chunk dots.  The staging of h and the weight
+// loads before the wait are pm_down_kernel's.
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 2) pm_down2_kernel(DecArgs a, int gshift) {
+  constexpr int LPR = 16;
+  constexpr int NB = kDownLoads;  // pairs whose chunk a lane holds at once
+  extern __shared__ __align__(16) uint8_t hsm[];  // [k][I/32] f16 chunks, then [k][I/32] sums
+  __shared__ const uint8_t* s_blk[kMaxPairs];
+  __shared__ float s_wq[kMaxPairs];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t = blockIdx.y, k = a.k;
+  const int H = a.H, I = a.I, IC = I / 32;
+  const int row = blockIdx.x * kWarps + warp;
+  const int half = lane / LPR, sub = lane % LPR;
+  // the next call (the next layer's router) may start its launch now: it
+  // waits for this grid before it reads anything
+  pdl_launch_dependents();
+  const uint32_t rowB = static_cast<uint32_t>(I / 2);
+  const uint32_t sbB = (FMT == FT_INT4) ? static_cast<uint32_t>((I / a.group) * 2) : static_cast<uint32_t>(I / 16);
+  float* hsum = reinterpret_cast<float*>(hsm + static_cast<size_t>(k) * IC * kChunkBytes);
+
+  for (int j = tid; j < k; j += kThreads) {
+    const int p = t * k + j;
+    const uint8_t* blk = pair_block(a, p, false);
+    s_blk[j] = blk;
+    float wq = 0.f;
+    if (blk != nullptr) {
+      wq = a.topk_w[p];
+      if constexpr (FMT == FT_NVFP4)
+        wq *= __ldg(a.tscale + 3 * (static_cast<int64_t>(a.layer) * a.E + a.raw_ids[p]) + 2);
+    }
+    s_wq[j] = wq;
+  }
+  __syncthreads();
+
+  uint4 w[NB];
+  uint32_t sc[NB];
+  auto load_batch = [&](int j0) {
+#pragma unroll
+    for (int e = 0; e < NB; ++e) {
+      const int j = j0 + 2 * e;
+      const uint8_t* blk = j < k ? s_blk[j] : nullptr;
+      if (blk != nullptr && sub < IC) {
+        w[e] = __ldg(reinterpret_cast<const uint4*>(blk + a.off[2] + static_cast<uint64_t>(row) * rowB) + sub);
+        sc[e] = load_scale<FMT>(blk + a.off[5] + static_cast<uint64_t>(row) * sbB, sub, gshift);
+      }
+    }
+  };
+  // the first pairs' weights do not depend on the previous grid
+  load_batch(half);
+  // h comes from the gate/up grid: wait for it, then stage the token's k
+  // rows as f16 chunks (one warp per pair)
+  pdl_wait();
+  for (int j = warp; j < k; j += kWarps)
+    if (s_blk[j] != nullptr) stage_h<FMT>(a, t * k + j, j, hsm, hsum, s_wq);
+  __syncthreads();
+
+  float acc = 0.f;
+  for (int j0 = half; j0 < k; j0 += 2 * NB) {
+    if (j0 != half) load_batch(j0);
+#pragma unroll
+    for (int e = 0; e < NB; ++e) {
+      const int j = j0 + 2 * e;
+      if (j < k && s_blk[j] != nullptr && sub < IC) {
+        const uint8_t* hp = hsm + static_cast<size_t>(j * IC + sub) * kChunkBytes;
+        uint32_t ha[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 v = *reinterpret_cast<const uint4*>(hp + 16 * q);
+          ha[4 * q] = v.x; ha[4 * q + 1] = v.y; ha[4 * q + 2] = v.z; ha[4 * q + 3] = v.w;
+        }
+        acc = fmaf(s_wq[j], chunk_dot<FMT>(w[e], sc[e], ha, hsum[j * IC + sub]), acc);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  acc += __shfl_xor_sync(0xffffffffu, acc, LPR);  // half 0's pairs + half 1's
+  if (lane == 0) {
+    const size_t idx = static_cast<size_t>(t) * H + row;
+    if (a.out_bf16) static_cast<uint16_t*>(a.out)[idx] = f32_to_bf16(acc);
+    else static_cast<float*>(a.out)[idx] = acc;
+  }
+}
+
 template <int FMT, int CPL, int RPW>
 ft_status launch_gateup(const DecArgs& a, int gshift, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
@@ -620,6 +712,29 @@ ft_status launch_gateup1(const DecArgs& a, int gshift, cudaStream_t s) {
   cudaError_t e = cudaLaunchKernelEx(&cfg, pm_gateup1_kernel<FMT, CPL>, a, gshift);
   if (e != cudaSuccess) return fail(FT_ERR_CUDA, "experts decode gate/up: %s", cudaGetErrorString(e));
   return launch_check("experts decode gate/up");
+}
+
+template <int FMT>
+ft_status launch_down2(const DecArgs& a, int gshift, cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(a.k) * (a.I / 32) * (kChunkBytes + 4);
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(pm_down2_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    attr = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.H / kWarps, a.T);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, pm_down2_kernel<FMT>, a, gshift);
+  if (e != cudaSuccess) return fail(FT_ERR_CUDA, "experts decode down: %s", cudaGetErrorString(e));
+  return launch_check("experts decode down");
 }
 
 template <int FMT, int LPR, int CPL>
@@ -690,7 +805,12 @@ ft_status launch_pm(const DecArgs& a, int gshift, cudaStream_t s) {
     st = launch_gateup<FMT, 2, 4>(a, gshift, s);
   }
   if (st != FT_OK) return st;
-  // down: lanes per row
+  // down: with rows of at most 16 chunks and a one-row-per-warp grid that
+  // is resident in one wave (2 CTAs per SM), the pairs split over warp
+  // halves; else lanes per row
+  if (IC <= 16 && IC > 8 && a.k >= 2 && a.H % kWarps == 0 &&
+      static_cast<int64_t>(a.H / kWarps) * a.T <= 2ll * num_sms_dec())
+    return launch_down2<FMT>(a, gshift, s);
   if (IC <= 8) return launch_down<FMT, 8, 1>(a, gshift, s);
   if (IC <= 16) return launch_down<FMT, 16, 1>(a, gshift, s);
   if (IC <= 32) return launch_down<FMT, 32, 1>(a, gshift, s);
