@@ -39,3 +39,11 @@ def test_fast_link_fetches_everything_slow_link_little():
     assert frac_q16_from_bandwidths(1e-12, 1e6) == 1
     with pytest.raises(ValueError):
         frac_q16_from_bandwidths(0.0, 1.0)
+
+
+def test_speculative_decode_needs_a_pool():
+    # the speculative copies come from the pool; refused before any device work
+    from quantized_expert_ffn_router_gb300.pipeline import SpeculativeDecode
+
+    with pytest.raises(ValueError):
+        SpeculativeDecode(None, None, None, 8, 2, 1)
