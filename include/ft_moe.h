@@ -158,8 +158,10 @@ FT_API ft_status ft_moe_get_status(const int32_t* dev_status, int32_t* out_host)
  *   renorm != 0).
  * x [T,H] bf16 row-major; w_router [E,H] fp32 row-major; topk_ids [T,k]
  * int32; topk_w [T,k] fp32.  ws: device scratch of ft_moe_route_workspace(T,E)
- * bytes: the logits, then (T <= 16, where one kernel computes the logits and
- * its last CTA the top-k) an arrival counter; ws must be zero-filled before
+ * bytes: an arrival counter in its first 256 bytes (T <= 16, where one
+ * kernel computes the logits and its last CTA the top-k), then the logits.
+ * The counter sits at the same place for every T, so one workspace sized for
+ * the largest T serves calls of any smaller T; ws must be zero-filled before
  * the first call that uses it, every call leaves the counter at zero, and
  * calls that may overlap on the GPU need separate workspaces.  Limits:
  * 1 <= k <= min(E, 32), E <= 4096, H % 8 == 0.  T == 0 is a no-op.
@@ -360,7 +362,10 @@ FT_API ft_status ft_moe_experts_fwd(const ft_bank* cache_host, const ft_bank* po
  * GPU that loads the library keeps the array until exit;
  * calls that may overlap on the GPU share the array and race, so the caller
  * serialises them; the first call on a device looks the array up (with that
- * device current) and should happen before any stream capture.
+ * device current) and should happen before any stream capture.  The address
+ * is kept for the life of the process, so the call must not be used on a
+ * device after cudaDeviceReset (or any other reset of its primary context)
+ * in the same process.
  */
 FT_API ft_status ft_moe_experts_decode_static(const ft_bank* cache_host, const ft_bank* pool_host,
                                               int32_t layer, int32_t E, const uint16_t* x, int32_t T,

@@ -222,22 +222,28 @@ int orc_dequant(const uint8_t* block, int fmt, int H, int I, int g, int which,
 }
 
 // ------------------------------------------------------------- q* split ----
-// [FT-KR] pattern 2 and [FT-ZH] sec. 6.  With phi = round(65536*B_P/B_H) and m
-// missed experts: when phi > 0, lo = floor(m*phi / 65536) and the number of
-// fetches is lo or lo+1, whichever has the smaller slower-branch cost
+// [FT-KR] pattern 2 and [FT-ZH] sec. 6.  phi = 65536*B_P/B_H in Q16; of m
+// missed experts, f are fetched (B_P) and m - f are computed on the host
+// path (B_H).  The two branches run side by side, so the step waits for the
+// slower one, whose time is proportional to
 //   cost(f) = max(f*(65536-phi), (m-f)*phi),
-// ties going to lo; the result is then capped at m.  When phi == 0 the cap is
-// not applied and every miss may be fetched.  Integer arithmetic in 64 bits.
+// and the split is the f in [0, m] that minimises it, the smallest such f
+// when several tie.  Written here as that definition: every f is tried.
+// When phi == 0 the pages apply no cap, and every miss may be fetched.
+// Integer arithmetic in 64 bits.
 int32_t orc_split_q16(int32_t m, int32_t phi) {
   if (m <= 0) return 0;
   if (phi <= 0) return m;
-  const int64_t q = 65536;
-  int64_t M = m, P = phi;
-  int64_t lo = (M * P) >> 16;
-  int64_t c_lo = std::max(lo * (q - P), (M - lo) * P);
-  int64_t c_hi = std::max((lo + 1) * (q - P), (M - lo - 1) * P);
-  int64_t max_fetch = (c_lo <= c_hi) ? lo : lo + 1;
-  return static_cast<int32_t>(std::min(M, max_fetch));
+  const int64_t q = 65536, P = phi;
+  int64_t best_f = 0, best_cost = -1;
+  for (int64_t f = 0; f <= m; ++f) {
+    const int64_t cost = std::max(f * (q - P), (static_cast<int64_t>(m) - f) * P);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_f = f;
+    }
+  }
+  return static_cast<int32_t>(best_f);
 }
 
 // The rule over a grid: out[(phi - phi_lo) * (m_max + 1) + m] for every

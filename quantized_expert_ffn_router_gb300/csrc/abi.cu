@@ -3,6 +3,10 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <atomic>
+#include <mutex>
+#include <vector>
+
 #include "ft_common.cuh"
 
 namespace ft {
@@ -22,6 +26,54 @@ ft_status fail(ft_status code, const char* fmt, ...) {
   vsnprintf(g_err, sizeof g_err, fmt, ap);
   va_end(ap);
   return code;
+}
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+
+struct SmemAttr {
+  const void* kernel;
+  int device;
+  int bytes;
+};
+std::mutex g_attr_mu;
+std::vector<SmemAttr> g_attrs;
+}  // namespace
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) dev = 0;
+  if (dev >= kMaxDevices) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+  }
+  int n = g_sm_count[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+    g_sm_count[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
+ft_status ensure_dyn_smem(const void* kernel, int bytes, const char* what) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(FT_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  for (const SmemAttr& a : g_attrs)
+    if (a.kernel == kernel && a.device == dev && a.bytes >= bytes) return FT_OK;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return fail(FT_ERR_CUDA, "%s: shared memory limit %d: %s", what, bytes, cudaGetErrorString(e));
+  for (SmemAttr& a : g_attrs)
+    if (a.kernel == kernel && a.device == dev) {
+      a.bytes = bytes;
+      return FT_OK;
+    }
+  g_attrs.push_back({kernel, dev, bytes});
+  return FT_OK;
 }
 
 ft_status launch_check(const char* what) {

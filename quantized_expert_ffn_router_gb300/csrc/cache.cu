@@ -66,18 +66,6 @@ __global__ void __launch_bounds__(kFetchThreads) fetch_kernel(
   }
 }
 
-int g_num_sms = 0;
-
-int num_sms() {
-  if (g_num_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g_num_sms <= 0) g_num_sms = 148;
-  }
-  return g_num_sms;
-}
-
 }  // namespace
 
 ft_status resolve_prepare(const ft_cache_state* st, int32_t layer, const int32_t* topk_ids, int32_t T,
@@ -152,10 +140,9 @@ namespace {
 // the previous kernel on the stream by programmatic launch.
 ft_status launch_resolve(const ft::ResolveArgs& a, size_t smem, void* stream, const char* what) {
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(ft::resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(ft::kResSmemCap));
-    if (e != cudaSuccess)
-      return ft::fail(FT_ERR_CUDA, "%s: smem attribute: %s", what, cudaGetErrorString(e));
+    ft_status st = ft::ensure_dyn_smem(reinterpret_cast<const void*>(ft::resolve_kernel),
+                                       static_cast<int>(ft::kResSmemCap), what);
+    if (st != FT_OK) return st;
   }
   // small calls usually finish in the one-warp path; 256 threads keep the
   // rest cheap to synchronise.  Larger calls get the whole block.
@@ -234,7 +221,7 @@ ft_status ft_moe_fetch(const ft_bank* pool, const ft_bank* cache, const int32_t*
   const uint64_t per = static_cast<uint64_t>(ft::kFetchThreads) * ft::kFetchVec;
   const uint64_t nchunks = (n16 + per - 1) / per;
   const uint64_t items = nchunks * static_cast<uint64_t>(max_list);
-  const int grid = static_cast<int>(std::min<uint64_t>(items, static_cast<uint64_t>(ft::num_sms())));
+  const int grid = static_cast<int>(std::min<uint64_t>(items, static_cast<uint64_t>(ft::device_sm_count())));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(ft::kFetchThreads);

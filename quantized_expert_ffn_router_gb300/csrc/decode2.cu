@@ -717,11 +717,9 @@ ft_status launch_gateup1(const DecArgs& a, int gshift, cudaStream_t s) {
 template <int FMT>
 ft_status launch_down2(const DecArgs& a, int gshift, cudaStream_t s) {
   const size_t smem = static_cast<size_t>(a.k) * (a.I / 32) * (kChunkBytes + 4);
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(pm_down2_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    attr = true;
-  }
+  ft_status st = ensure_dyn_smem(reinterpret_cast<const void*>(pm_down2_kernel<FMT>), 200 * 1024,
+                                 "experts decode down");
+  if (st != FT_OK) return st;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.H / kWarps, a.T);
   cfg.blockDim = dim3(kThreads);
@@ -740,11 +738,9 @@ ft_status launch_down2(const DecArgs& a, int gshift, cudaStream_t s) {
 template <int FMT, int LPR, int CPL>
 ft_status launch_down(const DecArgs& a, int gshift, cudaStream_t s) {
   const size_t smem = static_cast<size_t>(a.k) * (a.I / 32) * (kChunkBytes + 4);
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(pm_down_kernel<FMT, LPR, CPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    attr = true;
-  }
+  ft_status st = ensure_dyn_smem(reinterpret_cast<const void*>(pm_down_kernel<FMT, LPR, CPL>), 200 * 1024,
+                                 "experts decode down");
+  if (st != FT_OK) return st;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.H / (kWarps * (32 / LPR)), a.T);
   cfg.blockDim = dim3(kThreads);
@@ -760,17 +756,6 @@ ft_status launch_down(const DecArgs& a, int gshift, cudaStream_t s) {
   return launch_check("experts decode down");
 }
 
-int num_sms_dec() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
-
 // Which gate/up kernel runs.  Rows wider than 2048 always take the one-row
 // kernel: the other form has one row per warp there too, and converts the
 // activations in every warp (flash, one token: 23.1 against 28.5 us per
@@ -784,7 +769,7 @@ int num_sms_dec() {
 bool gateup_one_row(const DecArgs& a) {
   const int HC = a.H / 32;
   if (HC > 128 || a.I % kG1Warps != 0) return false;
-  return HC > 64 || static_cast<int64_t>(a.I / kG1Warps) * a.T * a.k <= 8ll * num_sms_dec();
+  return HC > 64 || static_cast<int64_t>(a.I / kG1Warps) * a.T * a.k <= 8ll * device_sm_count();
 }
 
 template <int FMT>
@@ -809,7 +794,7 @@ ft_status launch_pm(const DecArgs& a, int gshift, cudaStream_t s) {
   // is resident in one wave (2 CTAs per SM), the pairs split over warp
   // halves; else lanes per row
   if (IC <= 16 && IC > 8 && a.k >= 2 && a.H % kWarps == 0 &&
-      static_cast<int64_t>(a.H / kWarps) * a.T <= 2ll * num_sms_dec())
+      static_cast<int64_t>(a.H / kWarps) * a.T <= 2ll * device_sm_count())
     return launch_down2<FMT>(a, gshift, s);
   if (IC <= 8) return launch_down<FMT, 8, 1>(a, gshift, s);
   if (IC <= 16) return launch_down<FMT, 16, 1>(a, gshift, s);
@@ -820,14 +805,15 @@ ft_status launch_pm(const DecArgs& a, int gshift, cudaStream_t s) {
 
 }  // namespace
 
-// Launch the pair-major kernels; FT_ERR_UNSUPPORTED when the shape does not
-// fit them (the caller then uses the general kernels).
+// Launch the pair-major kernels; FT_ERR_UNSUPPORTED (with a message) for a
+// shape outside them, which the entry point's checks already exclude.
 ft_status decode_streaming(const DecArgs& a, cudaStream_t s) {
   const int HC = a.H / 32, IC = a.I / 32;
-  if (HC > 128 || IC > 128 || a.T * a.k > kMaxPairs || a.T > 65535) return FT_ERR_UNSUPPORTED;
-  if (!gateup_one_row(a) && (HC > 64 || a.I % (kWarps * 4) != 0)) return FT_ERR_UNSUPPORTED;
   const int lpr = IC <= 8 ? 8 : (IC <= 16 ? 16 : 32);
-  if (a.H % (kWarps * (32 / lpr))) return FT_ERR_UNSUPPORTED;
+  if (HC > 128 || IC > 128 || a.T * a.k > kMaxPairs || a.T > 65535 ||
+      (!gateup_one_row(a) && (HC > 64 || a.I % (kWarps * 4) != 0)) || a.H % (kWarps * (32 / lpr)))
+    return fail(FT_ERR_UNSUPPORTED, "experts decode: H=%d I=%d T=%d k=%d outside the decode kernels", a.H, a.I,
+                a.T, a.k);
   const int gshift = (a.fmt == FT_INT4) ? (a.group == 32 ? 0 : (a.group == 64 ? 1 : 2)) : 0;
   if (a.fmt == FT_INT4) return launch_pm<FT_INT4>(a, gshift, s);
   return launch_pm<FT_NVFP4>(a, gshift, s);

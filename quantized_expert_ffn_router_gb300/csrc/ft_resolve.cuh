@@ -66,19 +66,21 @@ ft_status resolve_prepare(const ft_cache_state* st, int32_t layer, const int32_t
 
 namespace {
 
-// The q* rule in Q16 fixed point: lo = floor(m*phi / 2^16); fetch lo or lo+1,
-// whichever gives the smaller slower-branch time max(f*(2^16-phi), (m-f)*phi)
-// (ties to lo), capped at m.  phi == 0 applies no cap.  64-bit intermediates.
+// The q* split in Q16 fixed point (phi = 2^16 * B_P / B_H).  Fetching f of
+// m misses costs max(f*(2^16-phi), (m-f)*phi): the larger of the copy time
+// and the host-path time, which run side by side.  The first term grows with
+// f and the second falls, so the minimum sits next to their crossing
+// f* = m*phi / 2^16.  With m*phi = 2^16*lo + r (0 <= r < 2^16), f = lo costs
+// (m-lo)*phi and f = lo+1 costs (lo+1)*(2^16-phi); the second is strictly
+// cheaper exactly when r + phi > 2^16, so that is when one more expert is
+// fetched (equal costs keep the smaller count).  lo+1 never exceeds m: lo = m
+// only at phi = 2^16, where r = 0.  phi == 0 applies no cap.
 __device__ __forceinline__ int32_t split_q16_dev(int32_t m, int32_t phi) {
   if (m <= 0) return 0;
   if (phi <= 0) return m;
-  const int64_t q = 65536;
-  const int64_t M = m, P = phi;
-  const int64_t lo = (M * P) >> 16;
-  const int64_t c_lo = max(lo * (q - P), (M - lo) * P);
-  const int64_t c_hi = max((lo + 1) * (q - P), (M - lo - 1) * P);
-  const int64_t f = (c_lo <= c_hi) ? lo : lo + 1;
-  return static_cast<int32_t>(min(M, f));
+  const uint64_t prod = static_cast<uint64_t>(m) * static_cast<uint32_t>(phi);
+  const uint32_t whole = static_cast<uint32_t>(prod >> 16), frac = static_cast<uint32_t>(prod & 0xffffu);
+  return static_cast<int32_t>(whole + (frac + static_cast<uint32_t>(phi) > 65536u ? 1u : 0u));
 }
 // Is slot s owned by an expert of this call that is already resident (a hit)?
 __device__ __forceinline__ bool is_hit_slot(const int32_t* __restrict__ owner, int s, int base,

@@ -21,6 +21,9 @@
 //     the caller;
 //   * the first call on each device looks the array's address up, once, with
 //     that device current; make that first call before any stream capture;
+//     the address is kept until the process exits, so the entry point must
+//     not be used on a device after a reset of its primary context
+//     (cudaDeviceReset) in the same process;
 //   * the kernels write every scratch element they read within a call, so
 //     nothing is cleared between calls.
 #include <mutex>

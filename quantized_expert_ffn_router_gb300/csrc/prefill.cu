@@ -606,11 +606,13 @@ ft_status experts_prefill(const ft_bank* cache, const ft_bank* pool, int32_t lay
             map_bank(&mds, base + L.off[5], I / 16, H, nb, st, 16, CU_TENSOR_MAP_SWIZZLE_NONE) &&
             map_acts(&mh, hp, I, n_rows);
   if (!ok) return fail(FT_ERR_INVALID, "experts prefill: tensor map encoding rejected the bank or batch");
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(pf_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, PfSmem<2>::total + 1024);
-    cudaFuncSetAttribute(pf_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, PfSmem<1>::total + 1024);
-    attr = true;
+  {
+    ft_status sa = ensure_dyn_smem(reinterpret_cast<const void*>(pf_kernel<2>), PfSmem<2>::total + 1024,
+                                   "experts prefill");
+    if (sa == FT_OK)
+      sa = ensure_dyn_smem(reinterpret_cast<const void*>(pf_kernel<1>), PfSmem<1>::total + 1024,
+                           "experts prefill");
+    if (sa != FT_OK) return sa;
   }
   PfArgs a;
   a.offsets = offsets;

@@ -18,6 +18,10 @@ constexpr int kGemvMaxT = 16;
 constexpr int kRouteMaxK = 32;
 constexpr int kRouteMaxE = 4096;
 
+// The arrival counter's own 256 bytes at the start of the workspace: the same
+// offset for every T, so a workspace sized for one T serves any smaller T.
+constexpr size_t kRouteCounterBytes = 256;
+
 size_t route_logits_bytes(int T, int E) {
   return (static_cast<size_t>(T) * E * sizeof(float) + 255) & ~static_cast<size_t>(255);
 }
@@ -363,19 +367,18 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
 
 
 // Host: launch route_rows_kernel (T <= kGemvMaxT), logits and top-k in one
-// kernel; the arrival counter follows the logits in ws.
+// kernel; the arrival counter is the first word of ws, the logits follow it.
 ft_status launch_rows(const uint16_t* x, int T, int H, const float* W, int E, int k, int renorm,
                       int32_t* ids, float* wts, void* ws, cudaStream_t s) {
-  float* logits = static_cast<float*>(ws);
-  unsigned* counter = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + route_logits_bytes(T, E));
+  unsigned* counter = static_cast<unsigned*>(ws);
+  float* logits = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kRouteCounterBytes);
   const size_t smem = static_cast<size_t>(T < 8 ? T : 8) * E * sizeof(float);
-  static bool attr = false;
-  if (!attr) {
+  {
     const int mx = 8 * kRouteMaxE * static_cast<int>(sizeof(float));
-    cudaFuncSetAttribute(route_rows_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-    cudaFuncSetAttribute(route_rows_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-    cudaFuncSetAttribute(route_rows_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-    attr = true;
+    ft_status st = ensure_dyn_smem(reinterpret_cast<const void*>(route_rows_kernel<1>), mx, "route");
+    if (st == FT_OK) st = ensure_dyn_smem(reinterpret_cast<const void*>(route_rows_kernel<4>), mx, "route");
+    if (st == FT_OK) st = ensure_dyn_smem(reinterpret_cast<const void*>(route_rows_kernel<16>), mx, "route");
+    if (st != FT_OK) return st;
   }
   cudaLaunchConfig_t rc = {};
   rc.gridDim = dim3(E);
@@ -405,7 +408,7 @@ extern "C" {
 
 size_t ft_moe_route_workspace(int32_t T, int32_t E) {
   if (T <= 0 || E <= 0) return 0;
-  return ft::route_logits_bytes(T, E) + 256;  // logits, then the arrival counter
+  return ft::kRouteCounterBytes + ft::route_logits_bytes(T, E);  // the arrival counter, then the logits
 }
 
 ft_status ft_moe_route(const uint16_t* x, int32_t T, int32_t H, const float* w_router, int32_t E,
@@ -422,7 +425,7 @@ ft_status ft_moe_route(const uint16_t* x, int32_t T, int32_t H, const float* w_r
   FT_REQUIRE(reinterpret_cast<uintptr_t>(x) % 16 == 0 && reinterpret_cast<uintptr_t>(w_router) % 16 == 0,
              "route: x and w_router must be 16-byte aligned");
   cudaStream_t s = ft::as_stream(stream);
-  float* logits = static_cast<float*>(ws);
+  float* logits = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + ft::kRouteCounterBytes);
   if (T <= ft::kGemvMaxT)  // logits and top-k in one kernel
     return ft::launch_rows(x, T, H, w_router, E, k, renorm, topk_ids, topk_w, ws, s);
   {

@@ -48,8 +48,8 @@ def test_route_parity(cuda_lib, name, T):
     x, redraws = gapped_tokens(cfg.seed, f"route-{name}", T, cfg.H, W, cfg.k, cfg.gap,
                                bias_feature=cfg.zipf is not None)
     ids_o, w_o = oracle.route(x, W, cfg.k)
-    # one workspace for every call: T <= 16 keeps an arrival counter after the
-    # logits, which each call must leave at zero
+    # one workspace for every call: T <= 16 keeps an arrival counter in the
+    # workspace's first 256 bytes, which each call must leave at zero
     ws = torch.zeros(ft.route_workspace(T, cfg.E), dtype=torch.uint8, device=DEV)
     for renorm in (False, True, False):
         ids = torch.empty((T, cfg.k), dtype=torch.int32, device=DEV)
@@ -59,7 +59,27 @@ def test_route_parity(cuda_lib, name, T):
         assert np.array_equal(ids.cpu().numpy(), ids_o)
         ref = w_o / w_o.sum(axis=1, keepdims=True) if renorm else w_o
         np.testing.assert_allclose(w.cpu().numpy(), ref, rtol=2e-5, atol=1e-7)
-        assert not ws[-256:].any()
+        assert not ws[:256].any()
+
+
+def test_route_workspace_shared_across_token_counts(cuda_lib):
+    """One zero-filled workspace sized for the largest call serves calls of
+    every smaller T in any order (the arrival counter has a fixed place), and
+    the tiled path (T > 16) may use it in between."""
+    ft = cuda_lib
+    cfg = synth.get_config("d35b")
+    W = synth.router_weights(cfg.seed, 5, cfg.E, cfg.H, cfg.router_std, zipf_bias=cfg.zipf)
+    ws = torch.zeros(ft.route_workspace(40, cfg.E), dtype=torch.uint8, device=DEV)
+    for T in (8, 1, 16, 40, 1, 3, 8):
+        x, _ = gapped_tokens(cfg.seed, f"route-ws-{T}", T, cfg.H, W, cfg.k, cfg.gap, bias_feature=True)
+        ids_o, w_o = oracle.route(x, W, cfg.k)
+        ids = torch.empty((T, cfg.k), dtype=torch.int32, device=DEV)
+        w = torch.empty((T, cfg.k), dtype=torch.float32, device=DEV)
+        ft.route(_t(x), _t(W), cfg.k, ids, w, ws)
+        torch.cuda.synchronize()
+        assert np.array_equal(ids.cpu().numpy(), ids_o), T
+        np.testing.assert_allclose(w.cpu().numpy(), w_o, rtol=2e-5, atol=1e-7)
+        assert not ws[:256].any(), T
 
 
 def test_route_prefill_full_size_sampled(cuda_lib):

@@ -72,6 +72,21 @@ def test_split_continuous_limit_and_edges():
         assert oracle.split_q16(m, 0) == m  # no cap at phi = 0
 
 
+def test_split_remainder_closed_form():
+    # cost(f) = max(f*(65536-phi), (m-f)*phi) falls until the crossing
+    # f* = m*phi/65536 and rises after it, so the minimum is at lo = floor(f*)
+    # or lo + 1.  Writing m*phi = 65536*lo + r, lo + 1 is strictly cheaper
+    # exactly when (lo+1)*(65536-phi) < (m-lo)*phi, i.e. when r + phi > 65536.
+    # The oracle tries every f; this closed form must agree over the whole
+    # domain of the Q16 rule for m <= 512.
+    grid = oracle.split_q16_grid(512, 1, 65536)  # [phi - 1, m]
+    phi = np.arange(1, 65537, dtype=np.int64)[:, None]
+    m = np.arange(513, dtype=np.int64)[None, :]
+    prod = m * phi
+    closed = (prod >> 16) + ((prod & 0xFFFF) + phi > 65536)
+    assert np.array_equal(grid, closed)
+
+
 # --------------------------------------------------------------- resolve ----
 def test_resolve_hand_worked_trace():
     g = json.load(open(os.path.join(GOLDEN, "resolve_trace_hand.json")))
