@@ -39,6 +39,8 @@ METRIC = "MoE-layer tokens/s; decode expert-weight HBM GB/s; prefill grouped-GEM
 # between the kernels (`bench.py --case decode --tokens T` under
 # `ncu --cache-control none`, summarised under profiles/)
 TRAFFIC_PER_CALL = {1: 13_372_928, 8: 104_289_536}
+# DRAM bytes per ft_moe_decode_layer launch (ncu); empty until captured for the current kernel
+LAYER_TRAFFIC_PER_CALL = {}
 # the same for one flash-shaped NVFP4 decode experts call at T = 1
 # (`bench.py --case decode-flash --tokens 1`)
 FLASH_TRAFFIC_PER_CALL = 27_660_544
@@ -229,7 +231,9 @@ class DecodeWorkload:
         self.rws = torch.zeros(ft.route_workspace(T, E), dtype=torch.uint8, device=device)
         self.ews = torch.zeros(ft.experts_workspace(ft.FT_DECODE, T, k, H, I, E), dtype=torch.uint8,
                                device=device)
+        self.lws = torch.zeros(ft.decode_layer_workspace(T, k, H, I, E), dtype=torch.uint8, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.fused = False
 
     def _init_resident(self, cfg, T, n_steps, device, log):
         """A cache holding every (layer, expert) block (flash: 24,576 x
@@ -282,30 +286,48 @@ class DecodeWorkload:
         self.rws = torch.zeros(ft.route_workspace(T, E), dtype=torch.uint8, device=device)
         self.ews = torch.zeros(ft.experts_workspace(ft.FT_DECODE, T, k, H, I, E), dtype=torch.uint8,
                                device=device)
+        self.lws = torch.zeros(ft.decode_layer_workspace(T, k, H, I, E), dtype=torch.uint8, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.fused = False
 
-    # one pass of the hot path over all layers (enqueue only): route, resolve,
-    # fetch, experts (two kernels) per layer.  `ev` holds per-layer events: 2
-    # around the experts call of every EXP_EVERY-th layer (an event node
-    # between kernels costs microseconds and breaks the programmatic launch
-    # chain, so the timed graph samples), or 5 around every op of every layer
-    # (per_op, the breakdown graph)
+    # one pass of the hot path over all layers (enqueue only).  Fused: one
+    # ft_moe_decode_layer kernel per layer.  Separate: route, resolve, fetch,
+    # experts (two kernels) per layer.  `ev` holds per-layer events: 2 around
+    # the layer kernel (fused) or the experts call (separate) of every
+    # EXP_EVERY-th layer (an event node between kernels costs microseconds and
+    # breaks the programmatic launch chain, so the timed graph samples), or
+    # one around every op of every layer (per_op, the breakdown graph)
     EXP_EVERY = 8
-    OPS = ["route", "resolve", "fetch", "experts"]
-    KERNELS_PER_LAYER = 5
+
+    @property
+    def OPS(self):
+        return ["layer"] if self.fused else ["route", "resolve", "fetch", "experts"]
+
+    @property
+    def KERNELS_PER_LAYER(self):
+        return 1 if self.fused else 5
 
     def step(self, ev=None, per_op=False):
         ft, cfg, T = self.ft, self.cfg, self.T
 
-        def mark(l, i):
+        def mark(l, i, edge=None):
+            # i: op boundary (per-op graph); edge: 0 / 1 = start / end of the
+            # sampled kernel (timed graph)
             if ev is None:
                 return
             if per_op:
                 ev[l][i].record()
-            elif i in (3, 4) and l % self.EXP_EVERY == 0:
-                ev[l // self.EXP_EVERY][i - 3].record()
+            elif edge is not None and l % self.EXP_EVERY == 0:
+                ev[l // self.EXP_EVERY][edge].record()
 
         for l in range(cfg.L):
+            if self.fused:
+                mark(l, 0, edge=0)
+                ft.decode_layer(self.x_stage[l], self.W[l], cfg.k, self.state, l, self.phi, self.cache_b,
+                                self.pool_b, self.ids[l], self.w[l], self.slot[l], self.nf[l], self.ff[l],
+                                self.fs[l], self.out[l], self.lws, dev_status=self.status)
+                mark(l, 1, edge=1)
+                continue
             mark(l, 0)
             ft.route(self.x_stage[l], self.W[l], cfg.k, self.ids[l], self.w[l], self.rws)
             mark(l, 1)
@@ -313,10 +335,30 @@ class DecodeWorkload:
                              self.fs[l], self.status)
             mark(l, 2)
             ft.fetch(self.pool_b, self.cache_b, self.nf[l], self.ff[l], self.fs[l], self.status)
-            mark(l, 3)
+            mark(l, 3, edge=0)
             ft.experts_fwd(self.cache_b, self.pool_b, l, cfg.E, self.x_stage[l], T, cfg.k, self.slot[l],
                            self.ids[l], self.w[l], self.out[l], self.ews, dev_status=self.status)
-            mark(l, 4)
+            mark(l, 4, edge=1)
+
+    def use_fused(self, want: bool) -> bool:
+        """Run the step as one fused kernel per layer when asked and the
+        library accepts the shape (one eager layer call decides); else the
+        separate calls."""
+        self.fused = False
+        if not want:
+            return False
+        import torch
+
+        x0 = self.x_stage[0].clone()
+        try:
+            self.fused = True
+            self.x_stage.copy_(self.x_all[0])
+            self.step()
+            torch.cuda.synchronize()
+        except self.ft.FtError:
+            self.fused = False
+        self.x_stage[0].copy_(x0)
+        return self.fused
 
     def capture(self):
         """Two graphs of one step: `graph` (timed) with events only around the
@@ -374,8 +416,9 @@ class DecodeWorkload:
         return nf / reps, hp / reps
 
     def experts_us(self):
-        """Mean device time (us) of one experts call (gate/up + down) over the
-        sampled layers of the last timed replay."""
+        """Mean device time (us) of one layer kernel (fused) or one experts call
+        (separate: gate/up + down) over the sampled layers of the last timed
+        replay."""
         return sum(e[0].elapsed_time(e[1]) for e in self.ev_exp) * 1e3 / len(self.ev_exp)
 
     def op_times(self, first: int, reps: int = 5):
@@ -568,37 +611,143 @@ def run_reference(args, cfg, T):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------- host link and q* cap -----
+def host_link_bench(wl, log=print, reps: int = 3):
+    """The host link's copy rate (one 1 GiB cudaMemcpyAsync from the pinned
+    pool to the device, best of `reps`) and the fetch kernel's rate moving 64
+    cached experts from the pool into the slots that already hold them (the
+    same bytes, so the cache stays consistent)."""
+    import torch
+
+    if wl.pool is None:
+        return None
+    ft = wl.ft
+    nb = min(wl.pool.shape[0], (1 << 30) // wl.pool.shape[1])
+    src = wl.pool[:nb]
+    dst = torch.empty(src.shape, dtype=torch.uint8, device=wl.dev)
+    best = None
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        dst.copy_(src, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) / 1e3
+        best = t if best is None else min(best, t)
+    copy_gbs = src.numel() / best / 1e9
+    del dst
+    owner = wl.state.slot_owner[: wl.S]
+    slots = torch.nonzero(owner >= 0).flatten()[:64].to(torch.int32)
+    n = int(slots.numel())
+    fetch_gbs = None
+    if n:
+        fids = owner[slots.long()].contiguous()
+        nf = torch.tensor([n], dtype=torch.int32, device=wl.dev)
+        ft.fetch(wl.pool_b, wl.cache_b, nf, fids, slots.contiguous())  # warm-up
+        torch.cuda.synchronize()
+        bestf = None
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            ft.fetch(wl.pool_b, wl.cache_b, nf, fids, slots.contiguous())
+            e1.record()
+            torch.cuda.synchronize()
+            t = e0.elapsed_time(e1) / 1e3
+            bestf = t if bestf is None else min(bestf, t)
+        fetch_gbs = n * wl.block / bestf / 1e9
+    res = {"h2d_copy_GBs": copy_gbs, "h2d_copy_bytes": int(src.numel()),
+           "fetch_kernel_GBs": fetch_gbs, "fetch_experts": n,
+           "fetch_frac_of_copy": (fetch_gbs / copy_gbs) if fetch_gbs else None,
+           "how": "one pinned-host -> device cudaMemcpyAsync of 1 GiB of the pool (best of 3); ft_moe_fetch of "
+                  "64 cached experts onto their own slots (best of 3), CUDA events"}
+    log(f"host link: copy {copy_gbs:.1f} GB/s, fetch kernel {fetch_gbs} GB/s")
+    return res
+
+
+def phi_bench(wl, phi: int, args, units, reduce_fn, world, log=print):
+    """The same decode step with the q* split capping the fetches at
+    frac_q16 = phi: the capped misses stay on the host path (the experts read
+    them in place from the pinned pool).  Timed like the headline line after
+    the cache settles under the new split."""
+    import torch
+
+    old = wl.phi
+    wl.phi = phi
+    wl.use_fused(wl.fused or args.layer_kernel == "fused")
+    wl.capture()
+    wl.settle(max(64, args.settle // 4), seed=2)
+    secs = time_device(wl, args.steps, args.warmup, reduce_fn, world, None)
+    value, secs_max, _ = aggregate(units, secs, world, reduce_fn)
+    nfetch, host_pairs = wl.fetch_rate(first=args.warmup + 2 * args.steps + 5)
+    st = wl.ft.get_status(wl.status)
+    wl.phi = old
+    if st != 0:
+        raise RuntimeError(f"device status {st} during the phi={phi} benchmark")
+    log(f"phi={phi}: {value:.1f} {UNIT}, {secs_max / args.steps * 1e3:.3f} ms/step, {nfetch:.2f} fetched and "
+        f"{host_pairs:.2f} host-path pairs per step")
+    torch.cuda.synchronize()
+    return {"frac_q16": phi, "value": value, "unit": UNIT, "ms_per_step": secs_max / args.steps * 1e3,
+            "fused": wl.fused, "fetched_experts_per_step": nfetch, "host_path_pairs_per_step": host_pairs,
+            "launch_us": wl.experts_us()}
+
+
 # ------------------------------------------------------- flash decode -----
-def flash_bench(steps: int, warmup: int, device, log=print):
+def host_mem_available() -> int:
+    """MemAvailable of this host in bytes (0 when unknown)."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def flash_bench(steps: int, warmup: int, device, log=print, cache_frac: float = 1.0):
     """The NVFP4 decode step of the flash config (48 layers x 512 experts,
-    top-10, H 2560, I 640, 2,764,800 B per expert block), every expert
-    resident in HBM (67.9 GB), one token per step: route, resolve (all hits),
-    fetch (nothing), experts per layer, captured in one CUDA graph; the same
-    timing as the headline decode line."""
+    top-10, H 2560, I 640, 2,764,800 B per expert block), one token per step,
+    captured in one CUDA graph; the same timing as the headline decode line.
+    cache_frac 1: every expert resident in HBM (67.9 GB), nothing is ever
+    fetched; below 1: a slot cache of that fraction of the 24,576 (layer,
+    expert) pairs in HBM and the whole pool in pinned host memory, the cache
+    settled under the step's own routing before timing."""
+    import dataclasses
+
     import torch
 
     import synth
 
     cfg = synth.get_config("flash")
-    n_steps = warmup + steps + 5
+    if cache_frac < 1.0:
+        cfg = dataclasses.replace(cfg, slots=int(round(cache_frac * cfg.L * cfg.E)))
+    n_steps = warmup + steps + 5 + 20
     wl = DecodeWorkload(cfg, 1, 65536, n_steps, device, log)
+    fused = wl.use_fused(True)
     wl.capture()
-    wl.settle(8)
+    wl.settle(8 if cache_frac >= 1.0 else 128)
     secs = time_device(wl, steps, warmup, None, 1)
+    nfetch, host_pairs = wl.fetch_rate(first=warmup + steps + 5)
     exp_us = wl.experts_us()
     ebytes = wl.distinct_expert_bytes()
     st = wl.ft.get_status(wl.status)
     if st != 0:
         raise RuntimeError(f"device status {st} during the flash decode benchmark")
-    per_call = ebytes / cfg.L
+    per_call = ebytes / cfg.L + (cfg.E * cfg.H * 4 if fused else 0)
+    where = ("every expert resident (67.9 GB)" if cache_frac >= 1.0 else
+             f"cache {cfg.slots} slots ({cache_frac:.0%} of 24,576) in HBM, pool in pinned host memory")
     res = {"workload": "flash-shaped NVFP4 decode: 48 layers x 512 experts, top-10, H2560, I640 "
-                       "(2,764,800 B/expert), every expert resident (67.9 GB), T=1",
+                       f"(2,764,800 B/expert), {where}, T=1",
            "value": cfg.L * steps / secs, "unit": UNIT, "ms_per_step": secs / steps * 1e3,
-           "model_tokens_per_s": steps / secs,
-           "experts_us_per_call": exp_us, "expert_bytes_per_call": per_call,
-           "experts_traffic_per_call": FLASH_TRAFFIC_PER_CALL,
+           "fetched_experts_per_step": nfetch, "host_path_pairs_per_step": host_pairs,
+           "model_tokens_per_s": steps / secs, "fused": fused,
+           "launch_us": exp_us, "bytes_per_launch": per_call,
+           "kernel": "ft_moe_decode_layer (expert + router bytes)" if fused else
+                     "ft_moe_experts_fwd decode (expert bytes)",
+           "experts_traffic_per_call": None if fused else FLASH_TRAFFIC_PER_CALL,
            "experts_GBs": per_call / (exp_us * 1e-6) / 1e9 if exp_us else None}
-    log(f"flash T=1: {res['value']:.1f} {UNIT}, {res['ms_per_step']:.3f} ms/step, experts {exp_us:.1f} us/call")
+    log(f"flash T=1 cache {cache_frac:.0%}: {res['value']:.1f} {UNIT}, {res['ms_per_step']:.3f} ms/step, "
+        f"{'layer kernel' if fused else 'experts'} {exp_us:.1f} us/call, {nfetch:.1f} fetched/step")
     del wl
     torch.cuda.empty_cache()
     return res
@@ -844,6 +993,9 @@ def main():
     ap.add_argument("--no-flash", action="store_true", help="skip the NVFP4 (flash) decode measurement")
     ap.add_argument("--prefill-layers", type=int, default=3,
                     help="layers streamed from host memory through the prefill double buffer (0: skip)")
+    ap.add_argument("--layer-kernel", choices=["fused", "separate"], default="fused",
+                    help="decode step as one ft_moe_decode_layer kernel per layer (when the shape fits) or as the "
+                         "separate route / resolve / fetch / experts calls")
     ap.add_argument("--case", choices=["decode", "decode-flash", "prefill"],
                     help="run a small kernel case for a profiler instead of the benchmark")
     args = ap.parse_args()
@@ -891,6 +1043,7 @@ def main():
             wl = DecodeWorkload(cfg, T, args.phi, n_steps, device, log)
         else:
             wl = reshape_workload(wl, T, n_steps)
+        fused = wl.use_fused(args.layer_kernel == "fused")
         wl.capture()
         wl.settle(args.settle)
         clocks = ClockSampler(local) if bi == 0 else None
@@ -906,11 +1059,30 @@ def main():
         e2e_val, _, _ = aggregate(units, e2e_secs, world, reduce_fn)
         results[T] = dict(value=value, secs=secs_max, kt=kt, exp_us=exp_us, ebytes=ebytes, nfetch=nfetch,
                           host_pairs=host_pairs, e2e=e2e_val, h2d=h2d, d2h=d2h,
-                          clocks=clocks.summary() if clocks else None)
+                          clocks=clocks.summary() if clocks else None, fused=fused,
+                          kernels_per_layer=wl.KERNELS_PER_LAYER)
         st = ft.get_status(wl.status)
         if st != 0:
             raise RuntimeError(f"device status {st} during the benchmark")
-        log(f"T={T}: {value:.1f} {UNIT}, {secs_max / args.steps * 1e3:.3f} ms/step, kernels {kt}")
+        log(f"T={T}: {value:.1f} {UNIT}, {secs_max / args.steps * 1e3:.3f} ms/step, "
+            f"{'fused' if fused else 'separate'}, kernels {kt}")
+        if fused:
+            # the same step through the separate calls, for comparison (after the timed runs)
+            wl.use_fused(False)
+            wl.capture()
+            secs_sep = time_device(wl, args.steps, args.warmup, reduce_fn, world, None)
+            v_sep, s_sep, _ = aggregate(units, secs_sep, world, reduce_fn)
+            results[T]["separate"] = {"value": v_sep, "ms_per_step": s_sep / args.steps * 1e3,
+                                      "experts_us_per_call": wl.experts_us(),
+                                      "per_op_us_per_step": wl.op_times(first=args.warmup + 2 * args.steps)}
+            log(f"T={T} separate calls: {v_sep:.1f} {UNIT}, {s_sep / args.steps * 1e3:.3f} ms/step")
+            st = ft.get_status(wl.status)
+            if st != 0:
+                raise RuntimeError(f"device status {st} during the benchmark")
+        if bi == 0:
+            results[T]["host_link"] = host_link_bench(wl, log)
+            if args.phi != 26214:
+                results[T]["phi_26214"] = phi_bench(wl, 26214, args, units, reduce_fn, world, log)
 
     prefill = None
     if not args.no_prefill:
@@ -932,6 +1104,14 @@ def main():
             del wl
         torch.cuda.empty_cache()
         flash = flash_bench(max(3, min(args.steps, 100)), args.warmup, device, log)
+        need = 24576 * 2764800 * 1.5
+        if host_mem_available() >= need:
+            torch.cuda.empty_cache()
+            flash["cache_25pct"] = flash_bench(max(3, min(args.steps, 50)), args.warmup, device, log,
+                                               cache_frac=0.25)
+        else:
+            flash["cache_25pct"] = {"skipped": f"host memory available {host_mem_available() / 1e9:.0f} GB "
+                                               f"< {need / 1e9:.0f} GB for the pinned 67.9 GB pool"}
     if rank != 0:
         return
     peaks, peak_kind = measured_peaks()
@@ -940,19 +1120,25 @@ def main():
     dom = max(kt, key=kt.get) if kt else "experts"
     exp_us = r["exp_us"]
     roof = None
+    router_bytes = cfg.E * cfg.H * 4
     if exp_us:
-        # algorithmic bytes of the experts calls of the last timed step (each
-        # distinct expert's block once) / their event-timed duration
-        per_call = r["ebytes"] / cfg.L
+        # algorithmic bytes of one launch (each distinct expert's block once,
+        # plus the router rows when the router runs in the same kernel) / its
+        # event-timed duration
+        per_call = r["ebytes"] / cfg.L + (router_bytes if r["fused"] else 0)
         achieved = per_call / (exp_us * 1e-6) / 1e9
-        roof = {"bound": "hbm", "kernel": "ft_moe_experts_fwd decode (gate/up + down kernels)",
+        kname = ("ft_moe_decode_layer (route, resolve, fetch, experts, combine: one kernel per layer)" if r["fused"]
+                 else "ft_moe_experts_fwd decode (gate/up + down kernels)")
+        roof = {"bound": "hbm", "kernel": kname,
                 "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": TRAFFIC_PER_CALL.get(args.tokens),
+                "frac": achieved / peaks["hbm_gbs"],
+                "traffic": (LAYER_TRAFFIC_PER_CALL if r["fused"] else TRAFFIC_PER_CALL).get(args.tokens),
                 "peak_kind": peak_kind, "frac_of_8tbs_nominal": achieved / 8000.0,
                 "algorithmic_bytes_per_launch": per_call,
                 "launch_us": exp_us,
-                "timing": f"events around the experts calls of every {DecodeWorkload.EXP_EVERY}th layer "
-                          "of the timed replays",
+                "timing": f"events around the {'layer kernel' if r['fused'] else 'experts calls'} of every "
+                          f"{DecodeWorkload.EXP_EVERY}th layer of the timed replays",
+                "step_us_per_layer": r["secs"] / args.steps / cfg.L * 1e6,
                 "dominant_op_by_time": dom}
     cpu = None
     if not args.no_cpu_baseline:
@@ -960,7 +1146,7 @@ def main():
         cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"{n} single-layer calls of {args.tokens} token(s) (route, resolve, fp64 experts) "
                          f"on 2 of 40 layers, {dt:.1f} s, single-threaded C++"}
-    launches_per_step = cfg.L * DecodeWorkload.KERNELS_PER_LAYER
+    launches_per_step = cfg.L * r["kernels_per_layer"]
     line = {
         "metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["secs"] / args.steps * 1e3, "higher_is_better": True,
@@ -982,7 +1168,12 @@ def main():
             "model_tokens_per_s": r["value"] / cfg.L,
             "per_op_us_per_step": kt,
             "expert_bytes_per_step": r["ebytes"],
-            "step": "per layer: ft_moe_route, ft_moe_resolve_slots, ft_moe_fetch, ft_moe_experts_fwd (two kernels)",
+            "step": ("per layer: ft_moe_decode_layer (one kernel: route, resolve with the q* split, fetch, "
+                     "experts, combine)" if r["fused"] else
+                     "per layer: ft_moe_route, ft_moe_resolve_slots, ft_moe_fetch, ft_moe_experts_fwd (two kernels)"),
+            "separate_calls": r.get("separate"),
+            "phi_26214": r.get("phi_26214"),
+            "host_link": r.get("host_link"),
             "settle_steps": args.settle,
             "fetched_experts_per_step": r["nfetch"],
             "host_path_pairs_per_step": r["host_pairs"],
@@ -1000,7 +1191,8 @@ def main():
                                             if flash["experts_GBs"] else None)),
             "other_batches": {str(T): {"value": v["value"], "ms_per_step": v["secs"] / args.steps * 1e3,
                                        "per_op_us_per_step": v["kt"], "expert_bytes_per_step": v["ebytes"],
-                                       "experts_us_per_call": v["exp_us"],
+                                       "fused": v["fused"], "launch_us": v["exp_us"],
+                                       "separate_calls": v.get("separate"),
                                        "e2e": v["e2e"]}
                               for T, v in results.items() if T != args.tokens},
         },
@@ -1029,6 +1221,7 @@ def reshape_workload(wl, T, n_steps):
     wl.fs = torch.empty((L, wl.ml), dtype=torch.int32, device=dev)
     wl.rws = torch.zeros(ft.route_workspace(T, E), dtype=torch.uint8, device=dev)
     wl.ews = torch.zeros(ft.experts_workspace(ft.FT_DECODE, T, k, H, cfg.I, E), dtype=torch.uint8, device=dev)
+    wl.lws = torch.zeros(ft.decode_layer_workspace(T, k, H, cfg.I, E), dtype=torch.uint8, device=dev)
     return wl
 
 

@@ -15,6 +15,8 @@
  *   ft_moe_combine        top-k weighted sum of permuted expert rows (prefill)
  *   ft_moe_split_q16      the q* rule alone, batched (the resolve kernel runs
  *                         the same device function)
+ *   ft_moe_decode_layer   route, resolve, fetch, experts and combine of one
+ *                         decode layer call in one kernel
  *
  * Sources, by page title and section:
  *   "FreeToken 딥다이브" (fiv.co.kr) -- design pattern 1 (whole-layer double
@@ -386,6 +388,53 @@ FT_API ft_status ft_moe_experts_decode_static(const ft_bank* cache_host, const f
  * multiplies its results by it).  ws: ft_moe_permute_workspace(T,k,E) bytes.
  * An id outside [0, E) records FT_ERR_BAD_ID.  Limits: E <= 4096.
  */
+/*
+ * ft_moe_decode_layer -- one decode layer call, the whole hot path in one
+ * kernel launch: ft_moe_route, ft_moe_resolve_slots (q* split inside),
+ * ft_moe_fetch and ft_moe_experts_fwd(FT_DECODE) with the pool as host path,
+ * in that order and with the same results (FreeToken paper post, secs. 2 and
+ * 6: router on the GPU, one kernel for dedup, residency, q, victims and the
+ * id rewrite, no host crossing in the layer; FreeToken deep-dive, design
+ * patterns 2, 3 and 5; SSD-tier 35B post, "How it works"; NVMe-streaming
+ * post, step 4).
+ * x [T,H] bf16; w_router [E,H] fp32 (E = state->E, H = the bank's); outputs
+ * as the separate calls write them: topk_ids/topk_w [T,k], slot_ids [T,k],
+ * *num_fetch, fetch_fid/fetch_slot [max_list], out [T,H] (out_dtype).  The
+ * pool (the source of truth) is required: fetched experts are copied from
+ * it and pairs left on slot -1 read it in place.  ws: device scratch of
+ * ft_moe_decode_layer_workspace(T,k,H,I,E) bytes, 256-byte aligned: a
+ * counter and a generation word in its first 256 bytes, then the logits and
+ * h.  ws must be zero-filled before the first call that uses it; every call
+ * leaves the counter at zero, so one workspace serves every later call of
+ * any shape it is large enough for; calls that may overlap on the GPU need
+ * separate workspaces.
+ * The grid is one CTA per SM, launched cooperatively (its CTAs wait for one
+ * another through the workspace, each wait bounded by ft_set_wait_limit_ns);
+ * a wait that gives up records FT_ERR_TIMEOUT in dev_status, the kernel
+ * returns, and later calls that see that status do nothing: the caller then
+ * zero-fills ws and the status word before calling again.
+ * Limits: 1 <= T <= 8, T*k <= 128, k <= min(E, 32), E <= 512 and
+ * E <= 4 x the SM count, H and I <= 4096, bank blocks 16-byte aligned, and
+ * the call's shared-memory plan must fit one SM (FT_ERR_INVALID otherwise,
+ * nothing launched; the separate calls serve those shapes).
+ */
+FT_API size_t ft_moe_decode_layer_workspace(int32_t T, int32_t k, int32_t H, int32_t I, int32_t E);
+FT_API ft_status ft_moe_decode_layer(const uint16_t* x, int32_t T, const float* w_router, int32_t k,
+                              int32_t renorm, const ft_cache_state* state_host, int32_t layer,
+                              int32_t frac_q16, const ft_bank* cache_host, const ft_bank* pool_host,
+                              int32_t* topk_ids, float* topk_w, int32_t* slot_ids, int32_t* num_fetch,
+                              int32_t* fetch_fid, int32_t* fetch_slot, int32_t max_list, void* out,
+                              int32_t out_dtype, void* ws, size_t ws_bytes, int32_t* dev_status,
+                              void* stream);
+
+/*
+ * ft_set_wait_limit_ns -- the limit of every bounded wait inside the kernels
+ * launched after this call (the decode layer's hand-offs and copy waits),
+ * in nanoseconds of the GPU's global timer; 0 restores the default of 2 s.
+ * Process-wide; not tied to a device or stream.  Always FT_OK.
+ */
+FT_API ft_status ft_set_wait_limit_ns(uint64_t ns);
+
 FT_API size_t ft_moe_permute_workspace(int32_t T, int32_t k, int32_t E);
 FT_API ft_status ft_moe_permute(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E,
                          const uint16_t* x, int32_t H, int32_t* perm, int32_t* inv,

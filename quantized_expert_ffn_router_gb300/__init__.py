@@ -69,6 +69,10 @@ _SIGS = {
                               _V]),
     "ft_moe_combine": (_I32, [_V, _V, _V, _I32, _I32, _I32, _V, _V, _V]),
     "ft_moe_merge_partials": (_I32, [_V, _V, _I64, _V, _I32, _V]),
+    "ft_moe_decode_layer_workspace": (_SZ, [_I32, _I32, _I32, _I32, _I32]),
+    "ft_moe_decode_layer": (_I32, [_V, _I32, _V, _I32, _I32, _V, _I32, _I32, _V, _V, _V, _V, _V, _V, _V, _V,
+                                   _I32, _V, _I32, _V, _SZ, _V, _V]),
+    "ft_set_wait_limit_ns": (_I32, [_U64]),
 }
 
 
@@ -130,15 +134,19 @@ def make_bank(fmt: int, H: int, I: int, group: int, blocks, tensor_scale=None) -
 class DeviceCacheState:
     """The slot-cache state as device tensors plus its ft_cache_state view."""
 
-    def __init__(self, L: int, E: int, S: int, device="cuda", recency_init: int = -1):
+    def __init__(self, L: int, E: int, S: int, device="cuda", recency_init: int = -1, alloc=None):
+        """alloc(shape, dtype, fill) -> tensor, default torch.full on `device`."""
         import torch
 
+        if alloc is None:
+            def alloc(shape, dtype, fill):
+                return torch.full(shape, fill, dtype=dtype, device=device)
         self.L, self.E, self.S = L, E, S
-        self.slot_owner = torch.full((max(S, 1),), -1, dtype=torch.int32, device=device)
-        self.map = torch.full((L * E,), -1, dtype=torch.int32, device=device)
-        self.usage = torch.full((max(S, 1),), -1, dtype=torch.int64, device=device)
-        self.recency = torch.full((L * E,), recency_init, dtype=torch.int64, device=device)
-        self.step = torch.zeros(1, dtype=torch.int64, device=device)
+        self.slot_owner = alloc((max(S, 1),), torch.int32, -1)
+        self.map = alloc((L * E,), torch.int32, -1)
+        self.usage = alloc((max(S, 1),), torch.int64, -1)
+        self.recency = alloc((L * E,), torch.int64, recency_init)
+        self.step = alloc((1,), torch.int64, 0)
 
     def struct(self) -> FtCacheState:
         return FtCacheState(self.L, self.E, self.S, _ptr(self.slot_owner), _ptr(self.map),
@@ -286,3 +294,29 @@ def merge_partials(a, b, out, stream=None):
     """out = a + b (fp32 partial sums; out fp32 or bf16)."""
     out_dtype = FT_OUT_BF16 if out.dtype.itemsize == 2 else FT_OUT_F32
     _check(load().ft_moe_merge_partials(_ptr(a), _ptr(b), a.numel(), _ptr(out), out_dtype, _stream(stream)))
+
+
+def decode_layer_workspace(T: int, k: int, H: int, I: int, E: int) -> int:
+    return int(load().ft_moe_decode_layer_workspace(T, k, H, I, E))
+
+
+def decode_layer(x, w_router, k: int, state: DeviceCacheState, layer: int, frac_q16: int, cache: FtBank,
+                 pool: FtBank, topk_ids, topk_w, slot_ids, num_fetch, fetch_fid, fetch_slot, out, ws,
+                 renorm: bool = False, dev_status=None, stream=None):
+    """One decode layer call in one kernel (ft_moe_decode_layer): route, resolve,
+    fetch, experts and combine, with the separate calls' results."""
+    import torch
+
+    T = x.shape[0]
+    out_dtype = FT_OUT_BF16 if out.dtype in (torch.bfloat16, torch.int16, torch.uint16) else FT_OUT_F32
+    st = state.struct()
+    _check(load().ft_moe_decode_layer(_ptr(x), T, _ptr(w_router), k, int(bool(renorm)), ctypes.byref(st), layer,
+                                      int(frac_q16), ctypes.byref(cache), ctypes.byref(pool), _ptr(topk_ids),
+                                      _ptr(topk_w), _ptr(slot_ids), _ptr(num_fetch), _ptr(fetch_fid),
+                                      _ptr(fetch_slot), fetch_fid.numel(), _ptr(out), out_dtype, _ptr(ws),
+                                      ws.numel() * ws.element_size(), _ptr(dev_status), _stream(stream)))
+
+
+def set_wait_limit_ns(ns: int):
+    """Limit of the kernels' bounded waits launched from now on (0: the 2 s default)."""
+    _check(load().ft_set_wait_limit_ns(int(ns)))

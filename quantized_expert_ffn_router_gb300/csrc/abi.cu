@@ -58,6 +58,19 @@ int device_sm_count() {
   return n;
 }
 
+int device_smem_optin() {
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) dev = 0;
+  int n = dev < kMaxDevices ? cache[dev].load(std::memory_order_relaxed) : 0;
+  if (n <= 0) {
+    cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (n <= 0) n = 48 * 1024;
+    if (dev < kMaxDevices) cache[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
 ft_status ensure_dyn_smem(const void* kernel, int bytes, const char* what) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

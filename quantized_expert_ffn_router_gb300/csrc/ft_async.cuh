@@ -91,6 +91,27 @@ __device__ __forceinline__ void l2_prefetch(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// GPU-scope acquire load / release store / acquire-release wrapping increment
+// of a 32-bit word in global memory, and the proxy fence that orders plain
+// stores before later bulk-copy (async proxy) reads of the same bytes.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// old = *p; *p = (old >= limit) ? 0 : old + 1; returns old.
+__device__ __forceinline__ uint32_t atom_inc_acq_rel_gpu(uint32_t* p, uint32_t limit) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(limit) : "memory");
+  return old;
+}
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Programmatic dependent launch: let the next grid in the stream start, and
 // wait for the previous grid's completion and memory.
 __device__ __forceinline__ void pdl_launch_dependents() {

@@ -28,8 +28,10 @@ ft_status check_bank(const ft_bank* b, const char* name, Layout* L);
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
-// The current device's SM count, looked up once per device.
+// The current device's SM count, and its per-block shared-memory limit
+// (opt-in), each looked up once per device.
 int device_sm_count();
+int device_smem_optin();
 // Raise a kernel's dynamic shared memory limit to `bytes` on the current
 // device, once per (kernel, device); FT_ERR_CUDA if the device refuses.
 ft_status ensure_dyn_smem(const void* kernel, int bytes, const char* what);

@@ -38,6 +38,12 @@ Stream orchestration only: every step is a call into libft_moe.so.
   in the cache and seed decode ("FreeToken 딥다이브", design pattern 1;
   "FreeToken: 让消费级电脑跑起 284B MoE", sec. 5).  With fewer than 2E slots the
   buffer is single: each layer is copied after the previous one's experts.
+
+* resize_cache rebuilds the slot cache at a new size: every new buffer is
+  allocated first, then ft_moe_cache_rebuild validates and copies; a failed
+  allocation or a refused rebuild leaves the running cache untouched
+  ("FreeToken 딥다이브", design pattern 7: validate before destroy;
+  "FreeToken: 让消费级电脑跑起 284B MoE", sec. 7).
 """
 
 from __future__ import annotations
@@ -45,8 +51,9 @@ from __future__ import annotations
 import ctypes
 
 from . import (FT_DECODE, FT_DECODE_HOST, FT_PREFILL, DeviceCacheState, FtBank, cache_install, combine, experts_fwd,
-               experts_workspace, fetch, fetch_layer, merge_partials, permute, permute_workspace, prefetch,
+               experts_workspace, fetch, fetch_layer, make_bank, merge_partials, permute, permute_workspace, prefetch,
                resolve_slots, route, route_workspace)
+from . import cache_rebuild as _cache_rebuild
 
 
 def frac_q16_from_bandwidths(b_p: float, b_h: float) -> int:
@@ -352,3 +359,33 @@ class PrefillLayers:
         main.wait_stream(self.copy_stream)
         return outs
 
+
+def resize_cache(state: DeviceCacheState, cache, fmt: int, H: int, I: int, group: int, new_S: int,
+                 budget_bytes: int, tensor_scale=None, alloc=None, rebuild=None, dev_status=None, stream=None):
+    """Rebuild the slot cache (state + its bank tensor `cache` [S, stride]) at
+    new_S slots.  Returns (new_state, new_cache, new_bank); the caller switches
+    to them and frees the old ones once the stream has passed the rebuild.
+
+    Everything the new cache needs is allocated before the library is
+    called, through alloc(shape, dtype, fill) (default: torch.full on the old
+    cache's device), and the rebuild itself validates before it writes.  So
+    an allocation that fails (out of memory) raises before any device work,
+    and a rebuild the library refuses (FtError FT_ERR_REJECTED: over budget,
+    wrong shape) raises after nothing was changed: either way the old state
+    and bank keep serving."""
+    import torch
+
+    if new_S < 0:
+        raise ValueError("new_S < 0")
+    device = cache.device
+    if alloc is None:
+        def alloc(shape, dtype, fill):
+            return torch.full(shape, fill, dtype=dtype, device=device)
+    stride = int(cache.stride(0)) * cache.element_size()
+    new_state = DeviceCacheState(state.L, state.E, new_S, device=device, alloc=alloc)
+    new_cache = alloc((max(new_S, 1), stride), torch.uint8, 0)
+    old_bank = make_bank(fmt, H, I, group, cache, tensor_scale)
+    new_bank = make_bank(fmt, H, I, group, new_cache, tensor_scale)
+    (rebuild or _cache_rebuild)(state, old_bank, new_state, new_bank, budget_bytes, dev_status=dev_status,
+                                stream=stream)
+    return new_state, new_cache, new_bank

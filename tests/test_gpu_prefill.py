@@ -118,14 +118,16 @@ def test_prefill_experts_small(cuda_lib, H, I, E, k, T):
     assert_close(got, ref, f"prefill rows {H}x{I}")
 
 
-def test_prefill_full_layer_sampled(cuda_lib):
-    """The whole-layer prefill shape (H 4096, I 2048, 256 experts, top-6,
-    T = 2048): route on the GPU, permute, grouped experts and combine; every row
-    of four sampled experts checked against the oracle, and the combine on
-    sampled tokens."""
+@pytest.mark.parametrize("T", [2048, 8192])
+def test_prefill_full_layer_sampled(cuda_lib, T):
+    """The whole-layer prefill shape (H 4096, I 2048, 256 experts, top-6) at
+    both prompt lengths the benchmark times: route on the GPU, permute, grouped
+    experts and combine; every row of four sampled experts (the largest, the
+    smallest active one and two fixed ones) checked against the oracle, and
+    the combine on sampled tokens."""
     ft = cuda_lib
     cfg = synth.get_config("prefill")
-    H, I, E, k, T = cfg.H, cfg.I, cfg.E, cfg.k, 2048
+    H, I, E, k = cfg.H, cfg.I, cfg.E, cfg.k
     W = synth.router_weights(cfg.seed, 0, E, H, cfg.router_std)
     x = synth.normal_bf16(synth.stream_key(cfg.seed, "prefill-x", T), (T, H))
     ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
@@ -154,7 +156,7 @@ def test_prefill_full_layer_sampled(cuda_lib):
     out = torch.empty((T, H), dtype=torch.int16, device=DEV)
     ft.combine(yp, inv, w, out)
     torch.cuda.synchronize()
-    toks = np.array([0, 5, 1000, T - 1])
+    toks = np.array([0, 5, 1000, T // 2 + 3, T - 1])
     inv_np = inv.cpu().numpy()
     ref_c = oracle.combine(yp.cpu().numpy().view(np.uint16), inv_np[toks], w.cpu().numpy()[toks])
     got_c = bf16_to_f64(out.cpu().numpy().view(np.uint16)[toks])

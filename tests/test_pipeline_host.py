@@ -47,3 +47,100 @@ def test_speculative_decode_needs_a_pool():
 
     with pytest.raises(ValueError):
         SpeculativeDecode(None, None, None, 8, 2, 1)
+
+
+# ------------------------------------------------- validate before destroy
+class _Allocs:
+    """torch.full on the CPU that raises torch.cuda.OutOfMemoryError on the
+    n-th allocation (the injected failure)."""
+
+    def __init__(self, fail_at=None):
+        self.n, self.fail_at = 0, fail_at
+
+    def __call__(self, shape, dtype, fill):
+        import torch
+
+        self.n += 1
+        if self.fail_at is not None and self.n == self.fail_at:
+            raise torch.cuda.OutOfMemoryError("injected: allocation failed")
+        return torch.full(shape, fill, dtype=dtype)
+
+
+def _old_cache():
+    import torch
+
+    import quantized_expert_ffn_router_gb300 as ft
+
+    st = ft.DeviceCacheState(2, 8, 4, device="cpu")
+    st.slot_owner.copy_(torch.tensor([3, 9, -1, 12], dtype=torch.int32))
+    st.usage.copy_(torch.tensor([5, 7, -1, 2], dtype=torch.int64))
+    st.map[3], st.map[9], st.map[12] = 0, 1, 3
+    st.step.fill_(8)
+    n, stride = ft.block_bytes(0, 256, 128, 32)
+    cache = torch.arange(4 * n, dtype=torch.int64).remainder(251).to(torch.uint8).reshape(4, n)
+    return st, cache, n
+
+
+def _snapshot(st, cache):
+    return [t.clone() for t in (st.slot_owner, st.map, st.usage, st.recency, st.step, cache)]
+
+
+@pytest.mark.parametrize("fail_at", [1, 2, 3, 4, 5, 6])
+def test_resize_cache_allocation_failure_leaves_old_cache(fail_at):
+    """Any of the six allocations of a resize (five state arrays and the bank)
+    failing raises before the library is called; the running cache is as it
+    was."""
+    import torch
+
+    from quantized_expert_ffn_router_gb300.pipeline import resize_cache
+
+    st, cache, n = _old_cache()
+    before = _snapshot(st, cache)
+    calls = []
+    with pytest.raises(torch.cuda.OutOfMemoryError):
+        resize_cache(st, cache, 0, 256, 128, 32, 6, 1 << 30, alloc=_Allocs(fail_at),
+                     rebuild=lambda *a, **k: calls.append(a))
+    assert calls == []
+    for a, b in zip(before, _snapshot(st, cache)):
+        assert torch.equal(a, b)
+
+
+def test_resize_cache_refused_rebuild_leaves_old_cache():
+    """A rebuild the library refuses (here: over budget) propagates its
+    FT_ERR_REJECTED; the old state and bank are untouched."""
+    import torch
+
+    import quantized_expert_ffn_router_gb300 as ft
+    from quantized_expert_ffn_router_gb300.pipeline import resize_cache
+
+    st, cache, n = _old_cache()
+    before = _snapshot(st, cache)
+
+    def refuse(old_state, old_bank, new_state, new_bank, budget, **kw):
+        assert new_state.S == 6 and new_bank.n_blocks == 6 and new_bank.stride == n
+        assert old_bank.base == cache.data_ptr()
+        raise ft.FtError(ft.FT_ERR_REJECTED, "over budget")
+
+    with pytest.raises(ft.FtError) as ei:
+        resize_cache(st, cache, 0, 256, 128, 32, 6, 100, alloc=_Allocs(), rebuild=refuse)
+    assert ei.value.status == ft.FT_ERR_REJECTED
+    for a, b in zip(before, _snapshot(st, cache)):
+        assert torch.equal(a, b)
+
+
+def test_resize_cache_allocates_everything_before_the_rebuild():
+    """All six allocations happen before the library call, which receives the
+    new buffers; the new objects are returned."""
+    from quantized_expert_ffn_router_gb300.pipeline import resize_cache
+
+    st, cache, n = _old_cache()
+    allocs = _Allocs()
+    seen = []
+
+    def rebuild(old_state, old_bank, new_state, new_bank, budget, **kw):
+        seen.append((allocs.n, new_state.S, new_bank.n_blocks, budget))
+
+    new_state, new_cache, new_bank = resize_cache(st, cache, 0, 256, 128, 32, 3, 12345, alloc=allocs,
+                                                  rebuild=rebuild)
+    assert seen == [(6, 3, 3, 12345)]
+    assert new_state.S == 3 and tuple(new_cache.shape) == (3, n) and new_bank.base == new_cache.data_ptr()

@@ -3,15 +3,15 @@
 Callers inside a stream capture or under another framework's memory pool
 cannot pass a workspace; ft_moe_experts_decode_static uses a scratch array the
 library owns instead.  Its results must match ft_moe_experts_fwd with a
-caller workspace, call after call (the shared scratch keeps the previous
-call's contents).  This file is collected last on purpose."""
+caller workspace and the CPU oracle, call after call (the shared scratch
+keeps the previous call's contents).  This file is collected last on purpose."""
 
 import numpy as np
 import pytest
 import torch
 
 import synth
-from gpu_helpers import assert_close, pool_blocks
+from gpu_helpers import assert_close, oracle_pairs_output, pool_blocks
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -24,10 +24,12 @@ def _case(cfg, T, seed):
     used = sorted(set(ids.ravel().tolist()))
     slot = {e: s for s, e in enumerate(used)}
     slots = np.vectorize(slot.get)(ids).astype(np.int32)
-    blocks = torch.from_numpy(pool_blocks(cfg, used)).to(DEV)
+    blocks_np = pool_blocks(cfg, used)
+    blocks = torch.from_numpy(blocks_np).to(DEV)
     w = rng.uniform(0.05, 0.3, (T, k)).astype(np.float32)
     x = synth.normal_bf16(synth.stream_key(seed, "noalloc-x"), (T, cfg.H))
-    return ids, slots, blocks, w, x
+    by_fid = {int(e): blocks_np[i] for i, e in enumerate(used)}  # layer 0: flat id = expert id
+    return ids, slots, blocks, w, x, by_fid
 
 
 @pytest.mark.parametrize("name,T", [("d35b", 1), ("flash", 1), ("tiny", 8)])
@@ -37,7 +39,7 @@ def test_static_scratch_matches_workspace_call_twice(cuda_lib, name, T):
     ts_np = synth.tensor_scales(cfg.fmt, cfg.H, cfg.I, cfg.L * cfg.E)
     ts = None if ts_np is None else torch.from_numpy(ts_np).to(DEV)
     for call in range(2):  # two calls in a row with different inputs
-        ids, slots, blocks, w, x = _case(cfg, T, 100 + call)
+        ids, slots, blocks, w, x, by_fid = _case(cfg, T, 100 + call)
         cb = ft.make_bank(cfg.fmt, cfg.H, cfg.I, cfg.g, blocks, ts)
         args = [torch.from_numpy(a).to(DEV) for a in (x.view(np.int16), slots, ids, w)]
         ref = torch.empty((T, cfg.H), dtype=torch.float32, device=DEV)
@@ -51,6 +53,9 @@ def test_static_scratch_matches_workspace_call_twice(cuda_lib, name, T):
         torch.cuda.synchronize()
         assert ft.get_status(status) == 0
         assert_close(got.cpu().numpy(), ref.cpu().numpy(), f"{name} static call {call}", ref_max=None)
+        # and both against the oracle
+        oref = oracle_pairs_output(by_fid, cfg, ts_np, x, ids, w, 0)
+        assert_close(got.cpu().numpy(), oref, f"{name} static call {call} vs oracle")
 
 
 def test_static_scratch_rejects_oversize(cuda_lib):
