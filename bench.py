@@ -361,16 +361,20 @@ class DecodeWorkload:
         return self.fused
 
     def capture(self):
-        """Two graphs of one step: `graph` (timed) with events only around the
-        experts calls, `graph_ops` with events around every op (breakdown).
-        Each recapture replaces both graphs and their events together."""
+        """Three graphs of one step: `graph` (timed) with no event inside (an
+        event node between kernels breaks the programmatic launch chain),
+        `graph_ev` with events around the layer kernel (fused) or the experts
+        call (separate) of every EXP_EVERY-th layer (launch durations, replayed
+        after the timed region), `graph_ops` with events around every op
+        (breakdown).  Each recapture replaces the graphs and their events
+        together."""
         import torch
 
         def events(n, rows):
             return [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(n)]
                     for _ in range(rows)]
 
-        self.graph = self.graph_ops = None  # before their events go
+        self.graph = self.graph_ev = self.graph_ops = None  # before their events go
         self.ev_exp = events(2, (self.cfg.L + self.EXP_EVERY - 1) // self.EXP_EVERY)
         self.ev_ops = events(len(self.OPS) + 1, self.cfg.L)
         self.x_stage.copy_(self.x_all[0])
@@ -378,6 +382,9 @@ class DecodeWorkload:
         torch.cuda.synchronize()
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph):
+            self.step()
+        self.graph_ev = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph_ev):
             self.step(self.ev_exp)
         self.graph_ops = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph_ops):
@@ -402,6 +409,18 @@ class DecodeWorkload:
             self.graph.replay()
         torch.cuda.synchronize()
 
+    def fresh_inputs(self, seed: int):
+        """Refill the device copy of the per-step inputs with new tokens
+        (N(0,1) bf16, feature 0 = 1.0), so that a further timed run meets
+        tokens the cache has not adapted to."""
+        import torch
+
+        g = torch.Generator(device=self.dev)
+        g.manual_seed(seed)
+        xv = self.x_all.view(torch.bfloat16)
+        xv.normal_(generator=g)
+        xv[..., 0] = 1.0
+
     def fetch_rate(self, first: int, reps: int = 20):
         """Mean fetched experts and host-path pairs per step over `reps` replays
         on the inputs first.. (outside the timed region)."""
@@ -415,11 +434,20 @@ class DecodeWorkload:
             hp += int((self.slot < 0).sum().item())
         return nf / reps, hp / reps
 
-    def experts_us(self):
-        """Mean device time (us) of one layer kernel (fused) or one experts call
-        (separate: gate/up + down) over the sampled layers of the last timed
-        replay."""
-        return sum(e[0].elapsed_time(e[1]) for e in self.ev_exp) * 1e3 / len(self.ev_exp)
+    def experts_us(self, first: int = 0, reps: int = 5):
+        """Device time (us) of one layer kernel (fused) or one experts call
+        (separate: gate/up + down): the median over `reps` replays of the
+        sampling graph (on inputs first..) of the mean over its sampled
+        layers."""
+        import torch
+
+        runs = []
+        for i in range(reps):
+            self.x_stage.copy_(self.x_all[(first + i) % self.x_all.shape[0]])
+            self.graph_ev.replay()
+            torch.cuda.synchronize()
+            runs.append(sum(e[0].elapsed_time(e[1]) for e in self.ev_exp) * 1e3 / len(self.ev_exp))
+        return statistics.median(runs)
 
     def op_times(self, first: int, reps: int = 5):
         """Per-op device time (us per step, summed over layers): the median of
@@ -673,7 +701,8 @@ def phi_bench(wl, phi: int, args, units, reduce_fn, world, log=print):
 
     old = wl.phi
     wl.phi = phi
-    wl.use_fused(wl.fused or args.layer_kernel == "fused")
+    wl.use_fused(args.layer_kernel == "fused")
+    wl.fresh_inputs(2000 + phi)
     wl.capture()
     wl.settle(max(64, args.settle // 4), seed=2)
     secs = time_device(wl, args.steps, args.warmup, reduce_fn, world, None)
@@ -907,6 +936,10 @@ def kernel_case(name: str, T: int):
     kernel family on a bank that fits in a few GB (no pool, no history).
       decode:  ft_moe_experts_fwd decode on the d35b or flash shape, fresh
                random experts each call (nothing reused in L2);
+      decode-step: the whole decode layer on two d35b-shaped layers over a
+               128-slot cache, as separate calls and as the fused kernel;
+      prefill-layer: route, permute, grouped experts and combine of one
+               prefill layer (256 experts resident, --tokens, default 2048);
       prefill: permute + ft_moe_experts_fwd prefill, NVFP4 H 4096 I 2048,
                16 experts, top-6, 512 tokens (or --tokens >= 16)."""
     import torch
@@ -942,6 +975,59 @@ def kernel_case(name: str, T: int):
             slots = torch.from_numpy(ids + (c % 2) * E).to(dev)
             ft.experts_fwd(cb, None, 0, E, x, T, k, slots, torch.from_numpy(ids).to(dev), w, out, ws,
                            dev_status=status)
+    elif name == "decode-step":
+        # two d35b-shaped layers (256 experts, top-8, H 2048, I 512, int4 g64)
+        # over a 128-slot cache, half filled: 4 steps of the separate calls
+        # (route, resolve, fetch, experts) then 4 of the fused layer kernel,
+        # on fresh tokens (misses, fetches and host-path pairs included)
+        cfg = synth.get_config("d35b")
+        L, E, k, H, I, g, S = 2, cfg.E, cfg.k, cfg.H, cfg.I, cfg.g, 128
+        _, stride = synth.block_layout(cfg.fmt, H, I, g)
+        pool = torch.empty((L * E, stride), dtype=torch.uint8).pin_memory()
+        tmp = torch.empty((64, stride), dtype=torch.uint8, device=dev)
+        for f0 in range(0, L * E, 64):
+            synth.bank_blocks_torch(cfg.seed, range(f0, f0 + 64), cfg.fmt, H, I, g, tmp, ref_K=cfg.ref_K)
+            pool[f0:f0 + 64].copy_(tmp)
+        cache = torch.empty((S, stride), dtype=torch.uint8, device=dev)
+        st = ft.DeviceCacheState(L, E, S, device=dev)
+        fids = torch.from_numpy(rng.choice(L * E, S // 2, replace=False).astype(np.int32)).to(dev)
+        slots = torch.arange(S // 2, dtype=torch.int32, device=dev)
+        st.slot_owner[: S // 2].copy_(fids)
+        st.map[fids.long()] = slots
+        st.usage[: S // 2].copy_(torch.arange(S // 2, dtype=torch.int64, device=dev))
+        st.step.fill_(S)
+        pb, cb = ft.make_bank(cfg.fmt, H, I, g, pool), ft.make_bank(cfg.fmt, H, I, g, cache)
+        ft.fetch(pb, cb, torch.tensor([S // 2], dtype=torch.int32, device=dev), fids, slots)
+        Ws = [torch.from_numpy(synth.router_weights(cfg.seed, l, E, H, cfg.router_std, zipf_bias=cfg.zipf)).to(dev)
+              for l in range(L)]
+        ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+        w = torch.empty((T, k), dtype=torch.float32, device=dev)
+        sl = torch.empty((T, k), dtype=torch.int32, device=dev)
+        nf = torch.zeros(1, dtype=torch.int32, device=dev)
+        ff = torch.empty(T * k, dtype=torch.int32, device=dev)
+        fs = torch.empty(T * k, dtype=torch.int32, device=dev)
+        out = torch.empty((T, H), dtype=torch.int16, device=dev)
+        rws = torch.zeros(ft.route_workspace(T, E), dtype=torch.uint8, device=dev)
+        ews = torch.zeros(ft.experts_workspace(ft.FT_DECODE, T, k, H, I, E), dtype=torch.uint8, device=dev)
+        lws = torch.zeros(ft.decode_layer_workspace(T, k, H, I, E), dtype=torch.uint8, device=dev)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(5)
+        x = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        torch.cuda.synchronize()
+        for fused in (False, True):
+            for step in range(4):
+                for l in range(L):
+                    x.normal_(generator=gen)
+                    x[:, 0] = 1.0
+                    xi = x.view(torch.int16)
+                    if fused:
+                        ft.decode_layer(xi, Ws[l], k, st, l, 65536, cb, pb, ids, w, sl, nf, ff, fs, out, lws,
+                                        dev_status=status)
+                    else:
+                        ft.route(xi, Ws[l], k, ids, w, rws)
+                        ft.resolve_slots(st, l, ids, 65536, sl, nf, ff, fs, status)
+                        ft.fetch(pb, cb, nf, ff, fs, status)
+                        ft.experts_fwd(cb, pb, l, E, xi, T, k, sl, ids, w, out, ews, dev_status=status)
     elif name == "prefill":
         # --tokens 128: ~48 rows per expert (the 2048-token layer's regime);
         # 512 (the default): ~192 rows per expert (the 8192-token layer's)
@@ -968,6 +1054,41 @@ def kernel_case(name: str, T: int):
         for _ in range(2):
             ft.experts_fwd(cb, None, 0, E, xp, Tp, k, slot, None, None, yp, ews, mode=ft.FT_PREFILL,
                            offsets=off, dev_status=status, x_scale=xs)
+    elif name == "prefill-layer":
+        # one whole prefill layer at the benchmark's shape (NVFP4, H 4096,
+        # I 2048, 256 experts resident, top-6) for --tokens (default 2048)
+        # tokens: route (tiled logits + top-k), permute, grouped experts,
+        # combine; twice
+        cfg = synth.get_config("prefill")
+        H, I, E, k = cfg.H, cfg.I, cfg.E, cfg.k
+        Tp = T if T >= 16 else 2048
+        _, stride = synth.block_layout(cfg.fmt, H, I, cfg.g)
+        bank = torch.empty((E, stride), dtype=torch.uint8, device=dev)
+        synth.bank_blocks_torch(cfg.seed, range(E), cfg.fmt, H, I, cfg.g, bank)
+        ts = torch.from_numpy(synth.tensor_scales(cfg.fmt, H, I, E)).to(dev)
+        cb = ft.make_bank(cfg.fmt, H, I, cfg.g, bank, ts)
+        W = torch.from_numpy(synth.router_weights(cfg.seed, 0, E, H, cfg.router_std)).to(dev)
+        x = torch.from_numpy(synth.normal_bf16(synth.stream_key(cfg.seed, "prefill-x", Tp), (Tp, H)).view(np.int16)).to(dev)
+        n = Tp * k
+        ids = torch.empty((Tp, k), dtype=torch.int32, device=dev)
+        w = torch.empty((Tp, k), dtype=torch.float32, device=dev)
+        rws = torch.zeros(ft.route_workspace(Tp, E), dtype=torch.uint8, device=dev)
+        perm = torch.empty(n, dtype=torch.int32, device=dev)
+        inv = torch.empty((Tp, k), dtype=torch.int32, device=dev)
+        off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        xp = torch.empty((n, H), dtype=torch.int16, device=dev)
+        xs = torch.empty(n, device=dev)
+        pws = torch.empty(ft.permute_workspace(Tp, k, E), dtype=torch.uint8, device=dev)
+        yp = torch.empty((n, H), dtype=torch.int16, device=dev)
+        out = torch.empty((Tp, H), dtype=torch.int16, device=dev)
+        ews = torch.empty(ft.experts_workspace(ft.FT_PREFILL, Tp, k, H, I, E), dtype=torch.uint8, device=dev)
+        slot = torch.arange(E, dtype=torch.int32, device=dev)
+        for _ in range(2):
+            ft.route(x, W, k, ids, w, rws)
+            ft.permute(ids, E, x, perm, inv, off, xp, pws, dev_status=status, xp_scale=xs)
+            ft.experts_fwd(cb, None, 0, E, xp, Tp, k, slot, None, None, yp, ews, mode=ft.FT_PREFILL,
+                           offsets=off, dev_status=status, x_scale=xs)
+            ft.combine(yp, inv, w, out)
     else:
         raise SystemExit(f"unknown case {name}")
     torch.cuda.synchronize()
@@ -993,10 +1114,11 @@ def main():
     ap.add_argument("--no-flash", action="store_true", help="skip the NVFP4 (flash) decode measurement")
     ap.add_argument("--prefill-layers", type=int, default=3,
                     help="layers streamed from host memory through the prefill double buffer (0: skip)")
-    ap.add_argument("--layer-kernel", choices=["fused", "separate"], default="fused",
-                    help="decode step as one ft_moe_decode_layer kernel per layer (when the shape fits) or as the "
-                         "separate route / resolve / fetch / experts calls")
-    ap.add_argument("--case", choices=["decode", "decode-flash", "prefill"],
+    ap.add_argument("--layer-kernel", choices=["fused", "separate"], default="separate",
+                    help="decode step as the separate route / resolve / fetch / experts calls (measured faster) or "
+                         "as one ft_moe_decode_layer kernel per layer (when the shape fits); the other form is "
+                         "timed too and reported in detail")
+    ap.add_argument("--case", choices=["decode", "decode-flash", "decode-step", "prefill", "prefill-layer"],
                     help="run a small kernel case for a profiler instead of the benchmark")
     args = ap.parse_args()
     if args.case:
@@ -1066,19 +1188,27 @@ def main():
             raise RuntimeError(f"device status {st} during the benchmark")
         log(f"T={T}: {value:.1f} {UNIT}, {secs_max / args.steps * 1e3:.3f} ms/step, "
             f"{'fused' if fused else 'separate'}, kernels {kt}")
-        if fused:
-            # the same step through the separate calls, for comparison (after the timed runs)
-            wl.use_fused(False)
+        # the same step in the other form (one fused kernel per layer, or the
+        # separate calls), timed the same way after the headline runs
+        if wl.use_fused(not fused) != fused:
+            wl.fresh_inputs(1000 + T)
             wl.capture()
-            secs_sep = time_device(wl, args.steps, args.warmup, reduce_fn, world, None)
-            v_sep, s_sep, _ = aggregate(units, secs_sep, world, reduce_fn)
-            results[T]["separate"] = {"value": v_sep, "ms_per_step": s_sep / args.steps * 1e3,
-                                      "experts_us_per_call": wl.experts_us(),
-                                      "per_op_us_per_step": wl.op_times(first=args.warmup + 2 * args.steps)}
-            log(f"T={T} separate calls: {v_sep:.1f} {UNIT}, {s_sep / args.steps * 1e3:.3f} ms/step")
+            wl.settle(max(32, args.settle // 8), seed=3)
+            secs_o = time_device(wl, args.steps, args.warmup, reduce_fn, world, None)
+            v_o, s_o, _ = aggregate(units, secs_o, world, reduce_fn)
+            results[T]["other_form"] = {"form": "fused" if wl.fused else "separate", "value": v_o,
+                                        "ms_per_step": s_o / args.steps * 1e3,
+                                        "us_per_layer": s_o / args.steps / cfg.L * 1e6,
+                                        "launch_us_sampled": wl.experts_us(),
+                                        "fetched_experts_per_step": wl.fetch_rate(first=args.warmup + 2 * args.steps
+                                                                                  + 5)[0]}
+            log(f"T={T} {'fused' if wl.fused else 'separate'} form: {v_o:.1f} {UNIT}, "
+                f"{s_o / args.steps * 1e3:.3f} ms/step")
             st = ft.get_status(wl.status)
             if st != 0:
                 raise RuntimeError(f"device status {st} during the benchmark")
+            wl.use_fused(fused)
+            wl.capture()
         if bi == 0:
             results[T]["host_link"] = host_link_bench(wl, log)
             if args.phi != 26214:
@@ -1119,6 +1249,10 @@ def main():
     kt = r["kt"] or {}
     dom = max(kt, key=kt.get) if kt else "experts"
     exp_us = r["exp_us"]
+    if r["fused"]:
+        # one kernel per layer and nothing else in the step: the timed
+        # region's CUDA events over steps x L launches give its duration
+        exp_us = r["secs"] / args.steps / cfg.L * 1e6
     roof = None
     router_bytes = cfg.E * cfg.H * 4
     if exp_us:
@@ -1136,8 +1270,13 @@ def main():
                 "peak_kind": peak_kind, "frac_of_8tbs_nominal": achieved / 8000.0,
                 "algorithmic_bytes_per_launch": per_call,
                 "launch_us": exp_us,
-                "timing": f"events around the {'layer kernel' if r['fused'] else 'experts calls'} of every "
-                          f"{DecodeWorkload.EXP_EVERY}th layer of the timed replays",
+                "launch_us_sampled": r["exp_us"],
+                "timing": ("CUDA events around the timed region on the launching stream / (steps x 40 launches): the "
+                           "step is one ft_moe_decode_layer kernel per layer and nothing else; launch_us_sampled: "
+                           "events around every 8th layer's kernel in a copy of the graph replayed after the timed "
+                           "region (each event node also breaks the launch chain)") if r["fused"] else
+                          (f"events around the experts calls of every {DecodeWorkload.EXP_EVERY}th layer in a copy of "
+                           "the step's graph replayed after the timed region"),
                 "step_us_per_layer": r["secs"] / args.steps / cfg.L * 1e6,
                 "dominant_op_by_time": dom}
     cpu = None
@@ -1171,7 +1310,7 @@ def main():
             "step": ("per layer: ft_moe_decode_layer (one kernel: route, resolve with the q* split, fetch, "
                      "experts, combine)" if r["fused"] else
                      "per layer: ft_moe_route, ft_moe_resolve_slots, ft_moe_fetch, ft_moe_experts_fwd (two kernels)"),
-            "separate_calls": r.get("separate"),
+            "other_form": r.get("other_form"),
             "phi_26214": r.get("phi_26214"),
             "host_link": r.get("host_link"),
             "settle_steps": args.settle,
@@ -1192,7 +1331,7 @@ def main():
             "other_batches": {str(T): {"value": v["value"], "ms_per_step": v["secs"] / args.steps * 1e3,
                                        "per_op_us_per_step": v["kt"], "expert_bytes_per_step": v["ebytes"],
                                        "fused": v["fused"], "launch_us": v["exp_us"],
-                                       "separate_calls": v.get("separate"),
+                                       "other_form": v.get("other_form"),
                                        "e2e": v["e2e"]}
                               for T, v in results.items() if T != args.tokens},
         },

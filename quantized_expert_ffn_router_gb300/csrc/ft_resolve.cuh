@@ -33,7 +33,14 @@ struct ResolveArgs {
   int32_t* fetch_fid;
   int32_t* fetch_slot;
   int32_t* dev_status;
+  // optional shared-memory copies of slot_ids [n] and num_fetch, for a caller
+  // that runs the resolve inside a larger kernel (null: global outputs only)
+  int32_t* slot_ids_sm;
+  int32_t* num_fetch_sm;
+  const int32_t* ids_sm;  // optional shared-memory copy of ids [n], read instead of ids
 };
+
+__device__ __forceinline__ int resolve_id(const ResolveArgs& a, int i) { return a.ids_sm ? a.ids_sm[i] : a.ids[i]; }
 
 __host__ __device__ inline size_t resolve_smem_bytes(int E, int n) {
   const int cap = n < E ? n : E;
@@ -103,7 +110,7 @@ __device__ bool resolve_small_no_fetch(const ResolveArgs& a) {
   const int lane = threadIdx.x & 31;
   const int n = a.n, E = a.E, base = a.layer * a.E;
   const int64_t now = *a.step;
-  const int e = lane < n ? a.ids[lane] : -1;
+  const int e = lane < n ? resolve_id(a, lane) : -1;
   const bool bad = lane < n && (e < 0 || e >= E);
   if (__any_sync(0xffffffffu, bad)) return false;
   const int s = lane < n ? a.map[base + e] : -1;
@@ -117,13 +124,17 @@ __device__ bool resolve_small_no_fetch(const ResolveArgs& a) {
     if (s >= 0) a.usage[s] = now;
     a.recency[base + e] = now;
   }
-  if (lane < n) a.slot_ids[lane] = s;
+  if (lane < n) {
+    a.slot_ids[lane] = s;
+    if (a.slot_ids_sm) a.slot_ids_sm[lane] = s;
+  }
   for (int i = lane; i < a.max_list; i += 32) {
     a.fetch_fid[i] = -1;
     a.fetch_slot[i] = -1;
   }
   if (lane == 0) {
     *a.num_fetch = 0;
+    if (a.num_fetch_sm) *a.num_fetch_sm = 0;
     *a.step = now + 1;
   }
   return true;
@@ -179,7 +190,7 @@ __device__ __noinline__ void resolve_block(const ResolveArgs& a, unsigned char* 
   }
   __syncthreads();
   for (int i = tid; i < n; i += nt) {
-    const int e = a.ids[i];
+    const int e = resolve_id(a, i);
     if (e < 0 || e >= E)
       s_bad = 1;
     else
@@ -188,13 +199,17 @@ __device__ __noinline__ void resolve_block(const ResolveArgs& a, unsigned char* 
   __syncthreads();
   if (s_bad) {
     if (!a.prefetch)
-      for (int i = tid; i < n; i += nt) a.slot_ids[i] = -1;
+      for (int i = tid; i < n; i += nt) {
+        a.slot_ids[i] = -1;
+        if (a.slot_ids_sm) a.slot_ids_sm[i] = -1;
+      }
     for (int i = tid; i < a.max_list; i += nt) {
       a.fetch_fid[i] = -1;
       a.fetch_slot[i] = -1;
     }
     if (tid == 0) {
       *a.num_fetch = 0;
+      if (a.num_fetch_sm) *a.num_fetch_sm = 0;
       record_status(a.dev_status, FT_ERR_BAD_ID);
     }
     return;
@@ -337,7 +352,8 @@ __device__ __noinline__ void resolve_block(const ResolveArgs& a, unsigned char* 
     int c = 0;
     for (int s = tid; s < S; s += nt)
       if (!slot_hit(s) && ukey(slot_use(s)) == gmin) ++c;
-    atomicAdd(&s_cmin, c);
+    c = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(c)));
+    if ((tid & 31) == 0 && c != 0) atomicAdd(&s_cmin, c);
     if (tid == 0) {
       s_prefix = 0ull;
       s_krem = nf;
@@ -354,23 +370,52 @@ __device__ __noinline__ void resolve_block(const ResolveArgs& a, unsigned char* 
         for (int b = tid; b < 256; b += nt) hist[b] = 0;
         __syncthreads();
         const unsigned long long pre = s_prefix;
-        for (int s = tid; s < S; s += nt) {
-          if (slot_hit(s)) continue;
-          const unsigned long long d = ukey(slot_use(s)) - gmin;
-          const bool match = (shift + 8 >= 64) ? true : ((d >> (shift + 8)) == pre);
-          if (match) atomicAdd(&hist[(d >> shift) & 255ull], 1u);
+        // histogram of the digit: one shared-memory add per distinct digit of
+        // a warp (slots with close usage share digits, and per-slot adds to
+        // one counter would serialise)
+        for (int s0 = 0; s0 < S; s0 += nt) {
+          const int s = s0 + tid;
+          int bin = -1;
+          if (s < S && !slot_hit(s)) {
+            const unsigned long long d = ukey(slot_use(s)) - gmin;
+            const bool match = (shift + 8 >= 64) ? true : ((d >> (shift + 8)) == pre);
+            if (match) bin = static_cast<int>((d >> shift) & 255ull);
+          }
+          const unsigned peers = __match_any_sync(0xffffffffu, bin);
+          if (bin >= 0 && (tid & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], static_cast<unsigned>(__popc(peers)));
         }
         __syncthreads();
-        if (tid == 0) {
-          int krem = s_krem;
-          int b = 0;
-          unsigned int cum = 0;
-          for (; b < 256; ++b) {
-            if (cum + hist[b] >= static_cast<unsigned int>(krem)) break;
-            cum += hist[b];
+        if (tid < 32) {
+          // the first digit at which the running count reaches krem: lane l
+          // sums digits 8l..8l+7, a warp scan gives the lane, that lane the digit
+          const int lane = tid;
+          unsigned c8[8];
+          unsigned loc = 0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            c8[j] = hist[8 * lane + j];
+            loc += c8[j];
           }
-          s_krem = krem - static_cast<int>(cum);
-          s_prefix = (pre << 8) | static_cast<unsigned long long>(b);
+          unsigned incl = loc;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          const int krem = s_krem;
+          const unsigned reach = __ballot_sync(0xffffffffu, incl >= static_cast<unsigned>(krem));
+          const int first = reach ? __ffs(reach) - 1 : 31;
+          if (lane == first) {
+            unsigned cum = incl - loc;
+            int b = 0;
+            for (; b < 8; ++b) {
+              if (cum + c8[b] >= static_cast<unsigned>(krem)) break;
+              cum += c8[b];
+            }
+            const int digit = reach ? 8 * lane + b : 256;  // 256: no digit reaches krem (cannot happen)
+            s_krem = krem - static_cast<int>(cum);
+            s_prefix = (pre << 8) | static_cast<unsigned long long>(digit);
+          }
         }
         __syncthreads();
       }
@@ -451,13 +496,18 @@ __device__ __noinline__ void resolve_block(const ResolveArgs& a, unsigned char* 
 
   // 6. outputs
   if (!a.prefetch)
-    for (int i = tid; i < n; i += nt) a.slot_ids[i] = slotOf[a.ids[i]];
+    for (int i = tid; i < n; i += nt) {
+      const int sl = slotOf[resolve_id(a, i)];
+      a.slot_ids[i] = sl;
+      if (a.slot_ids_sm) a.slot_ids_sm[i] = sl;
+    }
   for (int i = tid; i < a.max_list; i += nt) {
     a.fetch_fid[i] = (i < nf) ? base + fe[i] : -1;
     a.fetch_slot[i] = (i < nf) ? vs2[i] : -1;
   }
   if (tid == 0) {
     *a.num_fetch = nf;
+    if (a.num_fetch_sm) *a.num_fetch_sm = nf;
     if (!a.prefetch) *a.step = now + 1;
   }
 }

@@ -38,11 +38,12 @@ __device__ __forceinline__ void lane_best(const float* ls, int E, int lane, floa
 // Top-k of one token's E logits by one warp; ls is this warp's E floats of
 // shared memory.
 __device__ __forceinline__ void topk_warp(const float* __restrict__ l, float* ls, int E, int k, int renorm,
-                                          int32_t* __restrict__ ids_t, float* __restrict__ wts_t) {
+                                          int32_t* __restrict__ ids_t, float* __restrict__ wts_t,
+                                          int stride = 1) {
   const int lane = threadIdx.x & 31;
   float mx = -INFINITY;
   for (int e = lane; e < E; e += 32) {
-    const float v = __ldcg(l + e);
+    const float v = __ldcg(l + static_cast<size_t>(e) * stride);
     ls[e] = v;
     mx = fmaxf(mx, v);
   }
@@ -102,7 +103,8 @@ __device__ __forceinline__ uint32_t order_key(float v) {
 
 template <int VPL>
 __device__ __forceinline__ void topk_warp_reg(const float* __restrict__ l, int E, int k, int renorm,
-                                              int32_t* __restrict__ ids_t, float* __restrict__ wts_t) {
+                                              int32_t* __restrict__ ids_t, float* __restrict__ wts_t,
+                                              int stride = 1) {
   const int lane = threadIdx.x & 31;
   float v[VPL];
   uint32_t key[VPL];
@@ -110,7 +112,7 @@ __device__ __forceinline__ void topk_warp_reg(const float* __restrict__ l, int E
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
     const int e = lane + 32 * i;
-    v[i] = e < E ? __ldcg(l + e) : -INFINITY;
+    v[i] = e < E ? __ldcg(l + static_cast<size_t>(e) * stride) : -INFINITY;
     key[i] = e < E ? order_key(v[i]) : 0u;
     if (e < E) mx = fmaxf(mx, v[i]);
   }
@@ -154,15 +156,15 @@ __device__ __forceinline__ void topk_warp_reg(const float* __restrict__ l, int E
 }
 
 // Top-k of one token by one warp: the register form for E <= 512, else the
-// shared-memory form (ls: this warp's E floats).
+// shared-memory form (ls: this warp's E floats).  Logit e is l[e * stride].
 __device__ __forceinline__ void topk_any(const float* __restrict__ l, float* ls, int E, int k, int renorm,
-                                         int32_t* __restrict__ ids_t, float* __restrict__ wts_t) {
-  if (E <= 32) topk_warp_reg<1>(l, E, k, renorm, ids_t, wts_t);
-  else if (E <= 64) topk_warp_reg<2>(l, E, k, renorm, ids_t, wts_t);
-  else if (E <= 128) topk_warp_reg<4>(l, E, k, renorm, ids_t, wts_t);
-  else if (E <= 256) topk_warp_reg<8>(l, E, k, renorm, ids_t, wts_t);
-  else if (E <= 512) topk_warp_reg<16>(l, E, k, renorm, ids_t, wts_t);
-  else topk_warp(l, ls, E, k, renorm, ids_t, wts_t);
+                                         int32_t* __restrict__ ids_t, float* __restrict__ wts_t, int stride = 1) {
+  if (E <= 32) topk_warp_reg<1>(l, E, k, renorm, ids_t, wts_t, stride);
+  else if (E <= 64) topk_warp_reg<2>(l, E, k, renorm, ids_t, wts_t, stride);
+  else if (E <= 128) topk_warp_reg<4>(l, E, k, renorm, ids_t, wts_t, stride);
+  else if (E <= 256) topk_warp_reg<8>(l, E, k, renorm, ids_t, wts_t, stride);
+  else if (E <= 512) topk_warp_reg<16>(l, E, k, renorm, ids_t, wts_t, stride);
+  else topk_warp(l, ls, E, k, renorm, ids_t, wts_t, stride);
 }
 
 }  // namespace

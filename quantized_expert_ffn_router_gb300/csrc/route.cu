@@ -23,8 +23,15 @@ constexpr int kRouteMaxE = 4096;
 // offset for every T, so a workspace sized for one T serves any smaller T.
 constexpr size_t kRouteCounterBytes = 256;
 
+// Logits of the one-kernel path (T <= 16): [E][kRowsT(T)], every expert's
+// logits in a 32-byte sector (or two) of their own, since each is written by
+// a different CTA and partial writes from many SMs to one sector would queue
+// behind each other.  The tiled path keeps [T][E].
+__host__ __device__ constexpr int route_row_stride(int T) { return T <= 8 ? 8 : 16; }
+
 size_t route_logits_bytes(int T, int E) {
-  return (static_cast<size_t>(T) * E * sizeof(float) + 255) & ~static_cast<size_t>(255);
+  const size_t n = T <= kGemvMaxT ? static_cast<size_t>(E) * route_row_stride(T) : static_cast<size_t>(T) * E;
+  return (n * sizeof(float) + 255) & ~static_cast<size_t>(255);
 }
 
 // Small token counts: one CTA per expert row, its 8 warps splitting the
@@ -107,7 +114,7 @@ __global__ void __launch_bounds__(256) route_rows_kernel(const uint16_t* __restr
     float v = 0.f;
 #pragma unroll
     for (int w = 0; w < 8; ++w) v += part[w][threadIdx.x];
-    logits[static_cast<size_t>(threadIdx.x) * E + e] = v;
+    logits[static_cast<size_t>(e) * route_row_stride(T) + threadIdx.x] = v;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -124,8 +131,8 @@ __global__ void __launch_bounds__(256) route_rows_kernel(const uint16_t* __restr
   __syncthreads();
   if (!s_last) return;
   for (int t = warp; t < T; t += 8)
-    topk_any(logits + static_cast<size_t>(t) * E, lsm + static_cast<size_t>(warp) * E, E, k, renorm,
-             ids + static_cast<size_t>(t) * k, wts + static_cast<size_t>(t) * k);
+    topk_any(logits + t, lsm + static_cast<size_t>(warp) * E, E, k, renorm,
+             ids + static_cast<size_t>(t) * k, wts + static_cast<size_t>(t) * k, route_row_stride(T));
 }
 
 // Tiled SIMT GEMM: a 64-token x 64-expert tile per CTA, 256 threads with 4x4
