@@ -228,7 +228,7 @@ class DecodeWorkload:
         self.ml = T * k
         self.ff = torch.empty((L, self.ml), dtype=torch.int32, device=device)
         self.fs = torch.empty((L, self.ml), dtype=torch.int32, device=device)
-        self.rws = torch.zeros(ft.route_workspace(T, E), dtype=torch.uint8, device=device)
+        self.rws = torch.zeros(ft.route_workspace(T, E, H), dtype=torch.uint8, device=device)
         self.ews = torch.zeros(ft.experts_workspace(ft.FT_DECODE, T, k, H, I, E), dtype=torch.uint8,
                                device=device)
         self.lws = torch.zeros(ft.decode_layer_workspace(T, k, H, I, E), dtype=torch.uint8, device=device)
@@ -283,7 +283,7 @@ class DecodeWorkload:
         self.ml = T * k
         self.ff = torch.empty((L, self.ml), dtype=torch.int32, device=device)
         self.fs = torch.empty((L, self.ml), dtype=torch.int32, device=device)
-        self.rws = torch.zeros(ft.route_workspace(T, E), dtype=torch.uint8, device=device)
+        self.rws = torch.zeros(ft.route_workspace(T, E, H), dtype=torch.uint8, device=device)
         self.ews = torch.zeros(ft.experts_workspace(ft.FT_DECODE, T, k, H, I, E), dtype=torch.uint8,
                                device=device)
         self.lws = torch.zeros(ft.decode_layer_workspace(T, k, H, I, E), dtype=torch.uint8, device=device)
@@ -810,7 +810,7 @@ def prefill_bench(T: int, steps: int, warmup: int, device, log=print, state=None
                          .view(np.int16)).to(device)
     ids = torch.empty((T, k), dtype=torch.int32, device=device)
     w = torch.empty((T, k), dtype=torch.float32, device=device)
-    rws = torch.zeros(ft.route_workspace(T, E), dtype=torch.uint8, device=device)
+    rws = torch.zeros(ft.route_workspace(T, E, H), dtype=torch.uint8, device=device)
     perm = torch.empty(n, dtype=torch.int32, device=device)
     inv = torch.empty((T, k), dtype=torch.int32, device=device)
     off = torch.empty(E + 1, dtype=torch.int32, device=device)
@@ -1007,7 +1007,7 @@ def kernel_case(name: str, T: int):
         ff = torch.empty(T * k, dtype=torch.int32, device=dev)
         fs = torch.empty(T * k, dtype=torch.int32, device=dev)
         out = torch.empty((T, H), dtype=torch.int16, device=dev)
-        rws = torch.zeros(ft.route_workspace(T, E), dtype=torch.uint8, device=dev)
+        rws = torch.zeros(ft.route_workspace(T, E, H), dtype=torch.uint8, device=dev)
         ews = torch.zeros(ft.experts_workspace(ft.FT_DECODE, T, k, H, I, E), dtype=torch.uint8, device=dev)
         lws = torch.zeros(ft.decode_layer_workspace(T, k, H, I, E), dtype=torch.uint8, device=dev)
         gen = torch.Generator(device=dev)
@@ -1072,7 +1072,7 @@ def kernel_case(name: str, T: int):
         n = Tp * k
         ids = torch.empty((Tp, k), dtype=torch.int32, device=dev)
         w = torch.empty((Tp, k), dtype=torch.float32, device=dev)
-        rws = torch.zeros(ft.route_workspace(Tp, E), dtype=torch.uint8, device=dev)
+        rws = torch.zeros(ft.route_workspace(Tp, E, H), dtype=torch.uint8, device=dev)
         perm = torch.empty(n, dtype=torch.int32, device=dev)
         inv = torch.empty((Tp, k), dtype=torch.int32, device=dev)
         off = torch.empty(E + 1, dtype=torch.int32, device=dev)
@@ -1358,7 +1358,7 @@ def reshape_workload(wl, T, n_steps):
     wl.ml = T * k
     wl.ff = torch.empty((L, wl.ml), dtype=torch.int32, device=dev)
     wl.fs = torch.empty((L, wl.ml), dtype=torch.int32, device=dev)
-    wl.rws = torch.zeros(ft.route_workspace(T, E), dtype=torch.uint8, device=dev)
+    wl.rws = torch.zeros(ft.route_workspace(T, E, H), dtype=torch.uint8, device=dev)
     wl.ews = torch.zeros(ft.experts_workspace(ft.FT_DECODE, T, k, H, cfg.I, E), dtype=torch.uint8, device=dev)
     wl.lws = torch.zeros(ft.decode_layer_workspace(T, k, H, cfg.I, E), dtype=torch.uint8, device=dev)
     return wl

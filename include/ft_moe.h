@@ -159,16 +159,20 @@ FT_API ft_status ft_moe_get_status(const int32_t* dev_status, int32_t* out_host)
  *   ties to the lower id; topk_w = p at those ids (divided by their sum when
  *   renorm != 0).
  * x [T,H] bf16 row-major; w_router [E,H] fp32 row-major; topk_ids [T,k]
- * int32; topk_w [T,k] fp32.  ws: device scratch of ft_moe_route_workspace(T,E)
+ * int32; topk_w [T,k] fp32.  ws: device scratch of ft_moe_route_workspace(T,E,H)
  * bytes: an arrival counter in its first 256 bytes (T <= 16, where one
- * kernel computes the logits and its last CTA the top-k), then the logits.
+ * kernel computes the logits and its last CTA the top-k), then the logits,
+ * then (T > 16, E a multiple of 128, H of 64: the logits on the tcgen05
+ * tensor cores, summed over hidden slices of at most 1024) w_router split
+ * exactly into three bf16 terms and the partial logits of every slice after
+ * the first.
  * The counter sits at the same place for every T, so one workspace sized for
  * the largest T serves calls of any smaller T; ws must be zero-filled before
  * the first call that uses it, every call leaves the counter at zero, and
  * calls that may overlap on the GPU need separate workspaces.  Limits:
  * 1 <= k <= min(E, 32), E <= 4096, H % 8 == 0.  T == 0 is a no-op.
  */
-FT_API size_t ft_moe_route_workspace(int32_t T, int32_t E);
+FT_API size_t ft_moe_route_workspace(int32_t T, int32_t E, int32_t H);
 FT_API ft_status ft_moe_route(const uint16_t* x, int32_t T, int32_t H, const float* w_router,
                        int32_t E, int32_t k, int32_t renorm, int32_t* topk_ids, float* topk_w,
                        void* ws, size_t ws_bytes, void* stream);

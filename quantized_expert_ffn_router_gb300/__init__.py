@@ -50,7 +50,7 @@ _SIGS = {
     "ft_last_error": (ctypes.c_char_p, []),
     "ft_block_bytes": (_U64, [_I32, _I32, _I32, _I32, _V]),
     "ft_moe_get_status": (_I32, [_V, _V]),
-    "ft_moe_route_workspace": (_SZ, [_I32, _I32]),
+    "ft_moe_route_workspace": (_SZ, [_I32, _I32, _I32]),
     "ft_moe_route": (_I32, [_V, _I32, _I32, _V, _I32, _I32, _I32, _V, _V, _V, _SZ, _V]),
     "ft_moe_split_q16": (_I32, [_V, _I32, _I32, _V, _V]),
     "ft_moe_resolve_slots": (_I32, [_V, _I32, _V, _I32, _I32, _I32, _V, _V, _V, _V, _I32, _V, _V]),
@@ -166,8 +166,8 @@ class DeviceCacheState:
 
 
 # ------------------------------------------------------------------ entries
-def route_workspace(T: int, E: int) -> int:
-    return int(load().ft_moe_route_workspace(T, E))
+def route_workspace(T: int, E: int, H: int) -> int:
+    return int(load().ft_moe_route_workspace(T, E, H))
 
 
 def route(x, w_router, k: int, topk_ids, topk_w, ws, renorm: bool = False, stream=None):

@@ -32,6 +32,15 @@ inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s
 // (opt-in), each looked up once per device.
 int device_sm_count();
 int device_smem_optin();
+// The router logits of long prompts on the tensor cores (route_mma.cu): the
+// shapes it takes, the workspace its split router terms and partial logits
+// need, the launch (partial logits per hidden slice; *slices of them).
+bool route_mma_fits(int T, int E, int H);
+size_t route_mma_split_bytes(int T, int E, int H);
+float* route_mma_partials(void* extra, int E, int H);
+ft_status route_mma_logits(const uint16_t* x, int T, int H, const float* W, int E, float* logits, void* extra,
+                           int* slices, cudaStream_t s);
+
 // Raise a kernel's dynamic shared memory limit to `bytes` on the current
 // device, once per (kernel, device); FT_ERR_CUDA if the device refuses.
 ft_status ensure_dyn_smem(const void* kernel, int bytes, const char* what);

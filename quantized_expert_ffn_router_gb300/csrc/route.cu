@@ -204,17 +204,33 @@ __global__ void __launch_bounds__(256) route_tiled_kernel(const uint16_t* __rest
   }
 }
 
-__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T,
+// One warp per token.  With nx > 0 the logits come in 1 + nx partial sums
+// (logits, then partx's [nx][T][E]); the warp adds them in slice order over
+// its own row of `logits` (no other warp reads or writes that row) before the
+// top-k reads it back.
+__global__ void __launch_bounds__(256) route_topk_kernel(float* __restrict__ logits, int T,
                                                          int E, int k, int renorm,
                                                          int32_t* __restrict__ ids,
-                                                         float* __restrict__ wts) {
+                                                         float* __restrict__ wts,
+                                                         const float* __restrict__ partx, int nx) {
   extern __shared__ float lsm[];  // [warps][E]
   pdl_wait();
-  const int warp = threadIdx.x >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + warp;
   if (t >= T) return;
-  topk_any(logits + static_cast<size_t>(t) * E, lsm + static_cast<size_t>(warp) * E, E, k, renorm,
-           ids + static_cast<size_t>(t) * k, wts + static_cast<size_t>(t) * k);
+  float* row = logits + static_cast<size_t>(t) * E;
+  if (nx > 0) {
+    const size_t plane = static_cast<size_t>(T) * E;
+    const float* px = partx + static_cast<size_t>(t) * E;
+    for (int e = lane; e < E; e += 32) {
+      float v = row[e];
+      for (int z = 0; z < nx; ++z) v += px[z * plane + e];
+      row[e] = v;
+    }
+    __syncwarp();  // the row's sums, written by every lane, before any lane reads them
+  }
+  topk_any(row, lsm + static_cast<size_t>(warp) * E, E, k, renorm, ids + static_cast<size_t>(t) * k,
+           wts + static_cast<size_t>(t) * k);
 }
 
 
@@ -258,9 +274,11 @@ ft_status launch_rows(const uint16_t* x, int T, int H, const float* W, int E, in
 
 extern "C" {
 
-size_t ft_moe_route_workspace(int32_t T, int32_t E) {
-  if (T <= 0 || E <= 0) return 0;
-  return ft::kRouteCounterBytes + ft::route_logits_bytes(T, E);  // the arrival counter, then the logits
+size_t ft_moe_route_workspace(int32_t T, int32_t E, int32_t H) {
+  if (T <= 0 || E <= 0 || H <= 0) return 0;
+  // the arrival counter, the logits, then (long prompts on the tensor cores)
+  // the router's three bf16 terms
+  return ft::kRouteCounterBytes + ft::route_logits_bytes(T, E) + ft::route_mma_split_bytes(T, E, H);
 }
 
 ft_status ft_moe_route(const uint16_t* x, int32_t T, int32_t H, const float* w_router, int32_t E,
@@ -272,24 +290,32 @@ ft_status ft_moe_route(const uint16_t* x, int32_t T, int32_t H, const float* w_r
   FT_REQUIRE(H >= 8 && H % 8 == 0, "route: H %d must be a positive multiple of 8", H);
   if (T == 0) return FT_OK;
   FT_REQUIRE(x && w_router && topk_ids && topk_w && ws, "route: NULL pointer");
-  FT_REQUIRE(ws_bytes >= ft_moe_route_workspace(T, E), "route: workspace %zu < %zu", ws_bytes,
-             ft_moe_route_workspace(T, E));
+  FT_REQUIRE(ws_bytes >= ft_moe_route_workspace(T, E, H), "route: workspace %zu < %zu", ws_bytes,
+             ft_moe_route_workspace(T, E, H));
   FT_REQUIRE(reinterpret_cast<uintptr_t>(x) % 16 == 0 && reinterpret_cast<uintptr_t>(w_router) % 16 == 0,
              "route: x and w_router must be 16-byte aligned");
   cudaStream_t s = ft::as_stream(stream);
   float* logits = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + ft::kRouteCounterBytes);
   if (T <= ft::kGemvMaxT)  // logits and top-k in one kernel
     return ft::launch_rows(x, T, H, w_router, E, k, renorm, topk_ids, topk_w, ws, s);
-  {
+  ft_status st;
+  int slices = 1;
+  float* partx = nullptr;
+  if (ft::route_mma_fits(T, E, H)) {  // tensor cores: the split terms and partial logits follow the logits
+    void* extra = static_cast<uint8_t*>(ws) + ft::kRouteCounterBytes + ft::route_logits_bytes(T, E);
+    st = ft::route_mma_logits(x, T, H, w_router, E, logits, extra, &slices, s);
+    partx = ft::route_mma_partials(extra, E, H);
+  } else {
     FT_REQUIRE(H % ft::kTK == 0, "route: H %d must be a multiple of 32 for T > 16", H);
     dim3 grid((E + ft::kTN - 1) / ft::kTN, (T + ft::kTM - 1) / ft::kTM);
     ft::route_tiled_kernel<<<grid, 256, 0, s>>>(x, T, H, w_router, E, logits);
+    st = ft::launch_check("route logits");
   }
-  ft_status st = ft::launch_check("route logits");
   if (st != FT_OK) return st;
   // the top-k grid starts while the logits grid drains (programmatic launch)
   // one warp per token, each with E logits in shared memory (<= 32 KB per CTA)
   const int warps = E <= 1024 ? 8 : 2;
+  const int nx = slices - 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((T + warps - 1) / warps);
   cfg.blockDim = dim3(32 * warps);
@@ -300,8 +326,8 @@ ft_status ft_moe_route(const uint16_t* x, int32_t T, int32_t H, const float* w_r
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const float* lg = logits;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, ft::route_topk_kernel, lg, T, E, k, renorm, topk_ids, topk_w);
+  const float* px = partx;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, ft::route_topk_kernel, logits, T, E, k, renorm, topk_ids, topk_w, px, nx);
   if (e != cudaSuccess) return ft::fail(FT_ERR_CUDA, "route topk: %s", cudaGetErrorString(e));
   return ft::launch_check("route topk");
 }

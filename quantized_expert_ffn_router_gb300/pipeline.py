@@ -84,7 +84,7 @@ class DecodeLayer:
         self.num_fetch = torch.zeros(1, **i32)
         self.fetch_fid = torch.empty(ml, **i32)
         self.fetch_slot = torch.empty(ml, **i32)
-        self.route_ws = torch.zeros(route_workspace(T, E), dtype=torch.uint8, device=device)
+        self.route_ws = torch.zeros(route_workspace(T, E, H), dtype=torch.uint8, device=device)
         wsb = experts_workspace(FT_DECODE, T, k, H, I, E)
         self.ws = torch.zeros(wsb, dtype=torch.uint8, device=device)
         self.ws_host = torch.zeros(wsb, dtype=torch.uint8, device=device)
@@ -156,7 +156,7 @@ class SpeculativeDecode:
         i32 = dict(dtype=torch.int32, device=device)
         self.pred_ids = torch.empty((T, k), **i32)
         self.pred_w = torch.empty((T, k), dtype=torch.float32, device=device)
-        self.pred_ws = torch.zeros(route_workspace(T, E), dtype=torch.uint8, device=device)
+        self.pred_ws = torch.zeros(route_workspace(T, E, cache.H), dtype=torch.uint8, device=device)
         self.pf_num = torch.zeros(1, **i32)
         self.pf_fid = torch.empty(ml, **i32)
         self.pf_slot = torch.empty(ml, **i32)
@@ -307,7 +307,7 @@ class PrefillLayers:
         self.slot_of = [torch.arange(b * E, (b + 1) * E, **i32) for b in range(self.n_buf)]
         self.ids = torch.empty((T, k), **i32)
         self.w = torch.empty((T, k), dtype=torch.float32, device=device)
-        self.route_ws = torch.zeros(route_workspace(T, E), dtype=torch.uint8, device=device)
+        self.route_ws = torch.zeros(route_workspace(T, E, H), dtype=torch.uint8, device=device)
         self.perm = torch.empty(n, **i32)
         self.inv = torch.empty((T, k), **i32)
         self.offsets = torch.empty(E + 1, **i32)

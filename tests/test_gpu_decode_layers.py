@@ -73,7 +73,7 @@ class _Layer:
         self.ft = ft
         self.ids, self.w, self.sl = _i32(T, k), torch.empty((T, k), device=DEV), _i32(T, k)
         self.nf, self.ff, self.fs = torch.zeros(1, dtype=torch.int32, device=DEV), _i32(ml), _i32(ml)
-        self.rws = torch.zeros(ft.route_workspace(T, E), dtype=torch.uint8, device=DEV)
+        self.rws = torch.zeros(ft.route_workspace(T, E, H), dtype=torch.uint8, device=DEV)
         self.ews = torch.zeros(ft.experts_workspace(ft.FT_DECODE, T, k, H, I, E), dtype=torch.uint8, device=DEV)
         self.status = torch.zeros(1, dtype=torch.int32, device=DEV)
 

@@ -110,7 +110,7 @@ def test_prefill_double_buffer_matches_resident_layers(cuda_lib, extra_slots):
     n = T * k
     i32 = dict(dtype=torch.int32, device=DEV)
     ids, w = torch.empty((T, k), **i32), torch.empty((T, k), dtype=torch.float32, device=DEV)
-    rws = torch.zeros(ft.route_workspace(T, E), dtype=torch.uint8, device=DEV)
+    rws = torch.zeros(ft.route_workspace(T, E, H), dtype=torch.uint8, device=DEV)
     perm, inv, off = torch.empty(n, **i32), torch.empty((T, k), **i32), torch.empty(E + 1, **i32)
     xp, xsc = torch.empty((n, H), dtype=torch.int16, device=DEV), torch.empty(n, dtype=torch.float32, device=DEV)
     pws = torch.empty(ft.permute_workspace(T, k, E), dtype=torch.uint8, device=DEV)

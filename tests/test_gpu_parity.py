@@ -39,7 +39,7 @@ def test_split_q16_exhaustive(cuda_lib):
 
 # ------------------------------------------------------------------- route
 @pytest.mark.parametrize("name,T", [("tiny", 8), ("d35b", 1), ("d35b", 8), ("flash", 1), ("flash", 3),
-                                    ("prefill", 37)])
+                                    ("prefill", 37), ("d35b", 129), ("flash", 200), ("tiny", 40)])
 def test_route_parity(cuda_lib, name, T):
     ft = cuda_lib
     cfg = synth.get_config(name)
@@ -50,7 +50,7 @@ def test_route_parity(cuda_lib, name, T):
     ids_o, w_o = oracle.route(x, W, cfg.k)
     # one workspace for every call: T <= 16 keeps an arrival counter in the
     # workspace's first 256 bytes, which each call must leave at zero
-    ws = torch.zeros(ft.route_workspace(T, cfg.E), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(ft.route_workspace(T, cfg.E, cfg.H), dtype=torch.uint8, device=DEV)
     for renorm in (False, True, False):
         ids = torch.empty((T, cfg.k), dtype=torch.int32, device=DEV)
         w = torch.empty((T, cfg.k), dtype=torch.float32, device=DEV)
@@ -69,7 +69,7 @@ def test_route_workspace_shared_across_token_counts(cuda_lib):
     ft = cuda_lib
     cfg = synth.get_config("d35b")
     W = synth.router_weights(cfg.seed, 5, cfg.E, cfg.H, cfg.router_std, zipf_bias=cfg.zipf)
-    ws = torch.zeros(ft.route_workspace(40, cfg.E), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(ft.route_workspace(40, cfg.E, cfg.H), dtype=torch.uint8, device=DEV)
     for T in (8, 1, 16, 40, 1, 3, 8):
         x, _ = gapped_tokens(cfg.seed, f"route-ws-{T}", T, cfg.H, W, cfg.k, cfg.gap, bias_feature=True)
         ids_o, w_o = oracle.route(x, W, cfg.k)
@@ -93,7 +93,7 @@ def test_route_prefill_full_size_sampled(cuda_lib):
         x = synth.normal_bf16(synth.stream_key(cfg.seed, "prefill-x", T), (T, cfg.H))
         ids = torch.empty((T, cfg.k), dtype=torch.int32, device=DEV)
         w = torch.empty((T, cfg.k), dtype=torch.float32, device=DEV)
-        ws = torch.zeros(ft.route_workspace(T, cfg.E), dtype=torch.uint8, device=DEV)
+        ws = torch.zeros(ft.route_workspace(T, cfg.E, cfg.H), dtype=torch.uint8, device=DEV)
         ft.route(_t(x), _t(W), cfg.k, ids, w, ws)
         torch.cuda.synchronize()
         rows = np.random.default_rng(T).choice(T, 96, replace=False)

@@ -132,7 +132,7 @@ def test_prefill_full_layer_sampled(cuda_lib, T):
     x = synth.normal_bf16(synth.stream_key(cfg.seed, "prefill-x", T), (T, H))
     ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
     w = torch.empty((T, k), dtype=torch.float32, device=DEV)
-    rws = torch.zeros(ft.route_workspace(T, E), dtype=torch.uint8, device=DEV)
+    rws = torch.zeros(ft.route_workspace(T, E, H), dtype=torch.uint8, device=DEV)
     ft.route(_t(x), _t(W), k, ids, w, rws)
     torch.cuda.synchronize()
     ids_np = ids.cpu().numpy()
