@@ -821,46 +821,57 @@ def prefill_bench(T: int, steps: int, warmup: int, device, log=print, state=None
     ews = torch.empty(ft.experts_workspace(ft.FT_PREFILL, T, k, H, I, E), dtype=torch.uint8, device=device)
     out = torch.empty((T, H), dtype=torch.int16, device=device)
     status = torch.zeros(1, dtype=torch.int32, device=device)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
 
     def layer(timed):
+        # events between the ops (timed) break their programmatic overlap: the
+        # layer time comes from the loop without them
         if timed:
             ev[0].record()
         ft.route(x, state["W"], k, ids, w, rws)
-        ft.permute(ids, E, x, perm, inv, off, xp, pws, dev_status=status, xp_scale=xs)
         if timed:
             ev[1].record()
+        ft.permute(ids, E, x, perm, inv, off, xp, pws, dev_status=status, xp_scale=xs)
+        if timed:
+            ev[2].record()
         ft.experts_fwd(state["cb"], None, 0, E, xp, T, k, state["slot"], None, None, yp, ews,
                        mode=ft.FT_PREFILL, offsets=off, dev_status=status, x_scale=xs)
         if timed:
-            ev[2].record()
+            ev[3].record()
         ft.combine(yp, inv, w, out)
+        if timed:
+            ev[4].record()
 
     for _ in range(warmup):
         layer(False)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    gemm_ms = []
     e0.record()
     for _ in range(steps):
-        layer(True)
+        layer(False)
     e1.record()
     torch.cuda.synchronize()
-    # the experts interval of each step (events also sit on the stream)
     layer_ms = e0.elapsed_time(e1) / steps
+    # each op's interval, one step at a time
+    per_op = {"route": [], "permute": [], "grouped_gemm": [], "combine": []}
     for _ in range(steps):
         layer(True)
         torch.cuda.synchronize()
-        gemm_ms.append(ev[1].elapsed_time(ev[2]))
+        for i, name in enumerate(per_op):
+            per_op[name].append(ev[i].elapsed_time(ev[i + 1]))
     if ft.get_status(status) != 0:
         raise RuntimeError(f"device status {ft.get_status(status)} in prefill")
     flops = 6.0 * H * I * T * k
-    gm = statistics.median(gemm_ms)
+    gm = statistics.median(per_op["grouped_gemm"])
     res = {"T": T, "layer_ms": layer_ms, "layer_tokens_per_s": T / (layer_ms * 1e-3),
            "grouped_gemm_ms": gm, "grouped_gemm_tflops": flops / (gm * 1e-3) / 1e12,
-           "weight_bytes": int(state["bank"].numel()), "flops": flops}
-    log(f"prefill T={T}: layer {layer_ms:.3f} ms, grouped GEMM {gm:.3f} ms = {res['grouped_gemm_tflops']:.0f} TFLOP/s")
+           "weight_bytes": int(state["bank"].numel()), "flops": flops,
+           "per_op_ms": {name: statistics.median(v) for name, v in per_op.items()},
+           "per_op_timing": "events around each op, one step at a time (median); the layer time has no events inside"}
+    po = res["per_op_ms"]
+    log(f"prefill T={T}: layer {layer_ms:.3f} ms, grouped GEMM {gm:.3f} ms = {res['grouped_gemm_tflops']:.0f} TFLOP/s; "
+        f"route {po['route']:.3f}, permute {po['permute']:.3f}, combine {po['combine']:.3f} ms")
     return res, state
 
 

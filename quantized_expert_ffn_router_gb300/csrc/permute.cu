@@ -153,6 +153,55 @@ __global__ void __launch_bounds__(256) gather_f16_kernel(const uint16_t* __restr
   }
 }
 
+// The same gather, one warp per token: the row (H = 256 VPL) is read once
+// into registers, its prescale taken once, and written to the k positions
+// inv[t, j] of the token's valid pairs.
+template <int VPL>
+__global__ void __launch_bounds__(128) gather_f16_tok_kernel(const uint16_t* __restrict__ x, int T, int k,
+                                                             int E, const int32_t* __restrict__ ids,
+                                                             const int32_t* __restrict__ inv,
+                                                             uint16_t* __restrict__ xp,
+                                                             float* __restrict__ xp_scale) {
+  const int lane = threadIdx.x & 31;
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (t >= T) return;
+  constexpr int H = 256 * VPL;
+  const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
+  uint4 v[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) v[i] = __ldg(src + lane + 32 * i);
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16_lo(v[i].x)), fabsf(bf16_hi(v[i].x))),
+                       fmaxf(fabsf(bf16_lo(v[i].y)), fabsf(bf16_hi(v[i].y)))));
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16_lo(v[i].z)), fabsf(bf16_hi(v[i].z))),
+                       fmaxf(fabsf(bf16_lo(v[i].w)), fabsf(bf16_hi(v[i].w)))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const float f = f16_prescale(m);
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    uint4 o;
+    o.x = __halves2half2_bits(bf16_lo(v[i].x) * f, bf16_hi(v[i].x) * f);
+    o.y = __halves2half2_bits(bf16_lo(v[i].y) * f, bf16_hi(v[i].y) * f);
+    o.z = __halves2half2_bits(bf16_lo(v[i].z) * f, bf16_hi(v[i].z) * f);
+    o.w = __halves2half2_bits(bf16_lo(v[i].w) * f, bf16_hi(v[i].w) * f);
+    v[i] = o;
+  }
+  for (int j = 0; j < k; ++j) {
+    const size_t p = static_cast<size_t>(t) * k + j;
+    const int e = __ldg(ids + p);
+    if (e < 0 || e >= E) continue;  // no position (the count kernel recorded FT_ERR_BAD_ID)
+    const int pos = __ldg(inv + p);
+    uint4* dst = reinterpret_cast<uint4*>(xp + static_cast<size_t>(pos) * H);
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) dst[lane + 32 * i] = v[i];
+    if (lane == 0) xp_scale[pos] = 1.f / f;
+  }
+}
+
 // out[t] = host_partial[t] + sum_j w[t,j] * yp[inv[t,j]] (j order, fp32), bf16.
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ yp,
                                                       const int32_t* __restrict__ inv,
@@ -267,8 +316,22 @@ ft_status ft_moe_permute(const int32_t* topk_ids, int32_t T, int32_t k, int32_t 
     if (xp_format == FT_XP_BF16) {
       ft::gather_kernel<<<grid, 256, 0, s>>>(x, H, k, perm, n, xp);
     } else {
-      const int g2 = std::min((n + 7) / 8, ft::sms() * 16);
-      ft::gather_f16_kernel<<<g2, 256, 0, s>>>(x, H, k, perm, n, xp, xp_scale);
+      // one warp per token (rows of up to 4096 in registers), else one per pair
+      const unsigned gt = static_cast<unsigned>((T + 3) / 4);
+      switch (H % 256 == 0 ? H / 256 : 0) {
+#define FT_GATHER_TOK(V) \
+  case V:                \
+    ft::gather_f16_tok_kernel<V><<<gt, 128, 0, s>>>(x, T, k, E, topk_ids, inv, xp, xp_scale); \
+    break;
+        FT_GATHER_TOK(1) FT_GATHER_TOK(2) FT_GATHER_TOK(3) FT_GATHER_TOK(4) FT_GATHER_TOK(5) FT_GATHER_TOK(6)
+        FT_GATHER_TOK(7) FT_GATHER_TOK(8) FT_GATHER_TOK(9) FT_GATHER_TOK(10) FT_GATHER_TOK(11)
+        FT_GATHER_TOK(12) FT_GATHER_TOK(13) FT_GATHER_TOK(14) FT_GATHER_TOK(15) FT_GATHER_TOK(16)
+#undef FT_GATHER_TOK
+        default: {
+          const int g2 = std::min((n + 7) / 8, ft::sms() * 16);
+          ft::gather_f16_kernel<<<g2, 256, 0, s>>>(x, H, k, perm, n, xp, xp_scale);
+        }
+      }
     }
     if ((st = ft::launch_check("permute gather")) != FT_OK) return st;
   }

@@ -63,11 +63,12 @@ def _oracle_rows(bank_np_by_e, H, I, E, layer, x, perm, k, offsets, rows, ts_np)
     return out
 
 
-def test_permute_f16_gather_is_exact():
+@pytest.mark.parametrize("H", [256, 768, 4096, 264])  # one warp per token (rows in registers); 264: per pair
+def test_permute_f16_gather_is_exact(H):
     import quantized_expert_ffn_router_gb300 as ft
 
     ft.load()
-    T, k, E, H = 64, 3, 8, 256
+    T, k, E = 64, 3, 8
     rng = np.random.default_rng(3)
     ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
     xf = rng.standard_normal((T, H)).astype(np.float32)
