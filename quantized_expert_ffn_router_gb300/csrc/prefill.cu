@@ -23,6 +23,16 @@
 //      per row (x_scale undoes it), and for down the f16 h written by the
 //      gate/up epilogue with a fixed 2^-4 prescale.
 //
+// Stages.  With few tokens per expert (a launch whose mean segment is at
+// most 96 rows: MRG) each stage of the A ring also holds that k-step's token
+// tile, which the TMA completes on the same barrier the converters arrive
+// on, so an MMA issuer waits and commits once per k-step instead of twice.
+// On GB300 an mbarrier poll costs the issuing thread ~200-340 cycles even
+// when the phase has completed, against ~130-190 per MMA: at N ~ 48 the
+// issuer's loop, not the tensor pipe, sets the pace.  Longer segments keep a
+// separate, deeper token ring, which hides the ~1 us that their larger token
+// tiles take to arrive from L2.
+//
 // Roles (640 threads).  Warp 0 lane 0 streams the weights by TMA: E2M1 codes
 // in 64-byte-wide boxes (two k-steps, 64-byte swizzle) and E4M3 scales (four
 // k-steps per stage).  Warp 2 lane 0 streams the B tiles (tokens), with as
@@ -55,6 +65,7 @@ constexpr int kBRows = 64;      // rows per B TMA box
 constexpr int kBBytes = 64 * 1024;     // the B (tokens) ring for <= 128 tokens: 4 .. 8 stages
 constexpr int kBBytesBig = 96 * 1024;  // ... for more: 3 stages of 256 rows, 4 of 192
 constexpr int kBMaxStages = 8;
+constexpr int kMrgMeanRows = 96;  // launches with T k <= 96 E put token tiles in the A stages
 constexpr int kConvWarps = 16;  // four per SM sub-partition, in two groups of eight
 constexpr int kPfThreads = 128 + 32 * kConvWarps;  // + TMA x2, MMA issuer x2
 constexpr float kHScale = 0.0625f;  // h is stored as f16(h * 2^-4)
@@ -82,6 +93,9 @@ struct PfSmem {
   static constexpr int sc_stage = NMAT * kScTile;
   static constexpr int tail = kRawStages * raw_stage + kScStages * sc_stage;  // raw + scale rings
   static constexpr int total = kAStages * NMAT * kATile + kBBytes + tail;
+  static constexpr int kABBudget = total - tail;  // A and token rings
+  static constexpr int kAStagesMrg = NMAT == 2 ? 4 : 6;  // A + token stages, at most
+  static constexpr int kAStagesMax = kAStagesMrg > kAStages ? kAStagesMrg : kAStages;
   static_assert(kAStagesBig * NMAT * kATile + kBBytesBig + tail <= total, "big-N layout must fit");
 };
 
@@ -208,7 +222,8 @@ __device__ __forceinline__ void scales2(unsigned short two, uint32_t s2[2]) {
 
 // ---------------------------------------------------------------- kernel ---
 // NMAT = 2: gate/up (maps c0,c1 = codes, s0,s1 = scales); NMAT = 1: down.
-template <int NMAT>
+// MRG: token tiles inside the A stages (see "Stages" above).
+template <int NMAT, bool MRG>
 __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant__ CUtensorMap c0map,
                                                            const __grid_constant__ CUtensorMap c1map,
                                                            const __grid_constant__ CUtensorMap s0map,
@@ -216,7 +231,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
                                                            const __grid_constant__ CUtensorMap bmap,
                                                            PfArgs a) {
   using L = PfSmem<NMAT>;
-  constexpr int RS = L::kRawStages, SS = L::kScStages, AS_MAX = L::kAStages;
+  constexpr int RS = L::kRawStages, SS = L::kScStages, AS_MAX = L::kAStagesMax;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t raw_full[RS], raw_empty[RS];
@@ -248,12 +263,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
   const int nbox_max = (min(n_e, kNMax) + kBRows - 1) / kBRows;
   const int b_stage = nbox_max * kBBox;
   const bool big = nbox_max > 2;
-  const int AS = big ? L::kAStagesBig : L::kAStages;
+  // MRG: a stage is the A tiles then the token tile; otherwise the A ring
+  // and the token ring (NB stages of b_stage) are separate
+  const int a_stage = NMAT * kATile + (MRG ? b_stage : 0);
+  const int AS = MRG ? min(L::kAStagesMrg, L::kABBudget / a_stage) : big ? L::kAStagesBig : L::kAStages;
   const int b_bytes = big ? kBBytesBig : kBBytes;
-  const int NB = min(kBMaxStages, b_bytes / b_stage);
+  const int NB = MRG ? AS : min(kBMaxStages, b_bytes / b_stage);
   uint8_t* const a_base = smem;
-  uint8_t* const b_base = a_base + AS * NMAT * kATile;
-  uint8_t* const raw_base = b_base + b_bytes;
+  uint8_t* const b_base = MRG ? a_base + NMAT * kATile : a_base + AS * NMAT * kATile;
+  const int b_pitch = MRG ? a_stage : b_stage;  // bytes from one token stage to the next
+  uint8_t* const raw_base = a_base + L::kABBudget;
   uint8_t* const sc_base = raw_base + RS * L::raw_stage;
 
   if (tid == 0) {
@@ -266,13 +285,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
       mbar_init(&sc_empty[s], kConvWarps);
     }
     for (int s = 0; s < AS; ++s) {
-      mbar_init(&a_full[s], NMAT == 2 ? kConvWarps : kConvWarps / 2);
+      // the converter warps of a k-step (and with MRG the token producer)
+      mbar_init(&a_full[s], (NMAT == 2 ? kConvWarps : kConvWarps / 2) + (MRG ? 1 : 0));
       mbar_init(&a_empty[s], kIss);
     }
-    for (int s = 0; s < NB; ++s) {
-      mbar_init(&b_full[s], 1);
-      mbar_init(&b_empty[s], kIss);
-    }
+    if (!MRG)
+      for (int s = 0; s < NB; ++s) {
+        mbar_init(&b_full[s], 1);
+        mbar_init(&b_empty[s], kIss);
+      }
     mbar_init(&acc_full, 2);
     mbar_init(&acc_empty, kConvWarps);
     fence_barrier_init();
@@ -324,11 +345,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
         const int n_valid = min(kNMax, n_e - pass * kNMax);
         const int nbox = (n_valid + kBRows - 1) / kBRows;
         for (int kk = 0; kk < ksteps; ++kk) {
-          if (wrapped && !mbar_wait(&b_empty[bst], bph ^ 1u, a.dev_status)) goto done_b;
-          uint8_t* bt = b_base + bst * b_stage;
-          mbar_arrive_expect_tx(&b_full[bst], nbox * kBBox);
+          // MRG: the stage's release is the A stage's, its arrival counts on a_full
+          uint64_t* const bfull = MRG ? &a_full[bst] : &b_full[bst];
+          if (wrapped && !mbar_wait(MRG ? &a_empty[bst] : &b_empty[bst], bph ^ 1u, a.dev_status)) goto done_b;
+          uint8_t* bt = b_base + bst * b_pitch;
+          mbar_arrive_expect_tx(bfull, nbox * kBBox);
           for (int bx = 0; bx < nbox; ++bx)
-            tma_load_2d(bt + bx * kBBox, &bmap, kk * kBK, row_lo + pass * kNMax + bx * kBRows, &b_full[bst]);
+            tma_load_2d(bt + bx * kBBox, &bmap, kk * kBK, row_lo + pass * kNMax + bx * kBRows, bfull);
           if (++bst == NB) {
             bst = 0;
             bph ^= 1u;
@@ -360,20 +383,21 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
         }
         for (int kk = 0; kk < ksteps; ++kk) {
           if (NMAT == 2 || (kk & 1) == iss) {
-            if (!mbar_wait(&a_full[ast], aph, a.dev_status) || !mbar_wait(&b_full[bst], bph, a.dev_status)) {
+            if (!mbar_wait(&a_full[ast], aph, a.dev_status) ||
+                (!MRG && !mbar_wait(&b_full[bst], bph, a.dev_status))) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint8_t* at = a_base + ast * NMAT * kATile + (NMAT == 2 ? iss * kATile : 0);
+            const uint8_t* at = a_base + ast * a_stage + (NMAT == 2 ? iss * kATile : 0);
             const uint64_t adesc = sw128_desc(at);
-            const uint64_t bdesc = sw128_desc(b_base + bst * b_stage);
+            const uint64_t bdesc = sw128_desc(b_base + bst * b_pitch);
             const uint32_t first = NMAT == 2 ? (kk == 0) : (kk == iss);
 #pragma unroll
             for (int j = 0; j < kBK / 16; ++j)
               mma_f16(tmem + iss * 256, adesc + 2 * j, bdesc + 2 * j, idesc, (first && j == 0) ? 0u : 1u);
             mma_commit(&a_empty[ast]);
-            mma_commit(&b_empty[bst]);
+            if (!MRG) mma_commit(&b_empty[bst]);
           }
           if (++ast == AS) {
             ast = 0;
@@ -438,7 +462,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
                 ok = false;
                 break;
               }
-              uint8_t* at = a_base + ast * NMAT * kATile + m * kATile + r * 128;
+              uint8_t* at = a_base + ast * a_stage + m * kATile + r * 128;
               const uint32_t sw = j4 == 0 ? sc.x : j4 == 1 ? sc.y : j4 == 2 ? sc.z : sc.w;
               uint32_t s2[2];
               scales2(static_cast<unsigned short>(hf ? sw >> 16 : sw & 0xffffu), s2);
@@ -607,10 +631,16 @@ ft_status experts_prefill(const ft_bank* cache, const ft_bank* pool, int32_t lay
             map_acts(&mh, hp, I, n_rows);
   if (!ok) return fail(FT_ERR_INVALID, "experts prefill: tensor map encoding rejected the bank or batch");
   {
-    ft_status sa = ensure_dyn_smem(reinterpret_cast<const void*>(pf_kernel<2>), PfSmem<2>::total + 1024,
+    ft_status sa = ensure_dyn_smem(reinterpret_cast<const void*>(pf_kernel<2, false>), PfSmem<2>::total + 1024,
                                    "experts prefill");
     if (sa == FT_OK)
-      sa = ensure_dyn_smem(reinterpret_cast<const void*>(pf_kernel<1>), PfSmem<1>::total + 1024,
+      sa = ensure_dyn_smem(reinterpret_cast<const void*>(pf_kernel<2, true>), PfSmem<2>::total + 1024,
+                           "experts prefill");
+    if (sa == FT_OK)
+      sa = ensure_dyn_smem(reinterpret_cast<const void*>(pf_kernel<1, false>), PfSmem<1>::total + 1024,
+                           "experts prefill");
+    if (sa == FT_OK)
+      sa = ensure_dyn_smem(reinterpret_cast<const void*>(pf_kernel<1, true>), PfSmem<1>::total + 1024,
                            "experts prefill");
     if (sa != FT_OK) return sa;
   }
@@ -628,7 +658,12 @@ ft_status experts_prefill(const ft_bank* cache, const ft_bank* pool, int32_t lay
   a.M = I;
   a.x_scale = x_scale;
   a.out = hp;
-  pf_kernel<2><<<dim3(I / kBM, E), kPfThreads, PfSmem<2>::total + 1024, s>>>(mg, mu, mgs, mus, mx, a);
+  // token tiles inside the A stages when the mean segment is short
+  const bool mrg = static_cast<int64_t>(T) * k <= static_cast<int64_t>(kMrgMeanRows) * E;
+  if (mrg)
+    pf_kernel<2, true><<<dim3(I / kBM, E), kPfThreads, PfSmem<2>::total + 1024, s>>>(mg, mu, mgs, mus, mx, a);
+  else
+    pf_kernel<2, false><<<dim3(I / kBM, E), kPfThreads, PfSmem<2>::total + 1024, s>>>(mg, mu, mgs, mus, mx, a);
   ft_status stt = launch_check("experts prefill gate/up");
   if (stt != FT_OK) return stt;
   // down: K = I, M = H, output Yp (bf16)
@@ -636,7 +671,10 @@ ft_status experts_prefill(const ft_bank* cache, const ft_bank* pool, int32_t lay
   a.M = H;
   a.x_scale = nullptr;
   a.out = yp;
-  pf_kernel<1><<<dim3(H / kBM, E), kPfThreads, PfSmem<1>::total + 1024, s>>>(md, md, mds, mds, mh, a);
+  if (mrg)
+    pf_kernel<1, true><<<dim3(H / kBM, E), kPfThreads, PfSmem<1>::total + 1024, s>>>(md, md, mds, mds, mh, a);
+  else
+    pf_kernel<1, false><<<dim3(H / kBM, E), kPfThreads, PfSmem<1>::total + 1024, s>>>(md, md, mds, mds, mh, a);
   return launch_check("experts prefill down");
 }
 
