@@ -47,22 +47,49 @@ __global__ void __launch_bounds__(kChunk) perm_count_kernel(const int32_t* __res
 }
 
 // Exclusive scan of counts[E][nchunks] (expert-major) into base[][], and the
-// expert segment offsets.  One CTA; each thread owns a contiguous run.
+// expert segment offsets.  One CTA; warp w owns a contiguous segment of the
+// counts and reads it 32 consecutive counts at a time (coalesced): its total
+// first, then, after the warp totals' scan, a running warp-level inclusive
+// scan over the segment.
 __global__ void __launch_bounds__(1024) perm_scan_kernel(const int32_t* __restrict__ counts,
                                                          int E, int nchunks, int n,
                                                          int32_t* __restrict__ base,
                                                          int32_t* __restrict__ offsets) {
-  __shared__ int scratch[33];
+  __shared__ int wsum[32];
   const int N = E * nchunks;
-  const int per = (N + blockDim.x - 1) / blockDim.x;
-  const int lo = min(N, static_cast<int>(threadIdx.x) * per), hi = min(N, lo + per);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int seg = ((N + 32 * nw - 1) / (32 * nw)) * 32;  // a multiple of 32
+  const int lo = min(N, warp * seg), hi = min(N, lo + seg);
   int s = 0;
-  for (int i = lo; i < hi; ++i) s += counts[i];
-  int total;
-  int run = block_excl_scan(s, scratch, &total);
-  for (int i = lo; i < hi; ++i) {
-    base[i] = run;
-    run += counts[i];
+#pragma unroll 4
+  for (int i = lo + lane; i < hi; i += 32) s += counts[i];
+  s = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(s)));
+  if (lane == 0) wsum[warp] = s;
+  __syncthreads();
+  if (warp == 0) {
+    const int v = lane < nw ? wsum[lane] : 0;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane < nw) wsum[lane] = x - v;  // exclusive
+  }
+  __syncthreads();
+  int carry = wsum[warp];
+#pragma unroll 4
+  for (int i0 = lo; i0 < hi; i0 += 32) {
+    const int i = i0 + lane;
+    const int c = i < hi ? counts[i] : 0;
+    int x = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (i < hi) base[i] = carry + x - c;
+    carry += __shfl_sync(0xffffffffu, x, 31);
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) offsets[e] = base[static_cast<size_t>(e) * nchunks];

@@ -37,10 +37,10 @@
 // in 64-byte-wide boxes (two k-steps, 64-byte swizzle) and E4M3 scales (four
 // k-steps per stage).  Warp 2 lane 0 streams the B tiles (tokens), with as
 // many stages as the expert's token count leaves room for, so that neither
-// stream waits on the other.  Warps 1 and 3 (lane 0) issue the MMAs: one
-// thread issues a tcgen05.mma only every ~94 cycles whatever N is, so two
-// issuers share the work (gate / up; for down, even / odd k-steps into two
-// accumulators).  Warps 4..19, two groups of eight, dequantise into the
+// stream waits on the other.  Warps 1 and 3 (lane 0) issue the MMAs: an
+// issuing thread spends ~126 cycles per tcgen05.mma on fresh operands at any
+// N <= 128 (GB300), so two issuers share the work (gate / up; for down, even
+// / odd k-steps into two accumulators).  Warps 4..19, two groups of eight, dequantise into the
 // 128-byte-swizzled K-major A tiles (gate / up, or even / odd k-steps), half
 // a weight row per thread per k-step, and afterwards run the epilogue
 // (tcgen05.ld; the four warps of a TMEM lane quarter take every fourth

@@ -63,7 +63,7 @@ def _oracle_rows(bank_np_by_e, H, I, E, layer, x, perm, k, offsets, rows, ts_np)
     return out
 
 
-@pytest.mark.parametrize("H", [256, 768, 4096, 264])  # one warp per token (rows in registers); 264: per pair
+@pytest.mark.parametrize("H", [256, 768, 2048, 3072, 4096, 264])  # warp(s) per token; 264: per pair
 def test_permute_f16_gather_is_exact(H):
     import quantized_expert_ffn_router_gb300 as ft
 
