@@ -49,6 +49,8 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
+
 #include "ft_async.cuh"
 #include "ft_common.cuh"
 
@@ -103,12 +105,37 @@ struct PfArgs {
   const int32_t* offsets;  // [E+1]
   const int32_t* slot_of;  // [E] cache slot of each expert
   int E, K, M, n_rows, layer;
+  int tiles;               // 128-row weight tiles per expert (M / 128); work items = tiles * E
+  int pmax;                // tokens per pass: 128 (MRG launches) or 256
   int64_t n_blocks;
   const float* x_scale;    // [n_rows] (gate/up only)
   const float* tscale;     // [n_fids, 3]
   uint16_t* out;           // gate/up: Hp f16 [n_rows, M]; down: Yp bf16 [n_rows, M]
   int32_t* dev_status;
 };
+
+// Work item it = (expert e, row tile mt): its segment of the permuted batch
+// and its cache slot; run is false for an empty segment or an invalid entry
+// (recorded once, by the caller that passes report).
+struct PfItem {
+  int e, mt, row_lo, n_e, slot;
+  bool run;
+};
+
+__device__ __forceinline__ PfItem pf_item(const PfArgs& a, int it, bool report) {
+  PfItem I;
+  I.e = it / a.tiles;
+  I.mt = it - I.e * a.tiles;
+  I.row_lo = a.offsets[I.e];
+  I.n_e = a.offsets[I.e + 1] - I.row_lo;
+  I.slot = a.slot_of[I.e];
+  I.run = I.n_e > 0;
+  if (I.run && (I.slot < 0 || I.slot >= a.n_blocks || I.row_lo < 0 || I.row_lo + I.n_e > a.n_rows)) {
+    if (report) record_status(a.dev_status, I.slot < 0 ? FT_ERR_UNSUPPORTED : FT_ERR_BAD_ID);
+    I.run = false;
+  }
+  return I;
+}
 
 // ----------------------------------------------------------- PTX helpers ---
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
@@ -242,29 +269,19 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
   __shared__ uint32_t s_tmem;
 
   if (prior_timeout(a.dev_status)) return;
-  const int e = blockIdx.y, mt = blockIdx.x;
-  const int row_lo = a.offsets[e];
-  const int n_e = a.offsets[e + 1] - row_lo;
-  if (n_e <= 0) return;
-  const int slot = a.slot_of[e];
-  if (slot < 0 || slot >= a.n_blocks || row_lo < 0 || row_lo + n_e > a.n_rows) {
-    if (threadIdx.x == 0) record_status(a.dev_status, slot < 0 ? FT_ERR_UNSUPPORTED : FT_ERR_BAD_ID);
-    return;
-  }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ksteps = a.K / kBK;
-  const int rps = ksteps / kRawSteps;                  // code stages per pass
-  const int sps = ksteps / kScSteps;                   // scale stages per pass
-  const int n_pass = (n_e + kNMax - 1) / kNMax;
+  const int n_items = a.tiles * a.E;
+  const int pmax = a.pmax;  // tokens per pass (MMA N <= pmax)
   constexpr uint32_t kCols = 512;  // two accumulators of up to 256 columns
   constexpr int kIss = NMAT == 2 ? 2 : 1;  // MMA issuers that read each k-step's A and B
-  // the B ring: stages sized for this expert's widest pass; more than two
-  // boxes (128 tokens) take the big-N layout
-  const int nbox_max = (min(n_e, kNMax) + kBRows - 1) / kBRows;
+  // The ring geometry is fixed for the launch (the rings run on from one
+  // work item to the next): token stages of pmax / 64 boxes; more than two
+  // boxes take the big-N layout.  MRG: a stage is the A tiles then the token
+  // tile; otherwise the A ring and the token ring (NB stages) are separate.
+  const int nbox_max = pmax / kBRows;
   const int b_stage = nbox_max * kBBox;
   const bool big = nbox_max > 2;
-  // MRG: a stage is the A tiles then the token tile; otherwise the A ring
-  // and the token ring (NB stages of b_stage) are separate
   const int a_stage = NMAT * kATile + (MRG ? b_stage : 0);
   const int AS = MRG ? min(L::kAStagesMrg, L::kABBudget / a_stage) : big ? L::kAStagesBig : L::kAStages;
   const int b_bytes = big ? kBBytesBig : kBBytes;
@@ -309,27 +326,38 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
   tc_fence_after();
   const uint32_t tmem = s_tmem;
 
+  // Every role walks the same work items (row tile, expert) in the same
+  // order, it = blockIdx.x, + gridDim.x, ...; the ring positions and the
+  // accumulator's pass count carry over from one item to the next.
   if (warp == 0) {
     // -------------------------------------------------- TMA: weights ---
     if (lane == 0) {
       const CUtensorMap* cm[2] = {&c0map, &c1map};
       const CUtensorMap* sm[2] = {&s0map, &s1map};
-      for (int pass = 0; pass < n_pass; ++pass) {
-        for (int kk = 0; kk < ksteps; kk += kRawSteps) {
-          if (kk % kScSteps == 0) {
-            const int su = pass * sps + kk / kScSteps, sst = su % SS;
-            if (su >= SS && !mbar_wait(&sc_empty[sst], ((su / SS) - 1) & 1, a.dev_status)) goto done_w;
-            uint8_t* sc = sc_base + sst * L::sc_stage;
-            mbar_arrive_expect_tx(&sc_full[sst], NMAT * kScTile);
+      int su = 0, v = 0;  // scale and code stages issued so far
+      for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const PfItem I = pf_item(a, it, tid == 0);
+        if (!I.run) continue;
+        const int n_pass = (I.n_e + pmax - 1) / pmax;
+        for (int pass = 0; pass < n_pass; ++pass) {
+          for (int kk = 0; kk < ksteps; kk += kRawSteps) {
+            if (kk % kScSteps == 0) {
+              const int sst = su % SS;
+              if (su >= SS && !mbar_wait(&sc_empty[sst], ((su / SS) - 1) & 1, a.dev_status)) goto done_w;
+              uint8_t* sc = sc_base + sst * L::sc_stage;
+              mbar_arrive_expect_tx(&sc_full[sst], NMAT * kScTile);
+              for (int m = 0; m < NMAT; ++m)
+                tma_load_3d(sc + m * kScTile, sm[m], (kk / kScSteps) * 16, I.mt * kBM, I.slot, &sc_full[sst]);
+              ++su;
+            }
+            const int rst = v % RS;
+            if (v >= RS && !mbar_wait(&raw_empty[rst], ((v / RS) - 1) & 1, a.dev_status)) goto done_w;
+            uint8_t* raw = raw_base + rst * L::raw_stage;
+            mbar_arrive_expect_tx(&raw_full[rst], NMAT * kRawTile);
             for (int m = 0; m < NMAT; ++m)
-              tma_load_3d(sc + m * kScTile, sm[m], (kk / kScSteps) * 16, mt * kBM, slot, &sc_full[sst]);
+              tma_load_3d(raw + m * kRawTile, cm[m], (kk / kRawSteps) * 64, I.mt * kBM, I.slot, &raw_full[rst]);
+            ++v;
           }
-          const int v = pass * rps + kk / kRawSteps, rst = v % RS;
-          if (v >= RS && !mbar_wait(&raw_empty[rst], ((v / RS) - 1) & 1, a.dev_status)) goto done_w;
-          uint8_t* raw = raw_base + rst * L::raw_stage;
-          mbar_arrive_expect_tx(&raw_full[rst], NMAT * kRawTile);
-          for (int m = 0; m < NMAT; ++m)
-            tma_load_3d(raw + m * kRawTile, cm[m], (kk / kRawSteps) * 64, mt * kBM, slot, &raw_full[rst]);
         }
       }
     done_w:;
@@ -341,21 +369,26 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
       int bst = 0;
       uint32_t bph = 0;
       bool wrapped = false;
-      for (int pass = 0; pass < n_pass; ++pass) {
-        const int n_valid = min(kNMax, n_e - pass * kNMax);
-        const int nbox = (n_valid + kBRows - 1) / kBRows;
-        for (int kk = 0; kk < ksteps; ++kk) {
-          // MRG: the stage's release is the A stage's, its arrival counts on a_full
-          uint64_t* const bfull = MRG ? &a_full[bst] : &b_full[bst];
-          if (wrapped && !mbar_wait(MRG ? &a_empty[bst] : &b_empty[bst], bph ^ 1u, a.dev_status)) goto done_b;
-          uint8_t* bt = b_base + bst * b_pitch;
-          mbar_arrive_expect_tx(bfull, nbox * kBBox);
-          for (int bx = 0; bx < nbox; ++bx)
-            tma_load_2d(bt + bx * kBBox, &bmap, kk * kBK, row_lo + pass * kNMax + bx * kBRows, bfull);
-          if (++bst == NB) {
-            bst = 0;
-            bph ^= 1u;
-            wrapped = true;
+      for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const PfItem I = pf_item(a, it, false);
+        if (!I.run) continue;
+        const int n_pass = (I.n_e + pmax - 1) / pmax;
+        for (int pass = 0; pass < n_pass; ++pass) {
+          const int n_valid = min(pmax, I.n_e - pass * pmax);
+          const int nbox = (n_valid + kBRows - 1) / kBRows;
+          for (int kk = 0; kk < ksteps; ++kk) {
+            // MRG: the stage's release is the A stage's, its arrival counts on a_full
+            uint64_t* const bfull = MRG ? &a_full[bst] : &b_full[bst];
+            if (wrapped && !mbar_wait(MRG ? &a_empty[bst] : &b_empty[bst], bph ^ 1u, a.dev_status)) goto done_b;
+            uint8_t* bt = b_base + bst * b_pitch;
+            mbar_arrive_expect_tx(bfull, nbox * kBBox);
+            for (int bx = 0; bx < nbox; ++bx)
+              tma_load_2d(bt + bx * kBBox, &bmap, kk * kBK, I.row_lo + pass * pmax + bx * kBRows, bfull);
+            if (++bst == NB) {
+              bst = 0;
+              bph ^= 1u;
+              wrapped = true;
+            }
           }
         }
       }
@@ -363,52 +396,59 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
     }
   } else if (warp == 1 || warp == 3) {
     // ------------------------------------------------------------- MMA ---
-    // Two issuing threads: one thread issues a tcgen05.mma only every ~94
-    // cycles, whatever N is, so small token counts need two issuers to keep
-    // the tensor pipe busy.  gate/up: issuer i owns matrix i.  down: issuer i
-    // owns the k-steps kk % 2 == i, into accumulator i (summed in the
-    // epilogue).
+    // Two issuing threads: an issuing thread spends ~126 cycles per
+    // tcgen05.mma on fresh operands, whatever N is, so two issuers share the
+    // work.  gate/up: issuer i owns matrix i.  down: issuer i owns the
+    // k-steps kk % 2 == i, into accumulator i (summed in the epilogue).
     const int iss = warp == 1 ? 0 : 1;
     if (lane == 0) {
       bool ok = true;
-      int ast = 0, bst = 0;
+      int ast = 0, bst = 0, gp = 0;  // gp: passes issued so far (the accumulator's phase)
       uint32_t aph = 0, bph = 0;
-      for (int pass = 0; pass < n_pass && ok; ++pass) {
-        const int n_valid = min(kNMax, n_e - pass * kNMax);
-        const int n_mma = (n_valid + 15) & ~15;
-        const uint32_t idesc = idesc_f16(n_mma);
-        if (pass > 0) {
-          if (!mbar_wait(&acc_empty, (pass - 1) & 1, a.dev_status)) break;
-          tc_fence_after();
-        }
-        for (int kk = 0; kk < ksteps; ++kk) {
-          if (NMAT == 2 || (kk & 1) == iss) {
-            if (!mbar_wait(&a_full[ast], aph, a.dev_status) ||
-                (!MRG && !mbar_wait(&b_full[bst], bph, a.dev_status))) {
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        const PfItem I = pf_item(a, it, false);
+        if (!I.run) continue;
+        const int n_pass = (I.n_e + pmax - 1) / pmax;
+        for (int pass = 0; pass < n_pass && ok; ++pass, ++gp) {
+          const int n_valid = min(pmax, I.n_e - pass * pmax);
+          const int n_mma = (n_valid + 15) & ~15;
+          const uint32_t idesc = idesc_f16(n_mma);
+          if (gp > 0) {
+            if (!mbar_wait(&acc_empty, (gp - 1) & 1, a.dev_status)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint8_t* at = a_base + ast * a_stage + (NMAT == 2 ? iss * kATile : 0);
-            const uint64_t adesc = sw128_desc(at);
-            const uint64_t bdesc = sw128_desc(b_base + bst * b_pitch);
-            const uint32_t first = NMAT == 2 ? (kk == 0) : (kk == iss);
+          }
+          for (int kk = 0; kk < ksteps; ++kk) {
+            if (NMAT == 2 || (kk & 1) == iss) {
+              if (!mbar_wait(&a_full[ast], aph, a.dev_status) ||
+                  (!MRG && !mbar_wait(&b_full[bst], bph, a.dev_status))) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint8_t* at = a_base + ast * a_stage + (NMAT == 2 ? iss * kATile : 0);
+              const uint64_t adesc = sw128_desc(at);
+              const uint64_t bdesc = sw128_desc(b_base + bst * b_pitch);
+              const uint32_t first = NMAT == 2 ? (kk == 0) : (kk == iss);
 #pragma unroll
-            for (int j = 0; j < kBK / 16; ++j)
-              mma_f16(tmem + iss * 256, adesc + 2 * j, bdesc + 2 * j, idesc, (first && j == 0) ? 0u : 1u);
-            mma_commit(&a_empty[ast]);
-            if (!MRG) mma_commit(&b_empty[bst]);
+              for (int j = 0; j < kBK / 16; ++j)
+                mma_f16(tmem + iss * 256, adesc + 2 * j, bdesc + 2 * j, idesc, (first && j == 0) ? 0u : 1u);
+              mma_commit(&a_empty[ast]);
+              if (!MRG) mma_commit(&b_empty[bst]);
+            }
+            if (++ast == AS) {
+              ast = 0;
+              aph ^= 1u;
+            }
+            if (++bst == NB) {
+              bst = 0;
+              bph ^= 1u;
+            }
           }
-          if (++ast == AS) {
-            ast = 0;
-            aph ^= 1u;
-          }
-          if (++bst == NB) {
-            bst = 0;
-            bph ^= 1u;
-          }
+          if (ok) mma_commit(&acc_full);
         }
-        if (ok) mma_commit(&acc_full);
       }
     }
   } else {
@@ -426,117 +466,127 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
     const int m = NMAT == 2 ? grp : 0;  // matrix this group converts
     const int r = wc * 16 + (lane & 7) + ((lane >> 4) << 3), hf = (lane >> 3) & 1;
     bool ok = true;
-    int ast = 0, u = 0;
+    int ast = 0, u = 0, su = 0, v = 0, gp = 0;
     uint32_t aph = 0;
-    for (int pass = 0; pass < n_pass && ok; ++pass) {
-      for (int k4 = 0; k4 < ksteps; k4 += kScSteps) {
-        const int su = pass * sps + k4 / kScSteps, sst = su % SS;
-        if (!mbar_wait(&sc_full[sst], (su / SS) & 1, a.dev_status)) {
-          ok = false;
-          break;
-        }
-        const uint4 sc = *reinterpret_cast<const uint4*>(sc_base + sst * L::sc_stage + m * kScTile + r * 16);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sc_empty[sst]);
-#pragma unroll
-        for (int h2 = 0; h2 < kScSteps / kRawSteps; ++h2) {
-          const int v = pass * rps + k4 / kRawSteps + h2, rst = v % RS;
-          if (!mbar_wait(&raw_full[rst], (v / RS) & 1, a.dev_status)) {
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      const PfItem I = pf_item(a, it, false);
+      if (!I.run) continue;
+      const int n_pass = (I.n_e + pmax - 1) / pmax;
+      for (int pass = 0; pass < n_pass && ok; ++pass, ++gp) {
+        for (int k4 = 0; k4 < ksteps; k4 += kScSteps) {
+          const int sst = su % SS;
+          if (!mbar_wait(&sc_full[sst], (su / SS) & 1, a.dev_status)) {
             ok = false;
             break;
           }
-          uint4 cw[kRawSteps];
-          const uint8_t* raw = raw_base + rst * L::raw_stage + m * kRawTile + r * 64;
-#pragma unroll
-          for (int jj = 0; jj < kRawSteps; ++jj)
-            if (NMAT == 2 || jj == grp)
-              cw[jj] = *reinterpret_cast<const uint4*>(raw + (((2 * jj + hf) ^ ((r >> 1) & 3)) << 4));
+          ++su;
+          const uint4 sc = *reinterpret_cast<const uint4*>(sc_base + sst * L::sc_stage + m * kScTile + r * 16);
           __syncwarp();
-          if (lane == 0) mbar_arrive(&raw_empty[rst]);
+          if (lane == 0) mbar_arrive(&sc_empty[sst]);
 #pragma unroll
-          for (int jj = 0; jj < kRawSteps; ++jj) {
-            // k4 and 2 * h2 are even, so this k-step's parity is jj's
-            if (NMAT == 2 || jj == grp) {
-              const int j4 = h2 * kRawSteps + jj;  // k-step within the scale stage
-              if (u >= AS && !mbar_wait(&a_empty[ast], aph ^ 1u, a.dev_status)) {
-                ok = false;
-                break;
+          for (int h2 = 0; h2 < kScSteps / kRawSteps; ++h2) {
+            const int rst = v % RS;
+            if (!mbar_wait(&raw_full[rst], (v / RS) & 1, a.dev_status)) {
+              ok = false;
+              break;
+            }
+            ++v;
+            uint4 cw[kRawSteps];
+            const uint8_t* raw = raw_base + rst * L::raw_stage + m * kRawTile + r * 64;
+#pragma unroll
+            for (int jj = 0; jj < kRawSteps; ++jj)
+              if (NMAT == 2 || jj == grp)
+                cw[jj] = *reinterpret_cast<const uint4*>(raw + (((2 * jj + hf) ^ ((r >> 1) & 3)) << 4));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&raw_empty[rst]);
+#pragma unroll
+            for (int jj = 0; jj < kRawSteps; ++jj) {
+              // k4 and 2 * h2 are even, so this k-step's parity is jj's
+              if (NMAT == 2 || jj == grp) {
+                const int j4 = h2 * kRawSteps + jj;  // k-step within the scale stage
+                if (u >= AS && !mbar_wait(&a_empty[ast], aph ^ 1u, a.dev_status)) {
+                  ok = false;
+                  break;
+                }
+                uint8_t* at = a_base + ast * a_stage + m * kATile + r * 128;
+                const uint32_t sw = j4 == 0 ? sc.x : j4 == 1 ? sc.y : j4 == 2 ? sc.z : sc.w;
+                uint32_t s2[2];
+                scales2(static_cast<unsigned short>(hf ? sw >> 16 : sw & 0xffffu), s2);
+                const uint32_t words[4] = {cw[jj].x, cw[jj].y, cw[jj].z, cw[jj].w};
+#pragma unroll
+                for (int w = 0; w < 4; ++w)
+                  *reinterpret_cast<uint4*>(at + (((4 * hf + w) ^ (r & 7)) << 4)) = dequant8(words[w], s2[w >> 1]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&a_full[ast]);
               }
-              uint8_t* at = a_base + ast * a_stage + m * kATile + r * 128;
-              const uint32_t sw = j4 == 0 ? sc.x : j4 == 1 ? sc.y : j4 == 2 ? sc.z : sc.w;
-              uint32_t s2[2];
-              scales2(static_cast<unsigned short>(hf ? sw >> 16 : sw & 0xffffu), s2);
-              const uint32_t words[4] = {cw[jj].x, cw[jj].y, cw[jj].z, cw[jj].w};
-#pragma unroll
-              for (int w = 0; w < 4; ++w)
-                *reinterpret_cast<uint4*>(at + (((4 * hf + w) ^ (r & 7)) << 4)) = dequant8(words[w], s2[w >> 1]);
-              fence_proxy_async_smem();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&a_full[ast]);
+              ++u;
+              if (++ast == AS) {
+                ast = 0;
+                aph ^= 1u;
+              }
             }
-            ++u;
-            if (++ast == AS) {
-              ast = 0;
-              aph ^= 1u;
-            }
+            if (!ok) break;
           }
           if (!ok) break;
         }
         if (!ok) break;
-      }
-      if (!ok) break;
-      // epilogue of this pass: warp w reads TMEM lanes 32 (w % 4) .. + 31; the
-      // four warps of a lane quarter take every fourth 16-token chunk
-      if (!mbar_wait(&acc_full, pass & 1, a.dev_status)) break;
-      tc_fence_after();
-      float ts[2];
-      {
-        const int64_t fid = static_cast<int64_t>(a.layer) * a.E + e;
-        ts[0] = __ldg(a.tscale + 3 * fid + (NMAT == 2 ? 0 : 2));
-        ts[1] = NMAT == 2 ? __ldg(a.tscale + 3 * fid + 1) : 0.f;
-      }
-      const int q = warp & 3, part = cwarp >> 2;
-      const int n_valid = min(kNMax, n_e - pass * kNMax);
-      const int row = mt * kBM + q * 32 + lane;  // output column of Hp / Yp
-      const size_t m0 = static_cast<size_t>(row_lo) + pass * kNMax;
-      const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16);
-      for (int c0 = part * 16; c0 < n_valid; c0 += 64) {
-        float v0[16], v1[16];
-        tmem_ld16x2(tq + c0, tq + 256 + c0, v0, v1);
-        const float xs_l =
-            (NMAT == 2 && c0 + (lane & 15) < n_valid) ? __ldg(a.x_scale + m0 + c0 + (lane & 15)) : 0.f;
-#pragma unroll
-        for (int jj = 0; jj < 16; jj += 2) {
-          float o[2];
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (NMAT == 2) {
-              const float xs = __shfl_sync(0xffffffffu, xs_l, jj + t);
-              const float gv = v0[jj + t] * ts[0] * xs, uv = v1[jj + t] * ts[1] * xs;
-              o[t] = __fdividef(gv, 1.f + __expf(fminf(-gv, 80.f))) * uv * kHScale;
-              if (!(fabsf(o[t]) <= 65504.f) && c0 + jj + t < n_valid) record_status(a.dev_status, FT_ERR_RANGE);
-            } else {
-              o[t] = (v0[jj + t] + v1[jj + t]) * ts[0] * (1.f / kHScale);
-            }
-          }
-          // lane pairs swap halves so each lane stores two adjacent outputs of
-          // one token (even lane: token jj, odd lane: token jj + 1)
-          const float mine = (lane & 1) ? o[0] : o[1];
-          const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
-          const int col = c0 + jj + (lane & 1);
-          const float lo = (lane & 1) ? other : o[0], hi = (lane & 1) ? o[1] : other;
-          uint32_t pk;
-          if (NMAT == 2)
-            pk = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(lo))) |
-                 (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(hi))) << 16);
-          else
-            pk = static_cast<uint32_t>(f32_to_bf16(lo)) | (static_cast<uint32_t>(f32_to_bf16(hi)) << 16);
-          if (col < n_valid) *reinterpret_cast<uint32_t*>(a.out + (m0 + col) * a.M + (row & ~1)) = pk;
+        // epilogue of this pass: warp w reads TMEM lanes 32 (w % 4) .. + 31; the
+        // four warps of a lane quarter take every fourth 16-token chunk
+        if (!mbar_wait(&acc_full, gp & 1, a.dev_status)) {
+          ok = false;
+          break;
         }
+        tc_fence_after();
+        float ts[2];
+        {
+          const int64_t fid = static_cast<int64_t>(a.layer) * a.E + I.e;
+          ts[0] = __ldg(a.tscale + 3 * fid + (NMAT == 2 ? 0 : 2));
+          ts[1] = NMAT == 2 ? __ldg(a.tscale + 3 * fid + 1) : 0.f;
+        }
+        const int q = warp & 3, part = cwarp >> 2;
+        const int n_valid = min(pmax, I.n_e - pass * pmax);
+        const int row = I.mt * kBM + q * 32 + lane;  // output column of Hp / Yp
+        const size_t m0 = static_cast<size_t>(I.row_lo) + pass * pmax;
+        const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        for (int c0 = part * 16; c0 < n_valid; c0 += 64) {
+          float v0[16], v1[16];
+          tmem_ld16x2(tq + c0, tq + 256 + c0, v0, v1);
+          const float xs_l =
+              (NMAT == 2 && c0 + (lane & 15) < n_valid) ? __ldg(a.x_scale + m0 + c0 + (lane & 15)) : 0.f;
+#pragma unroll
+          for (int jj = 0; jj < 16; jj += 2) {
+            float o[2];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (NMAT == 2) {
+                const float xs = __shfl_sync(0xffffffffu, xs_l, jj + t);
+                const float gv = v0[jj + t] * ts[0] * xs, uv = v1[jj + t] * ts[1] * xs;
+                o[t] = __fdividef(gv, 1.f + __expf(fminf(-gv, 80.f))) * uv * kHScale;
+                if (!(fabsf(o[t]) <= 65504.f) && c0 + jj + t < n_valid) record_status(a.dev_status, FT_ERR_RANGE);
+              } else {
+                o[t] = (v0[jj + t] + v1[jj + t]) * ts[0] * (1.f / kHScale);
+              }
+            }
+            // lane pairs swap halves so each lane stores two adjacent outputs of
+            // one token (even lane: token jj, odd lane: token jj + 1)
+            const float mine = (lane & 1) ? o[0] : o[1];
+            const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+            const int col = c0 + jj + (lane & 1);
+            const float lo = (lane & 1) ? other : o[0], hi = (lane & 1) ? o[1] : other;
+            uint32_t pk;
+            if (NMAT == 2)
+              pk = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(lo))) |
+                   (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(hi))) << 16);
+            else
+              pk = static_cast<uint32_t>(f32_to_bf16(lo)) | (static_cast<uint32_t>(f32_to_bf16(hi)) << 16);
+            if (col < n_valid) *reinterpret_cast<uint32_t*>(a.out + (m0 + col) * a.M + (row & ~1)) = pk;
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty);
     }
   }
   tc_fence_before();
@@ -658,12 +708,18 @@ ft_status experts_prefill(const ft_bank* cache, const ft_bank* pool, int32_t lay
   a.M = I;
   a.x_scale = x_scale;
   a.out = hp;
-  // token tiles inside the A stages when the mean segment is short
+  // token tiles inside the A stages when the mean segment is short (passes
+  // of 128 tokens), else separate token rings (passes of 256); one CTA per SM
+  // walks the (row tile, expert) items
   const bool mrg = static_cast<int64_t>(T) * k <= static_cast<int64_t>(kMrgMeanRows) * E;
+  a.pmax = mrg ? 128 : kNMax;
+  const int sms = device_sm_count();
+  a.tiles = I / kBM;
+  const unsigned g1 = static_cast<unsigned>(std::min<int64_t>(static_cast<int64_t>(a.tiles) * E, sms));
   if (mrg)
-    pf_kernel<2, true><<<dim3(I / kBM, E), kPfThreads, PfSmem<2>::total + 1024, s>>>(mg, mu, mgs, mus, mx, a);
+    pf_kernel<2, true><<<g1, kPfThreads, PfSmem<2>::total + 1024, s>>>(mg, mu, mgs, mus, mx, a);
   else
-    pf_kernel<2, false><<<dim3(I / kBM, E), kPfThreads, PfSmem<2>::total + 1024, s>>>(mg, mu, mgs, mus, mx, a);
+    pf_kernel<2, false><<<g1, kPfThreads, PfSmem<2>::total + 1024, s>>>(mg, mu, mgs, mus, mx, a);
   ft_status stt = launch_check("experts prefill gate/up");
   if (stt != FT_OK) return stt;
   // down: K = I, M = H, output Yp (bf16)
@@ -671,10 +727,12 @@ ft_status experts_prefill(const ft_bank* cache, const ft_bank* pool, int32_t lay
   a.M = H;
   a.x_scale = nullptr;
   a.out = yp;
+  a.tiles = H / kBM;
+  const unsigned g2 = static_cast<unsigned>(std::min<int64_t>(static_cast<int64_t>(a.tiles) * E, sms));
   if (mrg)
-    pf_kernel<1, true><<<dim3(H / kBM, E), kPfThreads, PfSmem<1>::total + 1024, s>>>(md, md, mds, mds, mh, a);
+    pf_kernel<1, true><<<g2, kPfThreads, PfSmem<1>::total + 1024, s>>>(md, md, mds, mds, mh, a);
   else
-    pf_kernel<1, false><<<dim3(H / kBM, E), kPfThreads, PfSmem<1>::total + 1024, s>>>(md, md, mds, mds, mh, a);
+    pf_kernel<1, false><<<g2, kPfThreads, PfSmem<1>::total + 1024, s>>>(md, md, mds, mds, mh, a);
   return launch_check("experts prefill down");
 }
 
