@@ -6,7 +6,8 @@
 // MoE" (fengjutian.github.io), sec. 3 (prefill touches nearly every expert
 // and is dense compute).
 //
-// Two launches, each one CTA per (128-row weight tile, expert):
+// Two launches, each over the work items (128-row weight tile, expert), one
+// persistent CTA per SM walking items blockIdx.x, + gridDim.x, ...:
 //   gate/up:  Hp[m, i] = f16(2^-4 * silu(g) * u), g = gate[i].x_m, u = up[i].x_m
 //   down:     Yp[m, j] = bf16(down[j].h_m)
 // for the rows m of the expert's segment of the permuted batch.  The MMA is
