@@ -119,6 +119,30 @@ def test_prefill_experts_small(cuda_lib, H, I, E, k, T):
     assert_close(got, ref, f"prefill rows {H}x{I}")
 
 
+@pytest.mark.parametrize("E,k,T", [(400, 4, 100), (160, 4, 4000)])
+def test_prefill_experts_many_items(cuda_lib, E, k, T):
+    """More (row tile, expert) work items than SMs, so each persistent CTA
+    walks several and its rings run on from one item to the next: 400
+    experts of which most are empty (short segments, token tiles inside the A
+    stages), and 160 experts of ~100 rows (mean above 96: the separate token
+    ring).  Sampled permuted rows against the oracle."""
+    ft = cuda_lib
+    H, I = 256, 256
+    rng = np.random.default_rng(E + T)
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    x = synth.normal_bf16(synth.stream_key(0, "pf-items", E, T), (T, H))
+    yp, perm, inv, off, bank, ts = _run_prefill(ft, H, I, E, k, ids, x, seed=3)
+    bank_np = bank.cpu().numpy()
+    offsets = off.cpu().numpy()
+    assert np.array_equal(offsets, oracle.permute(ids, E)[2])
+    n = T * k
+    rows = np.unique(np.concatenate([rng.choice(n, min(n, 600), replace=False), [0, n - 1]]))
+    ref = _oracle_rows(lambda e: bank_np[e], H, I, E, 0, x, perm.cpu().numpy(), k, offsets, rows,
+                       synth.tensor_scales(FMT, H, I, E))
+    got = bf16_to_f64(yp.cpu().numpy().view(np.uint16))[rows]
+    assert_close(got, ref, f"prefill {E} experts, {T} tokens")
+
+
 @pytest.mark.parametrize("T", [2048, 8192])
 def test_prefill_full_layer_sampled(cuda_lib, T):
     """The whole-layer prefill shape (H 4096, I 2048, 256 experts, top-6) at
