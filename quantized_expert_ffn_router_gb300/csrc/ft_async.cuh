@@ -64,6 +64,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_
   }
 }
 
+// mbar_wait by every lane of a warp with one verdict for the whole warp (a
+// lane that gave up makes every lane give up), for warps that run
+// warp-collective instructions (tcgen05.ld) after the wait.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int32_t* status) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
+}
+
 // True (for the whole CTA) when an earlier wait of this stream's work already
 // gave up: kernels with bounded waits then return at once instead of waiting
 // out their own.  Every thread of the CTA must call it (it holds a barrier).

@@ -7,12 +7,15 @@
 // kernel does dedup, residency, q, victims and the id rewrite).
 #pragma once
 
+#include <climits>
+
 #include "ft_common.cuh"
 
 namespace ft {
 
 constexpr int kResMaxE = 4096;
 constexpr int kResMaxN = 4096;
+constexpr int kResFastVictims = 16;  // up to this many victims: iterated block argmin
 constexpr size_t kResSmemCap = 220 * 1024;  // dynamic shared memory the resolve kernel may use
 
 struct ResolveArgs {
@@ -324,7 +327,65 @@ __device__ __noinline__ void resolve_block(const ResolveArgs& a, unsigned char* 
   }
   auto slot_hit = [&](int s) -> bool { return shit ? shit[s] != 0 : blocked_global(s); };
   auto slot_use = [&](int s) -> int64_t { return su ? su[s] : a.usage[s]; };
-  if (nf > 0) {
+  if (nf > 0 && nf <= kResFastVictims) {
+    // few victims (the usual decode call): nf rounds of a block-wide argmin
+    // of (usage, slot) over the eligible slots not taken yet, which yields
+    // the nf smallest pairs already in (usage asc, slot asc) order
+    __shared__ long long s_wu[32];
+    __shared__ int s_ws[32];
+    const int lane = tid & 31, warp = tid >> 5, nw = (nt + 31) >> 5;
+    for (int r = 0; r < nf; ++r) {
+      long long bu = LLONG_MAX;
+      int bs = INT_MAX;
+      for (int s = tid; s < S; s += nt) {
+        if (slot_hit(s)) continue;
+        bool taken = false;
+        for (int j = 0; j < r; ++j) taken |= vs2[j] == s;
+        if (taken) continue;
+        const long long u = slot_use(s);
+        if (u < bu || (u == bu && s < bs)) {
+          bu = u;
+          bs = s;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const long long ou = __shfl_xor_sync(0xffffffffu, bu, o);
+        const int os = __shfl_xor_sync(0xffffffffu, bs, o);
+        if (ou < bu || (ou == bu && os < bs)) {
+          bu = ou;
+          bs = os;
+        }
+      }
+      if (lane == 0) {
+        s_wu[warp] = bu;
+        s_ws[warp] = bs;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        bu = lane < nw ? s_wu[lane] : LLONG_MAX;
+        bs = lane < nw ? s_ws[lane] : INT_MAX;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const long long ou = __shfl_xor_sync(0xffffffffu, bu, o);
+          const int os = __shfl_xor_sync(0xffffffffu, bs, o);
+          if (ou < bu || (ou == bu && os < bs)) {
+            bu = ou;
+            bs = os;
+          }
+        }
+        if (lane == 0) {
+          if (bs == INT_MAX) {  // fewer eligible slots than nf: an inconsistent state
+            record_status(a.dev_status, FT_ERR_RANGE);
+            bs = 0;
+          }
+          vs2[r] = bs;
+          vu2[r] = bu;
+        }
+      }
+      __syncthreads();
+    }
+  } else if (nf > 0) {
     unsigned long long kmin = ~0ull, kmax = 0ull;
     for (int s = tid; s < S; s += nt) {
       if (slot_hit(s)) continue;

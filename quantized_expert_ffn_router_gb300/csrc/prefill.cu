@@ -534,7 +534,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
         if (!ok) break;
         // epilogue of this pass: warp w reads TMEM lanes 32 (w % 4) .. + 31; the
         // four warps of a lane quarter take every fourth 16-token chunk
-        if (!mbar_wait(&acc_full, gp & 1, a.dev_status)) {
+        if (!mbar_wait_warp(&acc_full, gp & 1, a.dev_status)) {  // one verdict: tcgen05.ld follows
           ok = false;
           break;
         }
@@ -592,6 +592,18 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
   }
   tc_fence_before();
   __syncthreads();
+  // A wait that gave up (FT_ERR_TIMEOUT recorded) ends its role's loop with
+  // this CTA's TMA copies or MMAs possibly still in flight: let them land
+  // (a bounded 200 us) before the TMEM is freed and the CTA exits.
+  __shared__ int s_drain;
+  if (tid == 0) s_drain = a.dev_status != nullptr && *reinterpret_cast<const volatile int32_t*>(a.dev_status) == FT_ERR_TIMEOUT;
+  __syncthreads();
+  if (s_drain) {
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 200000ull) {
+    }
+    __syncthreads();
+  }
   if (warp == 0) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols) : "memory");

@@ -111,6 +111,7 @@ __global__ void __launch_bounds__(kRThreads, 1) route_mma_kernel(const __grid_co
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full[kRStages], empty[kRStages], acc_full;
   __shared__ uint32_t s_tmem;
+  __shared__ int s_gave_up;  // a wait gave up: copies or MMAs may be in flight at the end
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * kRM, n0 = blockIdx.y * kRN;
   const int kall = H / kRK, z = blockIdx.z, nz = gridDim.z;
@@ -122,6 +123,7 @@ __global__ void __launch_bounds__(kRThreads, 1) route_mma_kernel(const __grid_co
       mbar_init(&empty[s], 1);
     }
     mbar_init(&acc_full, 1);
+    s_gave_up = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -141,7 +143,10 @@ __global__ void __launch_bounds__(kRThreads, 1) route_mma_kernel(const __grid_co
     if (lane == 0) {
       for (int kk = 0; kk < ksteps; ++kk) {
         const int st = kk % kRStages;
-        if (kk >= kRStages && !mbar_wait(&empty[st], ((kk / kRStages) - 1) & 1, nullptr)) break;
+        if (kk >= kRStages && !mbar_wait(&empty[st], ((kk / kRStages) - 1) & 1, nullptr)) {
+          s_gave_up = 1;
+          break;
+        }
         uint8_t* stage = smem + st * kRStage;
         mbar_arrive_expect_tx(&full[st], kRStage);
         const int kc = (kbeg + kk) * kRK;
@@ -156,6 +161,7 @@ __global__ void __launch_bounds__(kRThreads, 1) route_mma_kernel(const __grid_co
         const int st = kk % kRStages;
         if (!mbar_wait(&full[st], (kk / kRStages) & 1, nullptr)) {
           ok = false;
+          s_gave_up = 1;
           break;
         }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -186,7 +192,9 @@ __global__ void __launch_bounds__(kRThreads, 1) route_mma_kernel(const __grid_co
     }
   } else {
     // warps 2..5: TMEM lane quarter q = warp % 4, token m0 + 32 q + lane
-    if (mbar_wait(&acc_full, 0, nullptr)) {
+    if (!mbar_wait_warp(&acc_full, 0, nullptr)) {  // one verdict per warp: tcgen05.ld follows
+      s_gave_up = 1;
+    } else {
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const int q = warp & 3;
       const int t = m0 + q * 32 + lane;
@@ -211,6 +219,12 @@ __global__ void __launch_bounds__(kRThreads, 1) route_mma_kernel(const __grid_co
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
+  if (s_gave_up) {  // let this CTA's copies and MMAs still in flight land (bounded)
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 200000ull) {
+    }
+    __syncthreads();
+  }
   if (warp == 1) {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kRCols) : "memory");
