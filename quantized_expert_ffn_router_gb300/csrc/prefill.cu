@@ -461,7 +461,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
     // half 1, so the eight lanes of each shared-memory phase touch eight
     // consecutive rows and, with the 64-byte swizzle of the code tiles and
     // the 128-byte swizzle of the A tiles, distinct banks.  Each stage's codes
-    // and scales go to registers at once and the stage is released.
+    // and scales go to registers at once and the stage is released.  The
+    // release is preceded by a proxy fence: the loads are generic-proxy reads
+    // and the TMA that refills the stage writes through the async proxy, and
+    // the mbarrier hand-off alone does not order the two.  Without the fence
+    // a load still outstanding at the arrive could return the next stage's
+    // bytes (seen on GB300 as a few weight rows of a tile differing from one
+    // run to the next, at 192-token segments).
     const int cwarp = warp - 4;
     const int grp = cwarp >> 3, wc = cwarp & 7;
     const int m = NMAT == 2 ? grp : 0;  // matrix this group converts
@@ -482,6 +488,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
           }
           ++su;
           const uint4 sc = *reinterpret_cast<const uint4*>(sc_base + sst * L::sc_stage + m * kScTile + r * 16);
+          fence_proxy_async_smem();  // the scale words are read before the TMA may refill the stage
           __syncwarp();
           if (lane == 0) mbar_arrive(&sc_empty[sst]);
 #pragma unroll
@@ -498,6 +505,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_kernel(const __grid_constant
             for (int jj = 0; jj < kRawSteps; ++jj)
               if (NMAT == 2 || jj == grp)
                 cw[jj] = *reinterpret_cast<const uint4*>(raw + (((2 * jj + hf) ^ ((r >> 1) & 3)) << 4));
+            fence_proxy_async_smem();  // likewise the code words
             __syncwarp();
             if (lane == 0) mbar_arrive(&raw_empty[rst]);
 #pragma unroll

@@ -186,3 +186,46 @@ def test_prefill_full_layer_sampled(cuda_lib, T):
     ref_c = oracle.combine(yp.cpu().numpy().view(np.uint16), inv_np[toks], w.cpu().numpy()[toks])
     got_c = bf16_to_f64(out.cpu().numpy().view(np.uint16)[toks])
     assert_close(got_c, ref_c, "prefill combine", ref_max=None)
+
+
+@pytest.mark.parametrize("T", [2048, 8192])
+def test_prefill_repeats_are_identical(cuda_lib, T):
+    """The grouped experts call is deterministic: at the whole-layer prefill
+    shape, twelve calls on the same permuted batch give byte-identical Hp
+    (gate/up output) and Yp.  At 8192 tokens (192-token segments, passes of
+    256) a ring stage released before its shared-memory loads had returned
+    once let the refilling TMA change a few weight rows of a tile in most
+    calls; this catches that class of race."""
+    ft = cuda_lib
+    cfg = synth.get_config("prefill")
+    H, I, E, k = cfg.H, cfg.I, cfg.E, cfg.k
+    n = T * k
+    W = synth.router_weights(cfg.seed, 0, E, H, cfg.router_std)
+    x = synth.normal_bf16(synth.stream_key(cfg.seed, "prefill-x", T), (T, H))
+    ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    rws = torch.zeros(ft.route_workspace(T, E, H), dtype=torch.uint8, device=DEV)
+    ft.route(_t(x), _t(W), k, ids, w, rws)
+    torch.cuda.synchronize()
+    _, perm, inv, off, bank, ts = _run_prefill(ft, H, I, E, k, ids.cpu().numpy(), x, seed=cfg.seed)
+    cb = ft.make_bank(FMT, H, I, 16, bank, ts)
+    xp = torch.empty((n, H), dtype=torch.int16, device=DEV)
+    xs = torch.empty(n, dtype=torch.float32, device=DEV)
+    pws = torch.empty(ft.permute_workspace(T, k, E), dtype=torch.uint8, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ft.permute(ids, E, _t(x), perm, inv, off, xp, pws, dev_status=status, xp_scale=xs)
+    slot = torch.arange(E, dtype=torch.int32, device=DEV)
+    yp = torch.empty((n, H), dtype=torch.int16, device=DEV)
+    ews = torch.empty(ft.experts_workspace(ft.FT_PREFILL, T, k, H, I, E), dtype=torch.uint8, device=DEV)
+    hp0 = yp0 = None
+    for rep in range(12):
+        ft.experts_fwd(cb, None, 0, E, xp, T, k, slot, None, None, yp, ews, mode=ft.FT_PREFILL, offsets=off,
+                       dev_status=status, x_scale=xs)
+        torch.cuda.synchronize()
+        assert ft.get_status(status) == 0
+        hp = ews[: n * I * 2].clone()
+        if hp0 is None:
+            hp0, yp0 = hp, yp.clone()
+        n_hp = int((hp != hp0).sum())
+        n_yp = int((yp != yp0).any(dim=1).sum())
+        assert n_hp == 0 and n_yp == 0, f"call {rep}: {n_hp} Hp bytes and {n_yp} Yp rows differ from the first call"
