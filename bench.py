@@ -299,9 +299,15 @@ class DecodeWorkload:
     # one around every op of every layer (per_op, the breakdown graph)
     EXP_EVERY = 8
 
+    # the separate calls' router and resolve as one C call (ft_moe_route_resolve:
+    # the top-k inside the resolve kernel); False: ft_moe_route + ft_moe_resolve_slots
+    combined = True
+
     @property
     def OPS(self):
-        return ["layer"] if self.fused else ["route", "resolve", "fetch", "experts"]
+        if self.fused:
+            return ["layer"]
+        return ["route_resolve", "fetch", "experts"] if self.combined else ["route", "resolve", "fetch", "experts"]
 
     @property
     def KERNELS_PER_LAYER(self):
@@ -329,16 +335,21 @@ class DecodeWorkload:
                 mark(l, 1, edge=1)
                 continue
             mark(l, 0)
-            ft.route(self.x_stage[l], self.W[l], cfg.k, self.ids[l], self.w[l], self.rws)
-            mark(l, 1)
-            ft.resolve_slots(self.state, l, self.ids[l], self.phi, self.slot[l], self.nf[l], self.ff[l],
-                             self.fs[l], self.status)
-            mark(l, 2)
+            if self.combined:
+                ft.route_resolve(self.x_stage[l], self.W[l], cfg.k, self.ids[l], self.w[l], self.rws, self.state, l,
+                                 self.phi, self.slot[l], self.nf[l], self.ff[l], self.fs[l], dev_status=self.status)
+            else:
+                ft.route(self.x_stage[l], self.W[l], cfg.k, self.ids[l], self.w[l], self.rws)
+                mark(l, 1)
+                ft.resolve_slots(self.state, l, self.ids[l], self.phi, self.slot[l], self.nf[l], self.ff[l],
+                                 self.fs[l], self.status)
+            n0 = 1 if self.combined else 2
+            mark(l, n0)
             ft.fetch(self.pool_b, self.cache_b, self.nf[l], self.ff[l], self.fs[l], self.status)
-            mark(l, 3, edge=0)
+            mark(l, n0 + 1, edge=0)
             ft.experts_fwd(self.cache_b, self.pool_b, l, cfg.E, self.x_stage[l], T, cfg.k, self.slot[l],
                            self.ids[l], self.w[l], self.out[l], self.ews, dev_status=self.status)
-            mark(l, 4, edge=1)
+            mark(l, n0 + 2, edge=1)
 
     def use_fused(self, want: bool) -> bool:
         """Run the step as one fused kernel per layer when asked and the
@@ -1125,6 +1136,8 @@ def main():
     ap.add_argument("--no-flash", action="store_true", help="skip the NVFP4 (flash) decode measurement")
     ap.add_argument("--prefill-layers", type=int, default=3,
                     help="layers streamed from host memory through the prefill double buffer (0: skip)")
+    ap.add_argument("--route-resolve", choices=["combined", "separate"], default="combined",
+                    help="the separate-calls step's router and resolve: ft_moe_route_resolve, or the two calls")
     ap.add_argument("--layer-kernel", choices=["fused", "separate"], default="separate",
                     help="decode step as the separate route / resolve / fetch / experts calls (measured faster) or "
                          "as one ft_moe_decode_layer kernel per layer (when the shape fits); the other form is "
@@ -1176,6 +1189,7 @@ def main():
             wl = DecodeWorkload(cfg, T, args.phi, n_steps, device, log)
         else:
             wl = reshape_workload(wl, T, n_steps)
+        wl.combined = args.route_resolve == "combined"
         fused = wl.use_fused(args.layer_kernel == "fused")
         wl.capture()
         wl.settle(args.settle)
@@ -1192,7 +1206,7 @@ def main():
         e2e_val, _, _ = aggregate(units, e2e_secs, world, reduce_fn)
         results[T] = dict(value=value, secs=secs_max, kt=kt, exp_us=exp_us, ebytes=ebytes, nfetch=nfetch,
                           host_pairs=host_pairs, e2e=e2e_val, h2d=h2d, d2h=d2h,
-                          clocks=clocks.summary() if clocks else None, fused=fused,
+                          clocks=clocks.summary() if clocks else None, fused=fused, combined=wl.combined,
                           kernels_per_layer=wl.KERNELS_PER_LAYER)
         st = ft.get_status(wl.status)
         if st != 0:
@@ -1320,7 +1334,9 @@ def main():
             "expert_bytes_per_step": r["ebytes"],
             "step": ("per layer: ft_moe_decode_layer (one kernel: route, resolve with the q* split, fetch, "
                      "experts, combine)" if r["fused"] else
-                     "per layer: ft_moe_route, ft_moe_resolve_slots, ft_moe_fetch, ft_moe_experts_fwd (two kernels)"),
+                     ("per layer: ft_moe_route_resolve (router logits grid, then one resolve CTA that takes the "
+                      "top-k first), ft_moe_fetch, ft_moe_experts_fwd (two kernels)" if r.get("combined", True) else
+                      "per layer: ft_moe_route, ft_moe_resolve_slots, ft_moe_fetch, ft_moe_experts_fwd (two kernels)")),
             "other_form": r.get("other_form"),
             "phi_26214": r.get("phi_26214"),
             "host_link": r.get("host_link"),

@@ -5,6 +5,8 @@
  * The layer, one call per step, all on one CUDA stream with no host sync:
  *   ft_moe_route          router logits, softmax, top-k
  *   ft_moe_resolve_slots  (layer, expert) -> cache slot or -1, q* split inside
+ *   ft_moe_route_resolve  the two calls above with the top-k taken inside the
+ *                         resolve kernel (one router grid, one resolve CTA)
  *   ft_moe_prefetch       speculative plan: the next layer's predicted misses
  *                         into eligible slots, one layer ahead of its resolve
  *   ft_moe_fetch          copy the chosen misses from the pool into the cache
@@ -212,6 +214,34 @@ FT_API ft_status ft_moe_resolve_slots(const ft_cache_state* state_host, int32_t 
                                int32_t frac_q16, int32_t* slot_ids, int32_t* num_fetch,
                                int32_t* fetch_fid, int32_t* fetch_slot, int32_t max_list,
                                int32_t* dev_status, void* stream);
+
+/*
+ * ft_moe_route_resolve -- ft_moe_route followed by ft_moe_resolve_slots
+ * (FreeToken paper post, sec. 2: the router on the GPU feeding the hit /
+ * miss split; sec. 6: one kernel dedups, checks residency, splits by q*,
+ * picks victims and rewrites ids), with every output of those two calls:
+ * topk_ids, topk_w, slot_ids, num_fetch, fetch_fid, fetch_slot and the
+ * state update, bit for bit.  For T * k <= 32, E <= 512 and the state's
+ * own E, the router grid writes only the logits and the resolve kernel takes
+ * each token's softmax and top-k (one warp per token) before resolving,
+ * which removes the router's arrival counter, its last CTA's top-k and the
+ * reload of the ids from the chain.  Other shapes run the two calls in
+ * order (larger calls resolve with the whole block, where the top-k in
+ * front of it gained nothing).  Arguments as in the two calls: x [T,H] bf16, w_router [E,H] fp32
+ * (both 16-byte aligned), route_ws of ft_moe_route_workspace(T,E,H) bytes
+ * (zero-filled before its first use; this call leaves its counter as it
+ * found it), the state, layer, frac_q16, slot_ids [T,k], num_fetch [1],
+ * fetch_fid / fetch_slot [max_list], dev_status.  Invalid arguments of
+ * either call are refused before anything is launched on the one-kernel
+ * shapes.
+ */
+FT_API ft_status ft_moe_route_resolve(const uint16_t* x, int32_t T, int32_t H, const float* w_router,
+                               int32_t E, int32_t k, int32_t renorm, int32_t* topk_ids,
+                               float* topk_w, void* route_ws, size_t route_ws_bytes,
+                               const ft_cache_state* state_host, int32_t layer, int32_t frac_q16,
+                               int32_t* slot_ids, int32_t* num_fetch, int32_t* fetch_fid,
+                               int32_t* fetch_slot, int32_t max_list, int32_t* dev_status,
+                               void* stream);
 
 /*
  * ft_moe_prefetch -- plan a speculative fetch of the next layer's experts

@@ -54,6 +54,8 @@ _SIGS = {
     "ft_moe_route": (_I32, [_V, _I32, _I32, _V, _I32, _I32, _I32, _V, _V, _V, _SZ, _V]),
     "ft_moe_split_q16": (_I32, [_V, _I32, _I32, _V, _V]),
     "ft_moe_resolve_slots": (_I32, [_V, _I32, _V, _I32, _I32, _I32, _V, _V, _V, _V, _I32, _V, _V]),
+    "ft_moe_route_resolve": (_I32, [_V, _I32, _I32, _V, _I32, _I32, _I32, _V, _V, _V, _SZ, _V, _I32, _I32, _V, _V,
+                                    _V, _V, _I32, _V, _V]),
     "ft_moe_prefetch": (_I32, [_V, _I32, _V, _I32, _I32, _I32, _V, _V, _V, _I32, _V, _V]),
     "ft_moe_fetch": (_I32, [_V, _V, _V, _V, _V, _I32, _V, _V]),
     "ft_moe_fetch_layer": (_I32, [_V, _V, _I32, _I32, _I32, _V]),
@@ -190,6 +192,19 @@ def resolve_slots(state: DeviceCacheState, layer: int, topk_ids, frac_q16: int, 
                                        _ptr(slot_ids), _ptr(num_fetch), _ptr(fetch_fid),
                                        _ptr(fetch_slot), fetch_fid.numel(), _ptr(dev_status),
                                        _stream(stream)))
+
+
+def route_resolve(x, w_router, k: int, topk_ids, topk_w, ws, state: DeviceCacheState, layer: int, frac_q16: int,
+                  slot_ids, num_fetch, fetch_fid, fetch_slot, dev_status=None, renorm: bool = False, stream=None):
+    """route() then resolve_slots() as one C call (ft_moe_route_resolve):
+    the same outputs, with the top-k taken inside the resolve kernel."""
+    T, H = x.shape
+    E = w_router.shape[0]
+    st = state.struct()
+    _check(load().ft_moe_route_resolve(_ptr(x), T, H, _ptr(w_router), E, k, int(bool(renorm)), _ptr(topk_ids),
+                                       _ptr(topk_w), _ptr(ws), ws.numel() * ws.element_size(), ctypes.byref(st),
+                                       layer, int(frac_q16), _ptr(slot_ids), _ptr(num_fetch), _ptr(fetch_fid),
+                                       _ptr(fetch_slot), fetch_fid.numel(), _ptr(dev_status), _stream(stream)))
 
 
 def prefetch(state: DeviceCacheState, layer: int, pred_ids, max_prefetch: int, num_fetch, fetch_fid,

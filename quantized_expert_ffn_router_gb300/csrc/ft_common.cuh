@@ -40,6 +40,11 @@ size_t route_mma_split_bytes(int T, int E, int H);
 float* route_mma_partials(void* extra, int E, int H);
 ft_status route_mma_logits(const uint16_t* x, int T, int H, const float* W, int E, float* logits, void* extra,
                            int* slices, cudaStream_t s);
+// The router logits alone for T <= 16 (route.cu), in the workspace of
+// ft_moe_route: *logits_out = [E][*stride_out] floats, token t's logit of
+// expert e at e * stride + t.
+ft_status route_rows_logits(const uint16_t* x, int T, int H, const float* W, int E, void* ws, cudaStream_t s,
+                            const float** logits_out, int* stride_out);
 
 // Raise a kernel's dynamic shared memory limit to `bytes` on the current
 // device, once per (kernel, device); FT_ERR_CUDA if the device refuses.

@@ -39,8 +39,10 @@ size_t route_logits_bytes(int T, int E) {
 // once; partial sums meet in shared memory (fixed order).  The last CTA to
 // finish (an arrival counter after the logits in the workspace, back at zero
 // when the call ends) then runs the softmax and top-k of every token.
+// TAIL = false: the logits only (the combined route + resolve call takes the
+// top-k in its resolve kernel, which waits for this whole grid anyway).
 
-template <int TMAX>
+template <int TMAX, bool TAIL = true>
 __global__ void __launch_bounds__(256) route_rows_kernel(const uint16_t* __restrict__ x, int T, int H,
                                                          const float* __restrict__ W, int E,
                                                          float* __restrict__ logits, unsigned* counter,
@@ -116,6 +118,7 @@ __global__ void __launch_bounds__(256) route_rows_kernel(const uint16_t* __restr
     for (int w = 0; w < 8; ++w) v += part[w][threadIdx.x];
     logits[static_cast<size_t>(e) * route_row_stride(T) + threadIdx.x] = v;
   }
+  if (!TAIL) return;
   __syncthreads();
   if (threadIdx.x == 0) {
     // the arrival releases this CTA's logits (written before the barrier
@@ -270,6 +273,40 @@ ft_status launch_rows(const uint16_t* x, int T, int H, const float* W, int E, in
 }
 
 }  // namespace
+
+// Logits only, for T <= 16: [E][route_row_stride(T)] floats at ws + 256
+// (the layout the top-k of the combined route + resolve call reads), one CTA
+// per expert row, launched as a programmatic dependent of the previous kernel.
+ft_status route_rows_logits(const uint16_t* x, int T, int H, const float* W, int E, void* ws, cudaStream_t s,
+                            const float** logits_out, int* stride_out) {
+  float* logits = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kRouteCounterBytes);
+  cudaLaunchConfig_t rc = {};
+  rc.gridDim = dim3(E);
+  rc.blockDim = dim3(256);
+  rc.dynamicSmemBytes = 0;
+  rc.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  rc.attrs = at;
+  rc.numAttrs = 1;
+  cudaError_t le;
+  unsigned* counter = static_cast<unsigned*>(ws);  // untouched without the tail
+  if (T <= 1)
+    le = cudaLaunchKernelEx(&rc, route_rows_kernel<1, false>, x, T, H, W, E, logits, counter, 1, 0,
+                            static_cast<int32_t*>(nullptr), static_cast<float*>(nullptr));
+  else if (T <= 4)
+    le = cudaLaunchKernelEx(&rc, route_rows_kernel<4, false>, x, T, H, W, E, logits, counter, 1, 0,
+                            static_cast<int32_t*>(nullptr), static_cast<float*>(nullptr));
+  else
+    le = cudaLaunchKernelEx(&rc, route_rows_kernel<16, false>, x, T, H, W, E, logits, counter, 1, 0,
+                            static_cast<int32_t*>(nullptr), static_cast<float*>(nullptr));
+  if (le != cudaSuccess) return fail(FT_ERR_CUDA, "route logits: %s", cudaGetErrorString(le));
+  *logits_out = logits;
+  *stride_out = route_row_stride(T);
+  return launch_check("route logits");
+}
+
 }  // namespace ft
 
 extern "C" {
