@@ -52,7 +52,7 @@ import ctypes
 
 from . import (FT_DECODE, FT_DECODE_HOST, FT_PREFILL, DeviceCacheState, FtBank, cache_install, combine, experts_fwd,
                experts_workspace, fetch, fetch_layer, make_bank, merge_partials, permute, permute_workspace, prefetch,
-               resolve_slots, route, route_workspace)
+               resolve_slots, route, route_resolve, route_workspace)
 from . import cache_rebuild as _cache_rebuild
 
 
@@ -101,9 +101,10 @@ class DecodeLayer:
         import torch
 
         main = torch.cuda.current_stream()
-        route(x, w_router, self.k, self.ids, self.w, self.route_ws, stream=main)
-        resolve_slots(self.state, layer, self.ids, frac_q16, self.slot_ids, self.num_fetch, self.fetch_fid,
-                      self.fetch_slot, self.status, stream=main)
+        # route + resolve in one call (the top-k inside the resolve kernel where the shape allows)
+        route_resolve(x, w_router, self.k, self.ids, self.w, self.route_ws, self.state, layer, frac_q16,
+                      self.slot_ids, self.num_fetch, self.fetch_fid, self.fetch_slot, dev_status=self.status,
+                      stream=main)
         if not overlapped or self.pool is None:
             if self.pool is not None:
                 fetch(self.pool, self.cache, self.num_fetch, self.fetch_fid, self.fetch_slot, self.status,
