@@ -103,44 +103,187 @@ __device__ __forceinline__ uint64_t ukey(int64_t u) {
   return static_cast<uint64_t>(u) ^ 0x8000000000000000ull;
 }
 
-// The common small case in one warp: n <= 32 ids, all valid, and the q*
+// The small calls, n <= 32 ids and all valid, start in one warp: lane i
+// holds pair i, its expert's slot before the update (map) and, on the first
+// lane of each distinct expert (its leader), whether it hits.  When the q*
 // split fetches nothing (every distinct expert hits, or the split or the
-// evictable slots allow no fetch).  Then the state update is only the usage
-// of the hit slots and the recency of the distinct experts, and the outputs
-// are the map lookups -- the same results as the general path below.
-// Returns true (warp-uniform) when it has done the whole call.
-__device__ bool resolve_small_no_fetch(const ResolveArgs& a) {
+// evictable slots allow no fetch) the warp finishes the call: the state
+// update is the usage of the hit slots and the recency of the distinct
+// experts, the outputs are the map lookups.  When it fetches 1 to
+// kResFastVictims experts, the warp ranks the misses by (recency desc, id
+// asc) and lists the hit slots; the block then takes the victims
+// (resolve_small_victims) and the warp installs them (resolve_small_finish).
+// Either way the results are those of the general path below.
+struct ResSmall {
+  int nf, nhit;
+  long long now;
+  int fe[32];        // the fetched experts, by rank
+  int hit[32];       // the slots the hits own (excluded from the victims)
+  int vict[kResFastVictims];
+  int lane_e[32];    // per pair: its expert
+  int lane_slot[32]; // per pair: its slot before the update, -1 for a miss
+  int lane_rank[32]; // per pair: its expert's rank among the misses, -1 for a hit
+};
+
+// Returns (warp-uniform) 1 when the call is done, 2 when the block goes on
+// with the victims, 0 for the general path.
+__device__ int resolve_small(const ResolveArgs& a, ResSmall* sm) {
   const int lane = threadIdx.x & 31;
   const int n = a.n, E = a.E, base = a.layer * a.E;
   const int64_t now = *a.step;
   const int e = lane < n ? resolve_id(a, lane) : -1;
   const bool bad = lane < n && (e < 0 || e >= E);
-  if (__any_sync(0xffffffffu, bad)) return false;
+  if (__any_sync(0xffffffffu, bad)) return 0;
   const int s = lane < n ? a.map[base + e] : -1;
   const unsigned same = __match_any_sync(0xffffffffu, e);
-  const bool leader = lane < n && lane == __ffs(same) - 1;
-  const int nhit = __popc(__ballot_sync(0xffffffffu, leader && s >= 0));
-  const int m = __popc(__ballot_sync(0xffffffffu, leader && s < 0));
+  const int lead = __ffs(same) - 1;
+  const bool leader = lane < n && lane == lead;
+  const unsigned hitb = __ballot_sync(0xffffffffu, leader && s >= 0);
+  const unsigned missb = __ballot_sync(0xffffffffu, leader && s < 0);
+  const int nhit = __popc(hitb), m = __popc(missb);
   const int nf = max(0, min(split_q16_dev(m, a.phi), a.S - nhit));
-  if (nf > 0) return false;
-  if (leader) {
-    if (s >= 0) a.usage[s] = now;
-    a.recency[base + e] = now;
+  if (nf == 0) {
+    if (leader) {
+      if (s >= 0) a.usage[s] = now;
+      a.recency[base + e] = now;
+    }
+    if (lane < n) {
+      a.slot_ids[lane] = s;
+      if (a.slot_ids_sm) a.slot_ids_sm[lane] = s;
+    }
+    for (int i = lane; i < a.max_list; i += 32) {
+      a.fetch_fid[i] = -1;
+      a.fetch_slot[i] = -1;
+    }
+    if (lane == 0) {
+      *a.num_fetch = 0;
+      if (a.num_fetch_sm) *a.num_fetch_sm = 0;
+      *a.step = now + 1;
+    }
+    return 1;
   }
+  if (nf > kResFastVictims) return 0;
+  const bool miss = leader && s < 0;
+  const int64_t rec = miss ? a.recency[base + e] : 0;
+  int r = 0;  // this miss's rank: misses before it by (recency desc, id asc)
+  for (int j = 0; j < 32; ++j) {
+    const int64_t rj = __shfl_sync(0xffffffffu, rec, j);
+    const int ej = __shfl_sync(0xffffffffu, e, j);
+    if ((missb >> j) & 1u) r += (rj > rec) || (rj == rec && ej < e);
+  }
+  if (miss && r < nf) sm->fe[r] = e;
+  if (leader && s >= 0) sm->hit[__popc(hitb & ((1u << lane) - 1u))] = s;
+  const int rank = __shfl_sync(0xffffffffu, miss ? r : -1, lead);  // the pair's expert's rank
   if (lane < n) {
-    a.slot_ids[lane] = s;
-    if (a.slot_ids_sm) a.slot_ids_sm[lane] = s;
-  }
-  for (int i = lane; i < a.max_list; i += 32) {
-    a.fetch_fid[i] = -1;
-    a.fetch_slot[i] = -1;
+    sm->lane_e[lane] = e;
+    sm->lane_slot[lane] = s;
+    sm->lane_rank[lane] = rank;
   }
   if (lane == 0) {
-    *a.num_fetch = 0;
-    if (a.num_fetch_sm) *a.num_fetch_sm = 0;
+    sm->nf = nf;
+    sm->nhit = nhit;
+    sm->now = now;
+  }
+  return 2;
+}
+
+// The block: nf rounds of a block-wide argmin of (usage, slot) over the
+// slots that no hit owns and no earlier round took, which yields the nf
+// victims already in (usage asc, slot asc) order.  Every thread calls it.
+__device__ void resolve_small_victims(const ResolveArgs& a, ResSmall* sm) {
+  __shared__ long long s_vu[32];
+  __shared__ int s_vs[32];
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = (nt + 31) >> 5;
+  const int nf = sm->nf, nhit = sm->nhit;
+  for (int r = 0; r < nf; ++r) {
+    long long bu = LLONG_MAX;
+    int bs = INT_MAX;
+    for (int s = tid; s < a.S; s += nt) {
+      bool skip = false;
+      for (int j = 0; j < nhit; ++j) skip |= sm->hit[j] == s;
+      for (int j = 0; j < r; ++j) skip |= sm->vict[j] == s;
+      if (skip) continue;
+      const long long u = a.usage[s];
+      if (u < bu || (u == bu && s < bs)) {
+        bu = u;
+        bs = s;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const long long ou = __shfl_xor_sync(0xffffffffu, bu, o);
+      const int os = __shfl_xor_sync(0xffffffffu, bs, o);
+      if (ou < bu || (ou == bu && os < bs)) {
+        bu = ou;
+        bs = os;
+      }
+    }
+    if (lane == 0) {
+      s_vu[warp] = bu;
+      s_vs[warp] = bs;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      bu = lane < nw ? s_vu[lane] : LLONG_MAX;
+      bs = lane < nw ? s_vs[lane] : INT_MAX;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const long long ou = __shfl_xor_sync(0xffffffffu, bu, o);
+        const int os = __shfl_xor_sync(0xffffffffu, bs, o);
+        if (ou < bu || (ou == bu && os < bs)) {
+          bu = ou;
+          bs = os;
+        }
+      }
+      if (lane == 0) {
+        if (bs == INT_MAX) {  // fewer eligible slots than nf: an inconsistent state
+          record_status(a.dev_status, FT_ERR_RANGE);
+          bs = 0;
+        }
+        sm->vict[r] = bs;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// The warp: evict the victims' owners, install the fetched experts, the
+// usage of hit and fetched slots, the recency of every distinct expert,
+// then the outputs.
+__device__ void resolve_small_finish(const ResolveArgs& a, const ResSmall* sm) {
+  const int lane = threadIdx.x & 31;
+  const int n = a.n, base = a.layer * a.E, nf = sm->nf;
+  const int64_t now = sm->now;
+  if (lane < sm->nhit) a.usage[sm->hit[lane]] = now;
+  if (lane < nf) {
+    const int old = a.slot_owner[sm->vict[lane]];
+    if (old >= 0) a.map[old] = -1;
+  }
+  __syncwarp();
+  if (lane < nf) {
+    const int e = sm->fe[lane], v = sm->vict[lane];
+    a.slot_owner[v] = base + e;
+    a.map[base + e] = v;
+    a.usage[v] = now;
+  }
+  const int e = lane < n ? sm->lane_e[lane] : -1;
+  const unsigned same = __match_any_sync(0xffffffffu, e);
+  if (lane < n && lane == __ffs(same) - 1) a.recency[base + e] = now;
+  if (lane < n) {
+    const int s0 = sm->lane_slot[lane], rk = sm->lane_rank[lane];
+    const int sl = s0 >= 0 ? s0 : (rk >= 0 && rk < nf ? sm->vict[rk] : -1);
+    a.slot_ids[lane] = sl;
+    if (a.slot_ids_sm) a.slot_ids_sm[lane] = sl;
+  }
+  for (int i = lane; i < a.max_list; i += 32) {
+    a.fetch_fid[i] = i < nf ? base + sm->fe[i] : -1;
+    a.fetch_slot[i] = i < nf ? sm->vict[i] : -1;
+  }
+  if (lane == 0) {
+    *a.num_fetch = nf;
+    if (a.num_fetch_sm) *a.num_fetch_sm = nf;
     *a.step = now + 1;
   }
-  return true;
 }
 // The whole resolve call by one CTA (any block size; every thread calls it).
 // smem: the dynamic shared memory resolve_prepare asked for.  ids must be
@@ -175,12 +318,18 @@ __device__ __noinline__ void resolve_block(const ResolveArgs& a, unsigned char* 
 
   if (n <= 32 && !a.prefetch) {
     __shared__ int s_done;
+    __shared__ ResSmall s_small;
     if (tid < 32) {
-      const bool done = resolve_small_no_fetch(a);
+      const int done = resolve_small(a, &s_small);
       if (tid == 0) s_done = done;
     }
     __syncthreads();
-    if (s_done) return;
+    if (s_done == 1) return;
+    if (s_done == 2) {
+      resolve_small_victims(a, &s_small);
+      if (tid < 32) resolve_small_finish(a, &s_small);
+      return;
+    }
   }
 
   for (int e = tid; e < E; e += nt) {
