@@ -30,9 +30,17 @@ struct RouteTopk {
   float* wts;
 };
 
+// The arguments stay in the parameter space (__grid_constant__): resolve_block
+// reads them there by reference instead of from a local copy.
 template <bool TOPK>
-__global__ void __launch_bounds__(kResThreads, 1) resolve_kernel(ResolveArgs a, RouteTopk r) {
+__global__ void __launch_bounds__(kResThreads, 1) resolve_kernel(const __grid_constant__ ResolveArgs a,
+                                                                 const __grid_constant__ RouteTopk r) {
   extern __shared__ __align__(16) unsigned char smem[];
+  if (TOPK && threadIdx.x == 0) {
+    // the step counter is not the router's output: its last writer finished
+    // before the router grid let this kernel start, so it may be fetched now
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(a.step));
+  }
   pdl_wait();               // ids (or the router logits) come from the previous kernel
   pdl_launch_dependents();  // the next call (fetch) may start its launch now
   if (!TOPK) {
@@ -45,9 +53,7 @@ __global__ void __launch_bounds__(kResThreads, 1) resolve_kernel(ResolveArgs a, 
     topk_any(r.logits + warp, nullptr, r.E, r.k, r.renorm, s_ids + warp * r.k, r.wts + warp * r.k, r.stride);
   __syncthreads();
   for (int i = threadIdx.x; i < r.T * r.k; i += blockDim.x) r.ids[i] = s_ids[i];
-  ResolveArgs b = a;
-  b.ids_sm = s_ids;
-  resolve_block(b, smem);
+  resolve_block(a, smem, s_ids);
 }
 
 // Copy fetched expert blocks pool[fid] -> cache[slot] for i < *num_fetch.

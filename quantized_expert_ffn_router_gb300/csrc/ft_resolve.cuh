@@ -127,11 +127,11 @@ struct ResSmall {
 
 // Returns (warp-uniform) 1 when the call is done, 2 when the block goes on
 // with the victims, 0 for the general path.
-__device__ int resolve_small(const ResolveArgs& a, ResSmall* sm) {
+__device__ __forceinline__ int resolve_small(const ResolveArgs& a, ResSmall* sm, const int32_t* ids_sm) {
   const int lane = threadIdx.x & 31;
   const int n = a.n, E = a.E, base = a.layer * a.E;
   const int64_t now = *a.step;
-  const int e = lane < n ? resolve_id(a, lane) : -1;
+  const int e = lane < n ? (ids_sm ? ids_sm[lane] : resolve_id(a, lane)) : -1;
   const bool bad = lane < n && (e < 0 || e >= E);
   if (__any_sync(0xffffffffu, bad)) return 0;
   const int s = lane < n ? a.map[base + e] : -1;
@@ -289,7 +289,9 @@ __device__ void resolve_small_finish(const ResolveArgs& a, const ResSmall* sm) {
 // smem: the dynamic shared memory resolve_prepare asked for.  ids must be
 // readable by the CTA (written by an earlier grid, or by this CTA before a
 // __syncthreads).
-__device__ __noinline__ void resolve_block(const ResolveArgs& a, unsigned char* smem) {
+// ids_sm, when not null, is a shared-memory copy of ids [n] that this CTA
+// wrote before a __syncthreads, read instead of a.ids / a.ids_sm.
+__device__ __noinline__ void resolve_block(const ResolveArgs& a, unsigned char* smem, const int32_t* ids_sm = nullptr) {
   const int E = a.E, n = a.n, S = a.S;
   const int cap = n < E ? n : E;
   int* inU = reinterpret_cast<int*>(smem);
@@ -320,7 +322,7 @@ __device__ __noinline__ void resolve_block(const ResolveArgs& a, unsigned char* 
     __shared__ int s_done;
     __shared__ ResSmall s_small;
     if (tid < 32) {
-      const int done = resolve_small(a, &s_small);
+      const int done = resolve_small(a, &s_small, ids_sm);
       if (tid == 0) s_done = done;
     }
     __syncthreads();
@@ -342,7 +344,7 @@ __device__ __noinline__ void resolve_block(const ResolveArgs& a, unsigned char* 
   }
   __syncthreads();
   for (int i = tid; i < n; i += nt) {
-    const int e = resolve_id(a, i);
+    const int e = ids_sm ? ids_sm[i] : resolve_id(a, i);
     if (e < 0 || e >= E)
       s_bad = 1;
     else
@@ -707,7 +709,7 @@ __device__ __noinline__ void resolve_block(const ResolveArgs& a, unsigned char* 
   // 6. outputs
   if (!a.prefetch)
     for (int i = tid; i < n; i += nt) {
-      const int sl = slotOf[resolve_id(a, i)];
+      const int sl = slotOf[ids_sm ? ids_sm[i] : resolve_id(a, i)];
       a.slot_ids[i] = sl;
       if (a.slot_ids_sm) a.slot_ids_sm[i] = sl;
     }
