@@ -43,17 +43,20 @@ __global__ void __launch_bounds__(kResThreads, 1) resolve_kernel(const __grid_co
   }
   pdl_wait();               // ids (or the router logits) come from the previous kernel
   pdl_launch_dependents();  // the next call (fetch) may start its launch now
-  if (!TOPK) {
-    resolve_block(a, smem);
-    return;
-  }
   __shared__ int32_t s_ids[kResTopkMax];
-  const int warp = threadIdx.x >> 5;
-  if (warp < r.T)  // E <= 512: the register top-k (no shared scratch)
-    topk_any(r.logits + warp, nullptr, r.E, r.k, r.renorm, s_ids + warp * r.k, r.wts + warp * r.k, r.stride);
-  __syncthreads();
-  for (int i = threadIdx.x; i < r.T * r.k; i += blockDim.x) r.ids[i] = s_ids[i];
-  resolve_block(a, smem, s_ids);
+  const int32_t* ids_sm = nullptr;
+  if (TOPK) {
+    const int warp = threadIdx.x >> 5;
+    if (warp < r.T)  // E <= 512: the register top-k (no shared scratch)
+      topk_any(r.logits + warp, nullptr, r.E, r.k, r.renorm, s_ids + warp * r.k, r.wts + warp * r.k, r.stride);
+    __syncthreads();
+    for (int i = threadIdx.x; i < r.T * r.k; i += blockDim.x) r.ids[i] = s_ids[i];
+    ids_sm = s_ids;
+  }
+  // the small calls inline (the arguments read from the parameter space),
+  // the rest in resolve_block
+  if (a.n <= 32 && !a.prefetch && resolve_small_path(a, ids_sm)) return;
+  resolve_block(a, smem, ids_sm, false);
 }
 
 // Copy fetched expert blocks pool[fid] -> cache[slot] for i < *num_fetch.

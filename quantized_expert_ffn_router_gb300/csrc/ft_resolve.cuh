@@ -190,7 +190,7 @@ __device__ __forceinline__ int resolve_small(const ResolveArgs& a, ResSmall* sm,
 // The block: nf rounds of a block-wide argmin of (usage, slot) over the
 // slots that no hit owns and no earlier round took, which yields the nf
 // victims already in (usage asc, slot asc) order.  Every thread calls it.
-__device__ void resolve_small_victims(const ResolveArgs& a, ResSmall* sm) {
+__device__ __forceinline__ void resolve_small_victims(const ResolveArgs& a, ResSmall* sm) {
   __shared__ long long s_vu[32];
   __shared__ int s_vs[32];
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = (nt + 31) >> 5;
@@ -250,7 +250,7 @@ __device__ void resolve_small_victims(const ResolveArgs& a, ResSmall* sm) {
 // The warp: evict the victims' owners, install the fetched experts, the
 // usage of hit and fetched slots, the recency of every distinct expert,
 // then the outputs.
-__device__ void resolve_small_finish(const ResolveArgs& a, const ResSmall* sm) {
+__device__ __forceinline__ void resolve_small_finish(const ResolveArgs& a, const ResSmall* sm) {
   const int lane = threadIdx.x & 31;
   const int n = a.n, base = a.layer * a.E, nf = sm->nf;
   const int64_t now = sm->now;
@@ -285,13 +285,36 @@ __device__ void resolve_small_finish(const ResolveArgs& a, const ResSmall* sm) {
     *a.step = now + 1;
   }
 }
+// The small path (n <= 32, not a prefetch) as a whole, for a kernel to inline
+// so that it reads its arguments straight from the parameter space (through
+// the reference of the non-inlined resolve_block every argument read is a
+// generic load).  Every thread of the block calls it; returns (block-uniform)
+// true when the call is done, false for resolve_block(..., small = false).
+__device__ __forceinline__ bool resolve_small_path(const ResolveArgs& a, const int32_t* ids_sm) {
+  __shared__ int s_done;
+  __shared__ ResSmall s_small;
+  if (threadIdx.x < 32) {
+    const int done = resolve_small(a, &s_small, ids_sm);
+    if (threadIdx.x == 0) s_done = done;
+  }
+  __syncthreads();
+  const int done = s_done;
+  if (done == 2) {
+    resolve_small_victims(a, &s_small);
+    if (threadIdx.x < 32) resolve_small_finish(a, &s_small);
+  }
+  return done != 0;
+}
+
 // The whole resolve call by one CTA (any block size; every thread calls it).
 // smem: the dynamic shared memory resolve_prepare asked for.  ids must be
 // readable by the CTA (written by an earlier grid, or by this CTA before a
 // __syncthreads).
 // ids_sm, when not null, is a shared-memory copy of ids [n] that this CTA
-// wrote before a __syncthreads, read instead of a.ids / a.ids_sm.
-__device__ __noinline__ void resolve_block(const ResolveArgs& a, unsigned char* smem, const int32_t* ids_sm = nullptr) {
+// wrote before a __syncthreads, read instead of a.ids / a.ids_sm.  small:
+// false when the caller has run the small path (resolve_small_path) already.
+__device__ __noinline__ void resolve_block(const ResolveArgs& a, unsigned char* smem, const int32_t* ids_sm = nullptr,
+                                          bool small = true) {
   const int E = a.E, n = a.n, S = a.S;
   const int cap = n < E ? n : E;
   int* inU = reinterpret_cast<int*>(smem);
@@ -318,7 +341,7 @@ __device__ __noinline__ void resolve_block(const ResolveArgs& a, unsigned char* 
   const int nt = blockDim.x;
   const int base = a.layer * E;
 
-  if (n <= 32 && !a.prefetch) {
+  if (small && n <= 32 && !a.prefetch) {
     __shared__ int s_done;
     __shared__ ResSmall s_small;
     if (tid < 32) {
