@@ -54,9 +54,15 @@ __global__ void __launch_bounds__(kResThreads, 1) resolve_kernel(const __grid_co
     ids_sm = s_ids;
   }
   // the small calls inline (the arguments read from the parameter space),
-  // the rest in resolve_block
+  // the rest in resolve_block, which reads its arguments through a reference:
+  // give it a shared-memory copy (one word per thread), not the parameters
   if (a.n <= 32 && !a.prefetch && resolve_small_path(a, ids_sm)) return;
-  resolve_block(a, smem, ids_sm, false);
+  __shared__ __align__(16) ResolveArgs s_args;
+  static_assert(sizeof(ResolveArgs) % 4 == 0, "copied a word at a time");
+  if (threadIdx.x < sizeof(ResolveArgs) / 4)
+    reinterpret_cast<uint32_t*>(&s_args)[threadIdx.x] = reinterpret_cast<const uint32_t*>(&a)[threadIdx.x];
+  __syncthreads();
+  resolve_block(s_args, smem, ids_sm, false);
 }
 
 // Copy fetched expert blocks pool[fid] -> cache[slot] for i < *num_fetch.
