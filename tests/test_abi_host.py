@@ -70,6 +70,14 @@ def test_host_validation_without_gpu(ft):
     assert lib.ft_moe_resolve_slots(*args(2, 100, 4)) == ft.FT_ERR_INVALID
     assert lib.ft_moe_resolve_slots(*args(0, -1, 4)) == ft.FT_ERR_INVALID
     assert lib.ft_moe_resolve_slots(*args(0, 100, 1)) == ft.FT_ERR_INVALID
+    # route + resolve: on a one-kernel shape (T*k <= 32, E <= 512, the state's E) a bad
+    # resolve argument (a short fetch list) is refused before anything runs; on a
+    # two-call shape (k = 0 is outside the one-kernel limits) the route's check refuses
+    rr = lambda T, k, ml: (dummy, T, 64, dummy, 8, k, 0, dummy, dummy, dummy, 1 << 20, ctypes.byref(st), 0, 100,
+                           dummy, dummy, dummy, dummy, ml, None, None)
+    assert lib.ft_moe_route_resolve(*rr(1, 2, 1)) == ft.FT_ERR_INVALID
+    assert "max_list" in ft.load().ft_last_error().decode()
+    assert lib.ft_moe_route_resolve(*rr(20, 0, 64)) == ft.FT_ERR_INVALID
     # prefetch: negative cap, layer out of range, short fetch list
     pargs = lambda layer, cap, ml: (ctypes.byref(st), layer, dummy, 1, 2, cap, dummy, dummy, dummy, ml,
                                     None, None)
