@@ -30,8 +30,10 @@ struct RouteTopk {
   float* wts;
 };
 
-// The arguments stay in the parameter space (__grid_constant__): resolve_block
-// reads them there by reference instead of from a local copy.
+// The arguments stay in the parameter space (__grid_constant__, no local
+// copy): the small path, inlined here, reads them as parameter loads, and the
+// block-wide body (not inlined, arguments by reference) gets a shared-memory
+// copy.
 template <bool TOPK>
 __global__ void __launch_bounds__(kResThreads, 1) resolve_kernel(const __grid_constant__ ResolveArgs a,
                                                                  const __grid_constant__ RouteTopk r) {
